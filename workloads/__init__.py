@@ -1,0 +1,261 @@
+"""Seeded synthetic inputs for paged-KV attention (shared by the oracle side and the CUDA side).
+
+This module only draws random numbers and lays out a script of block-pool
+operations; it holds none of the method's arithmetic (no slot computation, no
+attention, no copy-on-write logic).  Each side executes the script with its
+own pool and cache code.
+
+A workload is:
+  * shapes: dtype ('f32' or 'bf16'), Hq, Hkv, head_dim D, block_size
+  * a pool: ``num_blocks`` and ``free_order`` (a seeded permutation; the first
+    entry is handed out first)
+  * ``setup``: operations run before the measured step
+        ("add",  seq, n, row)   new sequence whose n tokens take K/V rows row..row+n-1
+        ("grow", seq, n, row)   append n tokens one at a time (rows row..row+n-1)
+        ("fork", parent, child) share all of parent's blocks
+        ("free", seq)
+  * ``step``: the same kinds of operation for this step's new tokens (their K/V
+    are appended before attention)
+  * ``batch``: [(seq, qlen)] in query-row order; qlen = 1 is a decode row, a
+    larger qlen is a prefill chunk (the sequence's last qlen tokens)
+  * ``q`` [Tq, Hq, D] and the token value rows ``k_rows``/``v_rows`` [N, Hkv, D]
+    in the storage dtype (float32, or bf16 bit patterns as uint16).
+
+Context lengths quoted for a configuration are the attended lengths: they count
+the step's own token(s), which are appended first.
+"""
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+CONFIG_NAMES = {
+    1: "tiny-decode-f32",
+    2: "llama2-7b-decode",
+    3: "llama3-8b-gqa-decode",
+    4: "splitfuse-2048",
+    5: "prefix-sharing-longctx",
+}
+
+
+@dataclass
+class Workload:
+    name: str
+    dtype: str
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    free_order: np.ndarray
+    setup: list
+    step: list
+    batch: list
+    q: np.ndarray
+    k_rows: np.ndarray
+    v_rows: np.ndarray
+    notes: dict = field(default_factory=dict)
+
+    @property
+    def elem_bytes(self):
+        return 4 if self.dtype == "f32" else 2
+
+    @property
+    def num_tokens_q(self):
+        return sum(q for _, q in self.batch)
+
+
+def _bf16_bits(x32):
+    """Round float32 to bf16 (round-to-nearest-even) with torch; return uint16 bits."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(x32, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _values(rng, shape, dtype, scale):
+    """Normal(0, 1) * scale in the storage dtype, drawn in bounded chunks."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.float32 if dtype == "f32" else np.uint16)
+    chunk = 1 << 24
+    for a in range(0, n, chunk):
+        b = min(n, a + chunk)
+        x = rng.standard_normal(b - a, dtype=np.float32)
+        if scale != 1.0:
+            x *= np.float32(scale)
+        out[a:b] = x if dtype == "f32" else _bf16_bits(x)
+    return out.reshape(shape)
+
+
+def _blocks(n, bs):
+    return -(-n // bs)
+
+
+def _decode_workload(name, rng, dtype, hq, hkv, d, bs, ctx, scale, pool=None, slack=0.1):
+    """One query token per sequence; sequence s holds ctx[s]-1 cached tokens before the step."""
+    ctx = [int(c) for c in ctx]
+    need = sum(_blocks(c, bs) for c in ctx)
+    nb = pool if pool is not None else int(np.ceil(need * (1.0 + slack)))
+    free_order = rng.permutation(nb).astype(np.int32)
+    setup, step, row = [], [], 0
+    for s, c in enumerate(ctx):
+        if c - 1 > 0:
+            setup.append(("add", s, c - 1, row))
+            row += c - 1
+    for s, c in enumerate(ctx):
+        if c - 1 > 0:
+            step.append(("grow", s, 1, row))
+        else:
+            step.append(("add", s, 1, row))
+        row += 1
+    k_rows = _values(rng, (row, hkv, d), dtype, scale)
+    v_rows = _values(rng, (row, hkv, d), dtype, scale)
+    q = _values(rng, (len(ctx), hq, d), dtype, scale)
+    batch = [(s, 1) for s in range(len(ctx))]
+    return Workload(name, dtype, hq, hkv, d, bs, nb, free_order, setup, step, batch, q,
+                    k_rows, v_rows, notes={"context_lens": ctx})
+
+
+def config1(seed=0):
+    """Tiny decode: fp32, 4 seqs, 8/8 heads, D=64, bs=16, ctx {17,64,131,200}, pool of 64."""
+    rng = np.random.default_rng(seed)
+    return _decode_workload(CONFIG_NAMES[1], rng, "f32", 8, 8, 64, 16, [17, 64, 131, 200],
+                            1.0, pool=64)
+
+
+def config2(seed=0, batch=64):
+    """Llama-2-7B-shaped decode: bf16, 32/32 heads, D=128, bs=16, ctx ~ U[512, 4096]."""
+    rng = np.random.default_rng(seed)
+    ctx = rng.integers(512, 4096, size=batch, endpoint=True)
+    return _decode_workload(CONFIG_NAMES[2], rng, "bf16", 32, 32, 128, 16, ctx, 0.5)
+
+
+def config3(seed=0, batch=256):
+    """Llama-3-8B-shaped GQA decode: bf16, 32/8 heads, ctx log-uniform in [1024, 8192]."""
+    rng = np.random.default_rng(seed)
+    ctx = np.rint(np.exp(rng.uniform(np.log(1024), np.log(8192), size=batch))).astype(int)
+    return _decode_workload(CONFIG_NAMES[3], rng, "bf16", 32, 8, 128, 16, ctx, 0.5)
+
+
+def config4(seed=0, n_decode=512, chunk=512, prefixes=(0, 1024, 3072)):
+    """SplitFuse mixed batch: 3 prefill chunks of 512 over cached prefixes 0/1024/3072
+    plus 512 decode sequences with ctx ~ U[256, 4096]; 2048 query tokens in all."""
+    rng = np.random.default_rng(seed)
+    hq, hkv, d, bs = 32, 8, 128, 16
+    dec_ctx = [int(c) for c in rng.integers(256, 4096, size=n_decode, endpoint=True)]
+    chunk_ctx = [p + chunk for p in prefixes]
+    need = sum(_blocks(c, bs) for c in chunk_ctx + dec_ctx)
+    nb = int(np.ceil(need * 1.1))
+    free_order = rng.permutation(nb).astype(np.int32)
+    setup, step, row = [], [], 0
+    n_chunk = len(prefixes)
+    for s, p in enumerate(prefixes):
+        if p > 0:
+            setup.append(("add", s, p, row))
+            row += p
+    for i, c in enumerate(dec_ctx):
+        setup.append(("add", n_chunk + i, c - 1, row))
+        row += c - 1
+    for s, p in enumerate(prefixes):
+        step.append(("grow", s, chunk, row) if p > 0 else ("add", s, chunk, row))
+        row += chunk
+    for i in range(n_decode):
+        step.append(("grow", n_chunk + i, 1, row))
+        row += 1
+    k_rows = _values(rng, (row, hkv, d), "bf16", 0.5)
+    v_rows = _values(rng, (row, hkv, d), "bf16", 0.5)
+    batch = [(s, chunk) for s in range(n_chunk)] + [(n_chunk + i, 1) for i in range(n_decode)]
+    q = _values(rng, (sum(x for _, x in batch), hq, d), "bf16", 0.5)
+    return Workload(CONFIG_NAMES[4], "bf16", hq, hkv, d, bs, nb, free_order, setup, step, batch,
+                    q, k_rows, v_rows,
+                    notes={"context_lens": chunk_ctx + dec_ctx, "prefixes": list(prefixes)})
+
+
+def config5(seed=0, groups=8, branches=8, prompt=3000, max_private=200, n_long=4,
+            long_ctx=32768):
+    """Parallel sampling + long context: bf16, 64/8 heads.  Each group's prompt is
+    forked into ``branches`` branches that share its blocks; the prompt sequence is
+    then freed; each branch generates U{1..max_private} private tokens, the last of
+    which is this step's token.  Plus ``n_long`` sequences at ``long_ctx``."""
+    rng = np.random.default_rng(seed)
+    hq, hkv, d, bs = 64, 8, 128, 16
+    priv = rng.integers(1, max_private, size=(groups, branches), endpoint=True)
+    # pool: prompts + every branch's private blocks + one copy per branch + long seqs
+    need = groups * _blocks(prompt, bs)
+    need += sum(_blocks(int(p) + bs, bs) + 1 for p in priv.ravel())
+    need += n_long * _blocks(long_ctx, bs)
+    nb = int(np.ceil(need * 1.1))
+    free_order = rng.permutation(nb).astype(np.int32)
+    setup, step, batch, row = [], [], [], 0
+    ctx = []
+    sid = 0
+    branch_ids = []
+    for gi in range(groups):
+        parent = sid
+        sid += 1
+        setup.append(("add", parent, prompt, row))
+        row += prompt
+        kids = []
+        for _ in range(branches):
+            setup.append(("fork", parent, sid))
+            kids.append(sid)
+            sid += 1
+        setup.append(("free", parent))
+        for bi, kid in enumerate(kids):
+            n = int(priv[gi, bi])
+            if n > 1:
+                setup.append(("grow", kid, n - 1, row))
+                row += n - 1
+            branch_ids.append((kid, n))
+    for kid, n in branch_ids:
+        step.append(("grow", kid, 1, row))
+        row += 1
+        batch.append((kid, 1))
+        ctx.append(prompt + n)
+    for _ in range(n_long):
+        setup.append(("add", sid, long_ctx - 1, row))
+        row += long_ctx - 1
+        step.append(("grow", sid, 1, row))
+        row += 1
+        batch.append((sid, 1))
+        ctx.append(long_ctx)
+        sid += 1
+    k_rows = _values(rng, (row, hkv, d), "bf16", 0.5)
+    v_rows = _values(rng, (row, hkv, d), "bf16", 0.5)
+    q = _values(rng, (len(batch), hq, d), "bf16", 0.5)
+    return Workload(CONFIG_NAMES[5], "bf16", hq, hkv, d, bs, nb, free_order, setup, step, batch,
+                    q, k_rows, v_rows, notes={"context_lens": ctx})
+
+
+def make(config, seed=0, **kw):
+    return {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}[config](seed=seed, **kw)
+
+
+def random_decode(seed, dtype, hq, hkv, d, bs, ctx, scale=1.0, pool=None, slack=0.1):
+    """A decode workload with explicit context lengths (for edge-case tests)."""
+    rng = np.random.default_rng(seed)
+    return _decode_workload(f"decode-{dtype}-{hq}x{hkv}x{d}", rng, dtype, hq, hkv, d, bs, ctx,
+                            scale, pool=pool, slack=slack)
+
+
+def random_varlen(seed, dtype, hq, hkv, d, bs, spans, scale=1.0, slack=0.1):
+    """A mixed batch from explicit (cached_prefix, qlen) spans (for edge-case tests)."""
+    rng = np.random.default_rng(seed)
+    need = sum(_blocks(p + q, bs) for p, q in spans)
+    nb = int(np.ceil(need * (1.0 + slack))) + 1
+    free_order = rng.permutation(nb).astype(np.int32)
+    setup, step, row = [], [], 0
+    for s, (p, _) in enumerate(spans):
+        if p > 0:
+            setup.append(("add", s, p, row))
+            row += p
+    for s, (p, qn) in enumerate(spans):
+        step.append(("grow", s, qn, row) if p > 0 else ("add", s, qn, row))
+        row += qn
+    k_rows = _values(rng, (row, hkv, d), dtype, scale)
+    v_rows = _values(rng, (row, hkv, d), dtype, scale)
+    batch = [(s, qn) for s, (_, qn) in enumerate(spans)]
+    q = _values(rng, (sum(qn for _, qn in spans), hq, d), dtype, scale)
+    return Workload(f"varlen-{dtype}", dtype, hq, hkv, d, bs, nb, free_order, setup, step, batch,
+                    q, k_rows, v_rows,
+                    notes={"context_lens": [p + qn for p, qn in spans]})
