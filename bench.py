@@ -1,0 +1,387 @@
+#!/usr/bin/env python
+"""Decode paged-attention benchmark on GB300 (one JSON line on stdout).
+
+A step is one pass of the hot path over one batch: copy-on-write block copies
+(if any), the slot-mapped append of the step's new K/V, and paged decode
+attention (planner, split kernel, merge) over the whole batch.  The default
+workload is the Llama-2-7B-shaped single-layer decode: bf16, 32 query heads =
+32 KV heads, head_dim 128, block_size 16, batch 64, context ~ U[512, 4096],
+values N(0,1) x 0.5, block tables from a seeded permutation of a pool 10%
+larger than needed.
+
+value    = algorithmic bytes of the step / device time of the step (inputs resident)
+e2e      = the same bytes / time of a step that also copies its inputs from pinned
+           host memory and reads the output back
+roofline = the decode attention call (planner + split + merge) against the
+           measured HBM copy bandwidth
+--impl reference runs the float64 CPU oracle on a bounded sample instead.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode paged-attn KV GB/s and % of GB300 HBM peak; mixed-batch tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------------------
+# algorithmic bytes (per step)
+# ----------------------------------------------------------------------------
+def attention_bytes(w, ctx):
+    """K and V bytes of every attended key + q in + out + block tables + lengths."""
+    es = w.elem_bytes
+    kv = sum(int(c) for c in ctx) * w.num_kv_heads * w.head_dim * es * 2
+    qo = len(ctx) * w.num_q_heads * w.head_dim * es * 2
+    tables = sum(math.ceil(int(c) / w.block_size) for c in ctx) * 4 + 4 * len(ctx)
+    return kv + qo + tables
+
+
+def append_bytes(w, n_tokens, n_pairs):
+    es = w.elem_bytes
+    row = w.num_kv_heads * w.head_dim * es
+    blk = row * w.block_size
+    return n_tokens * row * 2 * 2 + 8 * n_tokens + n_pairs * blk * 2 * 2 + 8 * n_pairs
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(kernel_src):
+    """DRAM bytes per launch recorded from an ncu capture, if the kernel is unchanged since."""
+    prof = os.path.join(ROOT, "profiles", "decode_attention_llama2_7b.md")
+    src = os.path.join(ROOT, "paged_kv_cache_51_gb300", "csrc", kernel_src)
+    try:
+        with open(src, "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()
+        vals = {}
+        with open(prof) as f:
+            for line in f:
+                if ":" in line and line.strip().startswith("- "):
+                    k, v = line.strip()[2:].split(":", 1)
+                    vals[k.strip()] = v.strip().strip("`")
+        if vals.get("kernel_source_sha256") == h:
+            return int(vals["dram_bytes_per_call"])
+    except Exception:
+        pass
+    return None
+
+
+# ----------------------------------------------------------------------------
+# clocks
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.proc = None
+        self.rows = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={index}", f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def summary(self, t0, t1):
+        if not self.rows:
+            return None
+
+        def ts(r):
+            try:
+                return time.mktime(time.strptime(r[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+            except Exception:
+                return None
+
+        during = [r for r in self.rows if ts(r) is not None and t0 - 1 <= ts(r) <= t1 + 1]
+        rows = during if len(during) >= 3 else self.rows
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "window": "timed" if rows is during else "run"}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle (reference arm and cpu_baseline)
+# ----------------------------------------------------------------------------
+def oracle_sample(config, n_seqs, seed=0):
+    """A bounded sample of the workload (its first sequences) ready for the oracle."""
+    import workloads
+    from oracle.run import OracleState
+
+    if config == 2:
+        w = workloads.config2(seed=seed, batch=n_seqs)
+    elif config == 3:
+        w = workloads.config3(seed=seed, batch=n_seqs)
+    else:
+        raise SystemExit("the CPU baseline covers decode configs 2 and 3")
+    st = OracleState(w)
+    st.run_setup()
+    st.run_step()
+    bt, ctx, _ = st.batch_metadata()
+    return w, st, bt, ctx
+
+
+def oracle_attention_once(w, st, bt, ctx):
+    from oracle import attention
+
+    return attention.decode(w.q, st.k_cache, st.v_cache, bt, ctx, w.block_size, w.dtype)
+
+
+def cpu_worker(config, n_seqs, seconds):
+    w, st, bt, ctx = oracle_sample(config, n_seqs)
+    nbytes = attention_bytes(w, ctx)
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        oracle_attention_once(w, st, bt, ctx)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    print(json.dumps({"value": nbytes * passes / el / 1e9, "unit": "GB/s", "seconds": el,
+                      "passes": passes, "seqs": n_seqs}))
+
+
+def cpu_baseline(config, seconds=10.0, n_seqs=4):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker",
+                        "--config", str(config), "--cpu-seqs", str(n_seqs),
+                        "--cpu-seconds", str(seconds)],
+                       capture_output=True, text=True, env=env, cwd=ROOT)
+    if r.returncode != 0:
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": f"failed: {r.stderr.strip()[-200:]}"}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": d["value"], "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": (f"first {n_seqs} sequences of the same workload (same generator), float64 "
+                       f"NumPy oracle attention repeated {d['passes']}x over {d['seconds']:.1f} s "
+                       f"on one host core")}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    n_seqs = 1
+    w, st, bt, ctx = oracle_sample(args.config, n_seqs)
+    nbytes = attention_bytes(w, ctx)
+    for _ in range(args.warmup):
+        oracle_attention_once(w, st, bt, ctx)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_attention_once(w, st, bt, ctx)
+    el = time.perf_counter() - t0
+    cores = 1 if os.environ.get("OPENBLAS_NUM_THREADS") == "1" else os.cpu_count()
+    value = nbytes * args.steps / el / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sample_seqs": n_seqs},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n_seqs} sequence(s) of {w.name} per step, float64 oracle"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+    return 0
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+def run_gpu(args):
+    import torch
+
+    import workloads
+    from paged_kv_cache_51_gb300 import _build
+
+    _build.build()
+    import paged_kv_cache_51_gb300 as pkv
+    from paged_kv_cache_51_gb300 import runner
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+
+    w = workloads.make(args.config, seed=rank)
+    dc, step = runner.prepare(w)
+    ctx_host = step.ctx.cpu().tolist()
+    attn_b = attention_bytes(w, ctx_host)
+    app_b = append_bytes(w, step.slot_mapping.numel(), step.pairs.shape[0])
+    step_bytes = attn_b + app_b
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    if pkv.device_error() != 0:
+        raise SystemExit("device error during warm-up")
+
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    a_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step.write_kv()
+        a_ev[i][0].record(stream)
+        step.attend()
+        a_ev[i][1].record(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if dist:
+        dist.barrier()
+    sampler.stop()
+    total_ms = ev0.elapsed_time(ev1)
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in a_ev)
+    if dist:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if pkv.device_error() != 0:
+        raise SystemExit("device error during the timed region")
+
+    # ---- end to end through host buffers ----
+    host_in = {name: getattr(step, name).cpu().pin_memory()
+               for name in ("q", "k_new", "v_new", "slot_mapping", "tables", "ctx", "pairs")}
+    host_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    k_e2e = max(3, min(args.steps, 200))
+
+    def e2e_step():
+        for name, t in host_in.items():
+            getattr(step, name).copy_(t, non_blocking=True)
+        step.run()
+        host_out.copy_(step.out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(k_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / k_e2e
+
+    ms_per_step = total_ms / args.steps
+    value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    achieved = attn_b / (attn_ms * 1e-3) / 1e9
+    launches_per_step = (1 if step.pairs.shape[0] else 0) + 1 + 2 + (
+        1 if math.ceil(step.max_ctx / 512) > 1 else 0)
+    clocks = sampler.summary(t_wall0, t_wall1)
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+    cpu = cpu_baseline(args.config) if world == 1 and not args.no_cpu else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {
+            "workload": w.name, "batch": len(w.batch), "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+            "block_size": w.block_size, "num_blocks": w.num_blocks,
+            "context_tokens": int(sum(ctx_host)), "max_context": int(step.max_ctx),
+            "step": "copy-on-write + append of the step's tokens + paged decode attention",
+            "l2": f"inputs larger than L2 (KV {attn_b / 1e9:.2f} GB read per step vs 129 MB L2)",
+            "parallelism": f"replicas x{world}",
+        },
+        "pct_hbm_peak": achieved / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": ncu_traffic("decode.cu"),
+                     "kernel": "paged_attention_decode (plan + split + merge)",
+                     "bytes_per_launch": attn_b, "ms_per_launch": attn_ms,
+                     "peak_kind": f"{peak_kind} hbm_gbs (burst copy)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-worker", action="store_true")
+    ap.add_argument("--cpu-seqs", type=int, default=4)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and not args.cpu_worker:
+        args.warmup = 3
+    if args.cpu_worker:
+        cpu_worker(args.config, args.cpu_seqs, args.cpu_seconds)
+        return 0
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

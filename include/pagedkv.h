@@ -1,0 +1,238 @@
+/*
+ * pagedkv.h -- C ABI of the paged KV-cache attention library (libpagedkv.so).
+ *
+ * The library implements the hot path of attention over a paged (blocked) KV
+ * cache on one GB300 (sm_103a): a host block pool with reference-counted,
+ * copy-on-write blocks; a slot-mapped K/V append; exact decode attention over
+ * non-contiguous blocks; and a ragged mixed batch in which prefill chunks
+ * attend causally to their cached prefix alongside decode tokens.
+ *
+ * Pages this follows (cited by title and section):
+ *   [Deploy]  "大模型部署.md" (AIGC-Interview-Book), §2.1 vLLM 框架技术详解:
+ *             3. 调度策略与显存块管理 (can_allocate, _allocate_sequence,
+ *             append_slots with copy-on-write), 4. PageAttention 内存管理技术详解;
+ *             §2.5 LMDeploy 2. TurboMind (split-K decoding);
+ *             §4.1 注意力机制计算优化 (1. FlashAttention, 4. MQA 与 GQA)
+ *   [Infra]   "【自用】AI infra相关", 一、推理两阶段 (decode appends K_t,V_t then
+ *             attends), 二、vLLM (block table, copy-on-write, free block list)
+ *   [FastGen] "DeepSpeed-FastGen 深度解析", §3.2 动态分割融合 (token budget)
+ *   [Ch15]    "第 15 章：推理引擎与部署", §15.1 算法详解 (online softmax),
+ *             §15.6 PagedAttention：分页 KV Cache, 两阶段与 Chunked Prefill
+ *
+ * Conventions for every function:
+ *   - Return an int status: PKV_OK (0) or a negative PKV_ERR_* code.  No
+ *     function aborts the process or throws across the ABI.
+ *   - Pointers documented "device" must point to memory of the current CUDA
+ *     device; pointers documented "host" to ordinary host memory.  The caller
+ *     owns all memory; no entry point allocates device memory.
+ *   - Device entry points only enqueue work on `stream` (a cudaStream_t passed
+ *     as void*, NULL = legacy default stream) and return without waiting.
+ *     Arguments that can be checked on the host are checked before anything
+ *     is launched (PKV_ERR_INVALID / PKV_ERR_UNSUPPORTED, nothing enqueued).
+ *     Values that live in device memory (block ids, slots, lengths) are
+ *     checked by the kernels: an offending access is skipped and a code is
+ *     recorded in the device error word (read it with pkv_device_error).
+ *   - Cache layout (fixed): K and V are separate pools, each
+ *     [num_blocks][num_kv_heads][block_size][head_dim], row-major, in the
+ *     cache dtype.  One (block, kv head) tile is contiguous.
+ *   - Query head h uses KV head h / (num_q_heads / num_kv_heads).
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define PKV_OK               0
+#define PKV_ERR_INVALID     -1  /* bad argument: null pointer, bad size, unknown sequence */
+#define PKV_ERR_NO_BLOCKS   -2  /* pool cannot serve the request now (LATER) */
+#define PKV_ERR_NEVER       -3  /* pool can never serve the request (NEVER) */
+#define PKV_ERR_UNSUPPORTED -4  /* shape / dtype the kernels do not implement */
+#define PKV_ERR_CUDA        -5  /* a CUDA runtime call or launch failed */
+#define PKV_ERR_WORKSPACE   -6  /* workspace null, misaligned or too small */
+#define PKV_ERR_HOST        -7  /* host memory allocation failed */
+
+/* ---- device error word codes (pkv_device_error) ------------------------ */
+#define PKV_DEV_OK               0
+#define PKV_DEV_BAD_BLOCK_ID     1  /* block table entry outside [0, num_blocks) */
+#define PKV_DEV_BAD_CONTEXT_LEN  2  /* context length < 1, > max_context_len, or < query length */
+#define PKV_DEV_BAD_SLOT         3  /* slot >= num_blocks * block_size */
+#define PKV_DEV_BAD_COPY_PAIR    4  /* copy pair block id outside the pool */
+#define PKV_DEV_BAD_QUERY_LAYOUT 5  /* query_start_loc not non-decreasing from 0 to num_query_tokens */
+#define PKV_DEV_WAIT_TIMEOUT     6  /* a pipeline wait exceeded its limit (internal fault) */
+#define PKV_DEV_TABLE_TOO_NARROW 7  /* context needs more blocks than max_blocks_per_seq */
+
+/* ---- data types -------------------------------------------------------- */
+#define PKV_F32  0
+#define PKV_BF16 1
+
+typedef struct pkv_cache_desc {
+    int32_t dtype;        /* PKV_F32 or PKV_BF16: cache, q, k, v and out share it */
+    int32_t num_blocks;   /* physical blocks in each of the K and V pools */
+    int32_t block_size;   /* tokens per block (the kernels implement 16) */
+    int32_t num_kv_heads;
+    int32_t num_q_heads;  /* multiple of num_kv_heads; group size 1, 2, 4 or 8 */
+    int32_t head_dim;     /* 64 or 128 */
+} pkv_cache_desc;
+
+/* ======================================================================== *
+ * Host block pool (metadata only; never touches device memory).
+ *
+ * Follows [Deploy §2.1 3.] and [Infra 二]: fixed-size physical blocks, a free
+ * block list, one block table per sequence, reference counts shared by forked
+ * sequences, copy-on-write of a shared last block, and admission with a
+ * watermark.  Readings where the pages are silent: the free list is a stack
+ * (the block freed last is handed out first); `free_order` lists the initial
+ * stack from the top; a sequence's blocks are released in table order.
+ * A pool object is not thread-safe.
+ * ======================================================================== */
+typedef struct pkv_pool pkv_pool;
+
+/* Create a pool of `num_blocks` blocks of `block_size` tokens.  `free_order`
+ * (host, optional, [num_blocks]) is a permutation of 0..num_blocks-1 whose
+ * first entry is handed out first; NULL means 0, 1, 2, ...  On success *out
+ * owns the pool (release with pkv_pool_destroy). */
+PKV_API int pkv_pool_create(int32_t num_blocks, int32_t block_size, int32_t watermark_blocks,
+                    const int32_t* free_order, pkv_pool** out);
+PKV_API int pkv_pool_destroy(pkv_pool* pool);
+PKV_API int pkv_pool_num_free(const pkv_pool* pool, int32_t* out);
+
+/* Admission of a new sequence of `num_tokens` tokens [Deploy §2.1 can_allocate]:
+ * PKV_ERR_NEVER if num_blocks - need < watermark, PKV_OK if
+ * free - need >= watermark, PKV_ERR_NO_BLOCKS (LATER) otherwise. */
+PKV_API int pkv_pool_can_allocate(const pkv_pool* pool, int32_t num_tokens);
+
+/* Add sequence `seq_id` with `num_tokens` prompt tokens: applies the admission
+ * rule above, then takes ceil(num_tokens / block_size) blocks with reference
+ * count 1.  `slots_out` (host, optional, [num_tokens]) receives the physical
+ * slot block * block_size + row of every token in order.  On any error the
+ * pool is unchanged. */
+PKV_API int pkv_seq_add(pkv_pool* pool, int64_t seq_id, int32_t num_tokens, int64_t* slots_out);
+
+/* New sequence `child` shares every block of `parent` (reference count + 1 each). */
+PKV_API int pkv_seq_fork(pkv_pool* pool, int64_t parent, int64_t child);
+
+/* Grow `seq_id` by one token [Deploy §2.1 append_slots].  A new block is taken
+ * only when the last block is full.  If the last block is shared (reference
+ * count > 1) a fresh block replaces it in this sequence's table and the pair
+ * (*cow_src, *cow_dst) tells the caller which whole block to copy (with
+ * pkv_copy_blocks) before writing the token; otherwise both are set to -1.
+ * *slot_out receives the token's slot.  PKV_ERR_NO_BLOCKS (pool unchanged)
+ * when a block is needed and none is free. */
+PKV_API int pkv_seq_append_slot(pkv_pool* pool, int64_t seq_id, int64_t* slot_out,
+                        int32_t* cow_src, int32_t* cow_dst);
+
+/* Drop one reference on each block of the sequence (table order); blocks that
+ * reach zero return to the free list. */
+PKV_API int pkv_seq_free(pkv_pool* pool, int64_t seq_id);
+
+PKV_API int pkv_seq_len(const pkv_pool* pool, int64_t seq_id, int32_t* len_out);
+PKV_API int pkv_block_ref_count(const pkv_pool* pool, int32_t block, int32_t* out);
+
+/* Export block tables and context lengths of `n` sequences (host buffers):
+ * tables_out [n][max_blocks] padded with -1, ctx_lens_out [n] (optional).
+ * PKV_ERR_INVALID if a table needs more than max_blocks entries. */
+PKV_API int pkv_block_tables(const pkv_pool* pool, const int64_t* seq_ids, int32_t n,
+                     int32_t max_blocks, int32_t* tables_out, int32_t* ctx_lens_out);
+
+/* ======================================================================== *
+ * Device entry points.
+ * ======================================================================== */
+
+/* Copy-on-write block copies [Deploy §2.1 append_slots "copy the tokens";
+ * Infra 二 copy-on-write]: for each pair i, K and V block pairs[2i+1] become
+ * byte-for-byte copies of block pairs[2i] (all heads, all rows).
+ * block_pairs: device int32 [num_pairs][2] (src, dst).  Destinations must be
+ * distinct and no destination may also be a source (pairs run in parallel).
+ * num_pairs == 0 is a no-op. */
+PKV_API int pkv_copy_blocks(const int32_t* block_pairs, int32_t num_pairs, void* k_cache, void* v_cache,
+                    const pkv_cache_desc* desc, void* stream);
+
+/* Append [Infra 一、2 解码 (K_t, V_t written into the cache); Deploy §2.1 (the
+ * block manager plans slots, the cache engine writes them)]:
+ *   cache[slot / block_size][h][slot % block_size][:] = x[t][h][:]
+ * for K and V and every kv head h.  k, v: device [num_tokens][num_kv_heads]
+ * [head_dim] in the cache dtype (a bit copy: no conversion).  slot_mapping:
+ * device int64 [num_tokens]; a negative slot skips that token (padding); slots
+ * must be distinct.  num_tokens == 0 is a no-op. */
+PKV_API int paged_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int32_t num_tokens,
+                    void* k_cache, void* v_cache, const pkv_cache_desc* desc, void* stream);
+
+/* Bytes of workspace paged_attention_decode needs for `num_seqs` sequences
+ * whose context lengths are at most `max_context_len` (0 on bad arguments). */
+PKV_API size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs,
+                                  int32_t max_context_len);
+
+/* Decode attention, one query token per sequence [Ch15 §15.1 (exact softmax
+ * computed with the online m / l / alpha recurrence); Ch15 §15.6 (block table
+ * lookup); Deploy §4.1 4. (GQA: a KV head is read once for its whole query
+ * group); Deploy §2.5 (split-K decoding)]:
+ *   out[s][h] = softmax(q[s][h] . K_s^T * scale) V_s
+ * over keys 0 .. context_lens[s]-1 of sequence s, where K_s/V_s are gathered
+ * through block_tables[s].  context_lens counts the query's own token, which
+ * must already be appended.
+ *   out, q:        device [num_seqs][num_q_heads][head_dim] (cache dtype)
+ *   block_tables:  device int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens:  device int32 [num_seqs], each in [1, max_context_len]
+ *   scale:         usually 1/sqrt(head_dim)
+ *   workspace:     device, >= pkv_decode_workspace_bytes(...), 256-byte aligned;
+ *                  holds split partials; must not be shared by concurrent calls.
+ * Long contexts are split into fixed spans of 512 tokens whose partial
+ * (max, sum, output) states are merged in a second kernel; the split depends
+ * only on the context length, so a sequence's result does not depend on the
+ * rest of the batch. */
+PKV_API int paged_attention_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                           const pkv_cache_desc* desc, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens,
+                           int32_t num_seqs, int32_t max_context_len, float scale,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace paged_attention_varlen needs. */
+PKV_API size_t pkv_varlen_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs,
+                                  int32_t num_query_tokens, int32_t max_query_len,
+                                  int32_t max_context_len);
+
+/* Ragged mixed batch [FastGen §3.2 动态分割融合; Ch15 §15.6 两阶段与 Chunked
+ * Prefill]: sequence s owns query rows query_start_loc[s] .. query_start_loc[s+1]-1
+ * (qlen_s rows, possibly 0).  Those rows are the sequence's last qlen_s
+ * positions, whose K/V must already be appended; row i attends causally to
+ * keys 0 .. context_lens[s] - qlen_s + i.  Rows with qlen_s == 1 take the
+ * decode path; longer spans (prefill chunks over a cached prefix) take the
+ * tensor-core prefill path.
+ *   out, q:           device [num_query_tokens][num_q_heads][head_dim]
+ *   query_start_loc:  device int32 [num_seqs + 1], 0 .. num_query_tokens
+ *   context_lens:     device int32 [num_seqs], >= qlen_s, <= max_context_len
+ *   max_query_len:    host upper bound of qlen_s
+ * Other arguments as for paged_attention_decode. */
+PKV_API int paged_attention_varlen(void* out, const void* q, const void* k_cache, const void* v_cache,
+                           const pkv_cache_desc* desc, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* query_start_loc,
+                           const int32_t* context_lens, int32_t num_seqs,
+                           int32_t num_query_tokens, int32_t max_query_len,
+                           int32_t max_context_len, float scale, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* Read the current device's error word into *code_out (PKV_DEV_* code of the
+ * first fault recorded since the last clear) and, if `clear` is non-zero,
+ * reset it.  Synchronizes the device. */
+PKV_API int pkv_device_error(int32_t* code_out, int32_t clear);
+
+/* Static description of a status code (never NULL). */
+PKV_API const char* pkv_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

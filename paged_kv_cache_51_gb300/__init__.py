@@ -1,0 +1,319 @@
+"""Paged KV-cache attention for GB300 (sm_103a): thin Python binding of libpagedkv.so.
+
+Every function here only marshals arguments (tensor data pointers, sizes and
+the current CUDA stream) into the C ABI declared in include/pagedkv.h; all work
+runs in the library's CUDA kernels or its C++ block pool.  There is no fallback:
+if the library is missing or was built for another machine, calls raise.
+
+PyTorch supplies device memory and streams only.
+"""
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
+
+PKV_OK = 0
+PKV_ERR_INVALID = -1
+PKV_ERR_NO_BLOCKS = -2
+PKV_ERR_NEVER = -3
+PKV_ERR_UNSUPPORTED = -4
+PKV_ERR_CUDA = -5
+PKV_ERR_WORKSPACE = -6
+PKV_ERR_HOST = -7
+
+PKV_F32 = 0
+PKV_BF16 = 1
+
+DEVICE_ERRORS = {
+    0: "ok", 1: "bad block id", 2: "bad context length", 3: "bad slot", 4: "bad copy pair",
+    5: "bad query layout", 6: "pipeline wait timeout", 7: "block table too narrow",
+}
+
+# every symbol the header declares (checked by the tests)
+EXPORTS = (
+    "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_num_free", "pkv_pool_can_allocate",
+    "pkv_seq_add", "pkv_seq_fork", "pkv_seq_append_slot", "pkv_seq_free", "pkv_seq_len",
+    "pkv_block_ref_count", "pkv_block_tables", "pkv_copy_blocks", "paged_kv_append",
+    "pkv_decode_workspace_bytes", "paged_attention_decode", "pkv_varlen_workspace_bytes",
+    "paged_attention_varlen", "pkv_device_error", "pkv_status_string",
+)
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("num_q_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib():
+    """Load libpagedkv.so (built by paged_kv_cache_51_gb300._build.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: run paged_kv_cache_51_gb300._build.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    i32, i64, p, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+    P = ctypes.POINTER
+    sig = {
+        "pkv_pool_create": (ctypes.c_int, [i32, i32, i32, p, P(p)]),
+        "pkv_pool_destroy": (ctypes.c_int, [p]),
+        "pkv_pool_num_free": (ctypes.c_int, [p, P(i32)]),
+        "pkv_pool_can_allocate": (ctypes.c_int, [p, i32]),
+        "pkv_seq_add": (ctypes.c_int, [p, i64, i32, p]),
+        "pkv_seq_fork": (ctypes.c_int, [p, i64, i64]),
+        "pkv_seq_append_slot": (ctypes.c_int, [p, i64, P(i64), P(i32), P(i32)]),
+        "pkv_seq_free": (ctypes.c_int, [p, i64]),
+        "pkv_seq_len": (ctypes.c_int, [p, i64, P(i32)]),
+        "pkv_block_ref_count": (ctypes.c_int, [p, i32, P(i32)]),
+        "pkv_block_tables": (ctypes.c_int, [p, p, i32, i32, p, p]),
+        "pkv_copy_blocks": (ctypes.c_int, [p, i32, p, p, P(CacheDesc), p]),
+        "paged_kv_append": (ctypes.c_int, [p, p, p, i32, p, p, P(CacheDesc), p]),
+        "pkv_decode_workspace_bytes": (sz, [P(CacheDesc), i32, i32]),
+        "paged_attention_decode": (ctypes.c_int, [p, p, p, p, P(CacheDesc), p, i32, p, i32, i32,
+                                                  ctypes.c_float, p, sz, p]),
+        "pkv_varlen_workspace_bytes": (sz, [P(CacheDesc), i32, i32, i32, i32]),
+        "paged_attention_varlen": (ctypes.c_int, [p, p, p, p, P(CacheDesc), p, i32, p, p, i32,
+                                                  i32, i32, i32, ctypes.c_float, p, sz, p]),
+        "pkv_device_error": (ctypes.c_int, [P(i32), i32]),
+        "pkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = L
+    return L
+
+
+def status_string(status):
+    try:
+        return lib().pkv_status_string(status).decode()
+    except Exception:
+        return "status"
+
+
+def _check(status, what):
+    if status != PKV_OK:
+        raise PagedKVError(status, what)
+
+
+# ----------------------------------------------------------------------------
+# host block pool
+# ----------------------------------------------------------------------------
+class BlockPool:
+    """Host block pool (C++): ref-counted blocks, block tables, copy-on-write."""
+
+    def __init__(self, num_blocks, block_size, watermark_blocks=0, free_order=None):
+        self._h = ctypes.c_void_p()
+        arr = None
+        if free_order is not None:
+            arr = (ctypes.c_int32 * num_blocks)(*[int(b) for b in free_order])
+        _check(lib().pkv_pool_create(num_blocks, block_size, watermark_blocks, arr,
+                                     ctypes.byref(self._h)), "pkv_pool_create")
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def close(self):
+        if self._h:
+            lib().pkv_pool_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def num_free(self):
+        out = ctypes.c_int32()
+        _check(lib().pkv_pool_num_free(self._h, ctypes.byref(out)), "pkv_pool_num_free")
+        return out.value
+
+    def can_allocate(self, num_tokens):
+        """PKV_OK, PKV_ERR_NO_BLOCKS (LATER) or PKV_ERR_NEVER."""
+        return lib().pkv_pool_can_allocate(self._h, num_tokens)
+
+    def add(self, seq_id, num_tokens):
+        """Returns the slots of the prompt's tokens (list of int)."""
+        slots = (ctypes.c_int64 * num_tokens)()
+        _check(lib().pkv_seq_add(self._h, seq_id, num_tokens, slots), "pkv_seq_add")
+        return list(slots)
+
+    def add_status(self, seq_id, num_tokens):
+        slots = (ctypes.c_int64 * max(num_tokens, 1))()
+        st = lib().pkv_seq_add(self._h, seq_id, num_tokens, slots)
+        return st, (list(slots)[:num_tokens] if st == PKV_OK else None)
+
+    def fork(self, parent, child):
+        _check(lib().pkv_seq_fork(self._h, parent, child), "pkv_seq_fork")
+
+    def append_slot(self, seq_id):
+        """Returns (slot, cow) with cow = (src, dst) or None."""
+        slot, src, dst = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+        _check(lib().pkv_seq_append_slot(self._h, seq_id, ctypes.byref(slot), ctypes.byref(src),
+                                         ctypes.byref(dst)), "pkv_seq_append_slot")
+        return slot.value, ((src.value, dst.value) if src.value >= 0 else None)
+
+    def append_slot_status(self, seq_id):
+        slot, src, dst = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+        st = lib().pkv_seq_append_slot(self._h, seq_id, ctypes.byref(slot), ctypes.byref(src),
+                                       ctypes.byref(dst))
+        return st, slot.value, ((src.value, dst.value) if st == PKV_OK and src.value >= 0 else None)
+
+    def free(self, seq_id):
+        _check(lib().pkv_seq_free(self._h, seq_id), "pkv_seq_free")
+
+    def seq_len(self, seq_id):
+        out = ctypes.c_int32()
+        _check(lib().pkv_seq_len(self._h, seq_id, ctypes.byref(out)), "pkv_seq_len")
+        return out.value
+
+    def ref_count(self, block):
+        out = ctypes.c_int32()
+        _check(lib().pkv_block_ref_count(self._h, block, ctypes.byref(out)), "pkv_block_ref_count")
+        return out.value
+
+    def block_tables(self, seq_ids, max_blocks):
+        """Returns (tables int32 tensor [n, max_blocks] padded with -1, ctx int32 tensor [n])."""
+        n = len(seq_ids)
+        ids = torch.tensor(list(seq_ids), dtype=torch.int64)
+        tables = torch.empty((n, max_blocks), dtype=torch.int32)
+        ctx = torch.empty(n, dtype=torch.int32)
+        _check(lib().pkv_block_tables(self._h, ids.data_ptr(), n, max_blocks, tables.data_ptr(),
+                                      ctx.data_ptr()), "pkv_block_tables")
+        return tables, ctx
+
+
+# ----------------------------------------------------------------------------
+# device entry points
+# ----------------------------------------------------------------------------
+_TORCH_DTYPE = {PKV_F32: torch.float32, PKV_BF16: torch.bfloat16}
+
+
+def cache_desc(k_cache, num_q_heads):
+    """Descriptor of a cache tensor [num_blocks, num_kv_heads, block_size, head_dim]."""
+    nb, hkv, bs, d = k_cache.shape
+    dt = {torch.float32: PKV_F32, torch.bfloat16: PKV_BF16}.get(k_cache.dtype)
+    if dt is None:
+        raise TypeError("cache dtype must be float32 or bfloat16")
+    return CacheDesc(dt, nb, bs, hkv, num_q_heads, d)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _need(t, dtype, name):
+    if not t.is_cuda or not t.is_contiguous() or t.dtype != dtype:
+        raise TypeError(f"{name} must be a contiguous CUDA {dtype} tensor")
+
+
+def pkv_copy_blocks(block_pairs, k_cache, v_cache, desc, stream=None):
+    """block_pairs: CUDA int32 [n, 2] (src, dst)."""
+    n = block_pairs.shape[0] if block_pairs is not None else 0
+    if n == 0:
+        return
+    _need(block_pairs, torch.int32, "block_pairs")
+    _check(lib().pkv_copy_blocks(_ptr(block_pairs), n, _ptr(k_cache), _ptr(v_cache),
+                                 ctypes.byref(desc), _stream(stream)), "pkv_copy_blocks")
+
+
+def paged_kv_append(k, v, slot_mapping, k_cache, v_cache, desc, stream=None):
+    """k, v: CUDA [T, Hkv, D] in the cache dtype; slot_mapping: CUDA int64 [T]."""
+    T = k.shape[0]
+    dt = _TORCH_DTYPE[desc.dtype]
+    for t, nm in ((k, "k"), (v, "v"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, dt, nm)
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    _check(lib().paged_kv_append(_ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache),
+                                 _ptr(v_cache), ctypes.byref(desc), _stream(stream)),
+           "paged_kv_append")
+
+
+def decode_workspace_bytes(desc, num_seqs, max_context_len):
+    return int(lib().pkv_decode_workspace_bytes(ctypes.byref(desc), num_seqs, max_context_len))
+
+
+def varlen_workspace_bytes(desc, num_seqs, num_query_tokens, max_query_len, max_context_len):
+    return int(lib().pkv_varlen_workspace_bytes(ctypes.byref(desc), num_seqs, num_query_tokens,
+                                                max_query_len, max_context_len))
+
+
+def workspace(nbytes, device=None):
+    """A workspace buffer (torch allocations are 256-byte aligned)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def paged_attention_decode(out, q, k_cache, v_cache, desc, block_tables, context_lens,
+                           max_context_len, scale=None, ws=None, stream=None):
+    """out, q: CUDA [S, Hq, D]; block_tables int32 [S, W]; context_lens int32 [S]."""
+    S = q.shape[0]
+    dt = _TORCH_DTYPE[desc.dtype]
+    for t, nm in ((out, "out"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, dt, nm)
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    if scale is None:
+        scale = 1.0 / math.sqrt(desc.head_dim)
+    if ws is None:
+        ws = workspace(decode_workspace_bytes(desc, S, max_context_len), q.device)
+    _check(lib().paged_attention_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                        ctypes.byref(desc), _ptr(block_tables),
+                                        block_tables.shape[1], _ptr(context_lens), S,
+                                        max_context_len, scale, _ptr(ws), ws.numel(),
+                                        _stream(stream)), "paged_attention_decode")
+    return out
+
+
+def paged_attention_varlen(out, q, k_cache, v_cache, desc, block_tables, query_start_loc,
+                           context_lens, max_query_len, max_context_len, scale=None, ws=None,
+                           stream=None):
+    """out, q: CUDA [Tq, Hq, D]; query_start_loc int32 [S+1]; context_lens int32 [S]."""
+    Tq = q.shape[0]
+    S = context_lens.shape[0]
+    dt = _TORCH_DTYPE[desc.dtype]
+    for t, nm in ((out, "out"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, dt, nm)
+    for t, nm in ((block_tables, "block_tables"), (query_start_loc, "query_start_loc"),
+                  (context_lens, "context_lens")):
+        _need(t, torch.int32, nm)
+    if scale is None:
+        scale = 1.0 / math.sqrt(desc.head_dim)
+    if ws is None:
+        ws = workspace(varlen_workspace_bytes(desc, S, Tq, max_query_len, max_context_len),
+                       q.device)
+    _check(lib().paged_attention_varlen(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                        ctypes.byref(desc), _ptr(block_tables),
+                                        block_tables.shape[1], _ptr(query_start_loc),
+                                        _ptr(context_lens), S, Tq, max_query_len, max_context_len,
+                                        scale, _ptr(ws), ws.numel(), _stream(stream)),
+           "paged_attention_varlen")
+    return out
+
+
+def device_error(clear=True):
+    """The device error word (0 = none); synchronizes the device."""
+    code = ctypes.c_int32()
+    _check(lib().pkv_device_error(ctypes.byref(code), 1 if clear else 0), "pkv_device_error")
+    return code.value

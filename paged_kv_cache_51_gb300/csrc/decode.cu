@@ -1,0 +1,625 @@
+// Decode attention over a paged KV cache: planner, split kernel and merge.
+//
+// What is computed: for one query token per sequence, exact
+// softmax(q K^T * scale) V over the sequence's keys, reached through its block
+// table ("第 15 章：推理引擎与部署" §15.6 PagedAttention：分页 KV Cache).  The
+// softmax is accumulated block by block with the online recurrence of §15.1
+// 算法详解 (running max m, running sum l, rescale alpha = exp(m_old - m_new)),
+// here in base 2: scores are pre-multiplied by scale * log2(e) and exp2 is used,
+// which is the same function.  The KV tile of one block (B_c = 16 keys) is the
+// recurrence's column block.
+//
+// GB300 design:
+//  * HBM-bound: each (block, kv head) K and V tile is one contiguous 16 x D run
+//    (4 KiB for bf16, D = 128), fetched by the TMA engine with cp.async.bulk
+//    into a shared-memory ring guarded by mbarriers; a producer warp keeps up
+//    to kStages tiles in flight per CTA.
+//  * GQA packing ("大模型部署.md" §4.1 4. MQA 与 GQA): one CTA owns one KV head
+//    and all G query heads that read it, so each KV byte is read once.
+//  * Split-K over the context ("大模型部署.md" §2.5 TurboMind split-K
+//    decoding): a sequence's context is cut into fixed 512-token splits; each
+//    (split, kv head) is one work unit; partial (m, l, O) states are merged by
+//    a second kernel with the same alpha rescaling.  The split depends only on
+//    the context length, so results do not depend on the batch.
+//  * Persistent grid (a multiple of the SM count) over a work list that a
+//    one-CTA planner kernel builds on the device, so no host round trip.
+#include <algorithm>
+#include <cfloat>
+#include <cuda_runtime.h>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// ---------------------------------------------------------------------------
+// Planner: one CTA scans the batch, validates lengths and writes the work list.
+// ---------------------------------------------------------------------------
+struct PlanParams {
+    const int32_t* context_lens;
+    const int32_t* query_start_loc;  // nullptr: decode-only batch
+    int32_t num_seqs;
+    int32_t num_query_tokens;
+    int32_t max_context_len;
+    int32_t table_stride;
+    int32_t tokens_per_tile;          // prefill tile height in tokens
+    Workspace ws;
+    int* err;
+};
+
+__global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
+    __shared__ int warp_d[32], warp_p[32];
+    __shared__ int carry_d, carry_p, layout_ok;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        carry_d = 0;
+        carry_p = 0;
+        layout_ok = 1;
+        if (p.query_start_loc) {
+            if (p.query_start_loc[0] != 0 || p.query_start_loc[p.num_seqs] != p.num_query_tokens) {
+                layout_ok = 0;
+                flag_error(p.err, PKV_DEV_BAD_QUERY_LAYOUT);
+            }
+        }
+    }
+    __syncthreads();
+    for (int base = 0; base < p.num_seqs; base += 1024) {
+        const int s = base + tid;
+        int nd = 0, np = 0;
+        if (s < p.num_seqs && layout_ok) {
+            const int ctx = p.context_lens[s];
+            int qlen = 1;
+            if (p.query_start_loc) qlen = p.query_start_loc[s + 1] - p.query_start_loc[s];
+            if (qlen < 0 || qlen > p.num_query_tokens) {
+                flag_error(p.err, PKV_DEV_BAD_QUERY_LAYOUT);
+            } else if (qlen > 0) {
+                if (ctx < 1 || ctx > p.max_context_len || ctx < qlen) {
+                    flag_error(p.err, PKV_DEV_BAD_CONTEXT_LEN);
+                } else if ((ctx + kBlockTokens - 1) / kBlockTokens > p.table_stride) {
+                    flag_error(p.err, PKV_DEV_TABLE_TOO_NARROW);
+                } else if (qlen == 1) {
+                    nd = (ctx + kSplitTokens - 1) / kSplitTokens;
+                } else {
+                    np = (qlen + p.tokens_per_tile - 1) / p.tokens_per_tile;
+                }
+            }
+        }
+        // block-wide exclusive scan of nd and np
+        int xd = nd, xp = np;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int yd = __shfl_up_sync(kFull, xd, off);
+            const int yp = __shfl_up_sync(kFull, xp, off);
+            if (lane >= off) {
+                xd += yd;
+                xp += yp;
+            }
+        }
+        if (lane == 31) {
+            warp_d[warp] = xd;
+            warp_p[warp] = xp;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            int wd = warp_d[lane], wp = warp_p[lane];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int yd = __shfl_up_sync(kFull, wd, off);
+                const int yp = __shfl_up_sync(kFull, wp, off);
+                if (lane >= off) {
+                    wd += yd;
+                    wp += yp;
+                }
+            }
+            warp_d[lane] = wd;  // inclusive prefix over warps
+            warp_p[lane] = wp;
+        }
+        __syncthreads();
+        const int before_d = carry_d + (warp ? warp_d[warp - 1] : 0) + xd - nd;
+        const int before_p = carry_p + (warp ? warp_p[warp - 1] : 0) + xp - np;
+        for (int k = 0; k < nd; ++k) p.ws.items[before_d + k] = make_int2(s, k);
+        for (int k = 0; k < np; ++k) {
+            if (before_p + k < p.ws.max_prefill_items) p.ws.prefill_items[before_p + k] = make_int2(s, k);
+        }
+        __syncthreads();
+        if (tid == 0) {
+            carry_d += warp_d[31];
+            carry_p += warp_p[31];
+        }
+        __syncthreads();
+    }
+    if (tid == 0) {
+        p.ws.counters[0] = carry_d;
+        p.ws.counters[1] = min(carry_p, p.ws.max_prefill_items);
+    }
+}
+
+int launch_plan(const AttnArgs& a) {
+    PlanParams p;
+    p.context_lens = a.context_lens;
+    p.query_start_loc = a.query_start_loc;
+    p.num_seqs = a.num_seqs;
+    p.num_query_tokens = a.num_query_tokens;
+    p.max_context_len = a.max_context_len;
+    p.table_stride = a.table_stride;
+    p.tokens_per_tile = kPrefillRows / (a.desc->num_q_heads / a.desc->num_kv_heads);
+    p.ws = a.ws;
+    p.err = a.err;
+    plan_kernel<<<1, 1024, 0, a.stream>>>(p);
+    return cuda_status(cudaGetLastError());
+}
+
+// ---------------------------------------------------------------------------
+// Split kernel
+// ---------------------------------------------------------------------------
+struct SplitParams {
+    const void* q;
+    void* out;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    const int32_t* query_start_loc;
+    const int2* items;
+    const int32_t* n_items;
+    float2* part_ml;
+    float* part_o;
+    int32_t table_stride;
+    int32_t num_blocks;
+    int32_t num_kv_heads;
+    int32_t num_q_heads;
+    int32_t max_splits;
+    float scale_log2;
+    int* err;
+};
+
+constexpr size_t align_up_c(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+template <typename T, int D, int G>
+struct SplitCfg {
+    static constexpr int kWarps = 4;                        // consumer warps
+    static constexpr int kThreads = (kWarps + 1) * 32;      // + one producer warp
+    static constexpr int kDPL = D / 32;                     // head dims per lane
+    static constexpr int kTileBytes = kBlockTokens * D * int(sizeof(T));
+    static constexpr int kStageBytes = 2 * kTileBytes;      // K tile + V tile
+    static constexpr int kStages = kStageBytes <= 8192 ? 8 : 4;
+    static constexpr int kTC = G == 1 ? 16 : 32 / G;        // tokens per reduction chunk
+    static constexpr int kNV = kTC * G;                     // values per reduction (16 or 32)
+    static constexpr int kNC = kBlockTokens / kTC;          // chunks per block
+    static constexpr int kPBuf = G * kBlockTokens + G;      // p values + alphas per warp
+    static constexpr int kComb = G * (D + 2);               // per-warp combine record
+    static constexpr size_t kRingOff = 0;
+    static constexpr size_t kPBufOff = size_t(kStages) * kStageBytes;
+    static constexpr size_t kCombOff = kPBufOff + size_t(kWarps) * kPBuf * 4;
+    static constexpr size_t kBarOff = align_up_c(kCombOff + size_t(kWarps) * kComb * 4, 16);
+    static constexpr size_t kSmem = kBarOff + 2 * kStages * 8;
+    static_assert(kDPL == 2 || kDPL == 4, "head_dim 64 or 128");
+    static_assert(kNV == 16 || kNV == 32, "group size 1, 2, 4 or 8");
+};
+
+// Reduce-scatter across the warp: every lane holds NV partial sums; afterwards
+// lane l holds the full sum of value l (NV = 32) or of value l >> 1 (NV = 16).
+template <int NV>
+__device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane) {
+#pragma unroll
+    for (int step = 0; (NV >> step) > 1; ++step) {
+        const int n = NV >> step;
+        const int off = 16 >> step;
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float send = upper ? v[i] : v[i + n / 2];
+            const float keep = upper ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(kFull, send, off);
+        }
+    }
+    float r = v[0];
+    if (NV == 16) r += __shfl_xor_sync(kFull, r, 1);
+    return r;
+}
+
+// max / sum over the lanes that hold the same query head
+template <int G, int TC>
+__device__ __forceinline__ float group_max(float x) {
+    if (G == 1) {
+#pragma unroll
+        for (int off = 2; off < 32; off <<= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, off));
+    } else {
+#pragma unroll
+        for (int off = 1; off < TC; off <<= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, off));
+    }
+    return x;
+}
+template <int G, int TC>
+__device__ __forceinline__ float group_sum(float x) {
+    if (G == 1) {
+#pragma unroll
+        for (int off = 2; off < 32; off <<= 1) x += __shfl_xor_sync(kFull, x, off);
+    } else {
+#pragma unroll
+        for (int off = 1; off < TC; off <<= 1) x += __shfl_xor_sync(kFull, x, off);
+    }
+    return x;
+}
+
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(SplitCfg<T, D, G>::kThreads)
+    decode_split_kernel(SplitParams p) {
+    using C = SplitCfg<T, D, G>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char* ring = smem + C::kRingOff;
+    float* pbuf_all = reinterpret_cast<float*>(smem + C::kPBufOff);
+    float* comb = reinterpret_cast<float*>(smem + C::kCombOff);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+    uint64_t* empty = full + C::kStages;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const int Hkv = p.num_kv_heads, Hq = p.num_q_heads;
+    const int n_units = p.n_items[0] * Hkv;
+
+    if (warp == C::kWarps) {
+        // ---------------- producer warp: keeps the ring full ----------------
+        uint32_t it = 0;
+        bool ok = true;
+        const unsigned char* kb = static_cast<const unsigned char*>(p.k_cache);
+        const unsigned char* vb = static_cast<const unsigned char*>(p.v_cache);
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            const int2 item = p.items[u / Hkv];
+            const int kvh = u % Hkv;
+            const int ctx = p.context_lens[item.x];
+            const int b0 = item.y * (kSplitTokens / kBlockTokens);
+            const int nb = min(kSplitTokens / kBlockTokens, (ctx + kBlockTokens - 1) / kBlockTokens - b0);
+            int my_blk = 0;
+            if (lane < nb) my_blk = p.block_tables[size_t(item.x) * p.table_stride + b0 + lane];
+            for (int j = 0; j < nb; ++j, ++it) {
+                const int blk = __shfl_sync(kFull, my_blk, j);
+                const int st = it % C::kStages;
+                const uint32_t par = (it / C::kStages) & 1;
+                ok = __all_sync(kFull, mbar_wait(&empty[st], par ^ 1, p.err));
+                if (!ok) break;
+                if (lane == 0) {
+                    if (blk < 0 || blk >= p.num_blocks) {
+                        flag_error(p.err, PKV_DEV_BAD_BLOCK_ID);
+                        mbar_arrive(&full[st]);  // no data: consumers read a stale tile
+                    } else {
+                        mbar_arrive_expect_tx(&full[st], C::kStageBytes);
+                        const size_t off = (size_t(blk) * Hkv + kvh) * C::kTileBytes;
+                        unsigned char* dst = ring + size_t(st) * C::kStageBytes;
+                        bulk_g2s(dst, kb + off, C::kTileBytes, &full[st]);
+                        bulk_g2s(dst + C::kTileBytes, vb + off, C::kTileBytes, &full[st]);
+                    }
+                }
+                __syncwarp();
+            }
+        }
+        // never leave with bulk copies in flight: wait for the last fill of each stage
+        if (lane == 0) {
+            for (int k = 0; k < C::kStages && uint32_t(k) < it; ++k) {
+                const uint32_t last = it - 1 - k;
+                mbar_wait(&full[last % C::kStages], (last / C::kStages) & 1, p.err);
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumer warps ----------------
+    constexpr int DPL = C::kDPL, TC = C::kTC, NV = C::kNV, NC = C::kNC;
+    const int my_head = G == 1 ? 0 : lane / TC;          // query head (within group) this lane scores
+    const int my_tok = G == 1 ? (lane >> 1) : lane % TC; // token (within chunk) this lane scores
+    float* pbuf = pbuf_all + warp * C::kPBuf;
+    const T* qbase = static_cast<const T*>(p.q);
+    uint32_t it_base = 0;
+    bool ok = true;
+
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const int2 item = p.items[u / Hkv];
+        const int seq = item.x, split = item.y;
+        const int kvh = u % Hkv;
+        const int ctx = p.context_lens[seq];
+        const int nblk_seq = (ctx + kBlockTokens - 1) / kBlockTokens;
+        const int b0 = split * (kSplitTokens / kBlockTokens);
+        const int nb = min(kSplitTokens / kBlockTokens, nblk_seq - b0);
+        const int qrow = p.query_start_loc ? p.query_start_loc[seq] : seq;
+
+        float qr[G][DPL];
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            float t[DPL];
+            Elem<T>::template load<DPL>(qbase + (size_t(qrow) * Hq + kvh * G + j) * D + lane * DPL, t);
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) qr[j][d] = t[d] * p.scale_log2;
+        }
+        float m = -INFINITY, l = 0.f;
+        float o[G][DPL];
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) o[j][d] = 0.f;
+
+        for (int jb = warp; jb < nb; jb += C::kWarps) {
+            const uint32_t it = it_base + jb;
+            const int st = it % C::kStages;
+            if (ok) ok = __all_sync(kFull, mbar_wait(&full[st], (it / C::kStages) & 1, p.err));
+            if (!ok) continue;
+            const T* kt = reinterpret_cast<const T*>(ring + size_t(st) * C::kStageBytes);
+            const T* vt = kt + kBlockTokens * D;
+            const int nvalid = min(kBlockTokens, ctx - (b0 + jb) * kBlockTokens);
+
+            // scores s = q . k for this lane's (head, token) in each chunk
+            float s[NC];
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                float part[NV];
+#pragma unroll
+                for (int tt = 0; tt < TC; ++tt) {
+                    float kf[DPL];
+                    Elem<T>::template load<DPL>(kt + (c * TC + tt) * D + lane * DPL, kf);
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        float acc = qr[j][0] * kf[0];
+#pragma unroll
+                        for (int d = 1; d < DPL; ++d) acc = fmaf(qr[j][d], kf[d], acc);
+                        part[j * TC + tt] = acc;
+                    }
+                }
+                s[c] = reduce_scatter<NV>(part, lane);
+                if (c * TC + my_tok >= nvalid) s[c] = -INFINITY;
+            }
+            // online softmax update over this block (column block of 16 keys)
+            float mx = s[0];
+#pragma unroll
+            for (int c = 1; c < NC; ++c) mx = fmaxf(mx, s[c]);
+            mx = group_max<G, TC>(mx);
+            const float m_new = fmaxf(m, mx);
+            const float alpha = exp2f(m - m_new);
+            float psum = 0.f;
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                const float pc = exp2f(s[c] - m_new);
+                psum += pc;
+                pbuf[my_head * kBlockTokens + c * TC + my_tok] = pc;
+            }
+            psum = group_sum<G, TC>(psum);
+            l = l * alpha + psum;
+            m = m_new;
+            if (my_tok == 0) pbuf[G * kBlockTokens + my_head] = alpha;
+            __syncwarp();
+            // O = diag(alpha) O + P V
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                const float a = pbuf[G * kBlockTokens + j];
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) o[j][d] *= a;
+            }
+            for (int t = 0; t < nvalid; ++t) {
+                float vf[DPL];
+                Elem<T>::template load<DPL>(vt + t * D + lane * DPL, vf);
+#pragma unroll
+                for (int j = 0; j < G; ++j) {
+                    const float pj = pbuf[j * kBlockTokens + t];
+#pragma unroll
+                    for (int d = 0; d < DPL; ++d) o[j][d] = fmaf(pj, vf[d], o[j][d]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+        }
+        it_base += nb;
+
+        // ---- combine the consumer warps' states ----
+        float* rec = comb + warp * C::kComb;
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) rec[j * D + lane * DPL + d] = o[j][d];
+        if (my_tok == 0) {
+            rec[G * D + my_head] = m;
+            rec[G * D + G + my_head] = l;
+        }
+        consumer_sync(C::kWarps * 32);
+        const int nsplit = (ctx + kSplitTokens - 1) / kSplitTokens;
+        for (int idx = threadIdx.x; idx < G * D; idx += C::kWarps * 32) {
+            const int j = idx / D, d = idx % D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < C::kWarps; ++w) M = fmaxf(M, comb[w * C::kComb + G * D + j]);
+            float L = 0.f, O = 0.f;
+#pragma unroll
+            for (int w = 0; w < C::kWarps; ++w) {
+                const float* r = comb + w * C::kComb;
+                const float sc = exp2f(r[G * D + j] - M);
+                L = fmaf(r[G * D + G + j], sc, L);
+                O = fmaf(r[j * D + d], sc, O);
+            }
+            const int h = kvh * G + j;
+            if (nsplit == 1) {
+                static_cast<T*>(p.out)[(size_t(qrow) * Hq + h) * D + d] = Elem<T>::store_val(O / L);
+            } else {
+                const size_t slot = (size_t(seq) * Hq + h) * p.max_splits + split;
+                p.part_o[slot * D + d] = O;
+                if (d == 0) p.part_ml[slot] = make_float2(M, L);
+            }
+        }
+        consumer_sync(C::kWarps * 32);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Merge kernel: one warp per (sequence, query head) with more than one split.
+//   M = max_k m_k,  L = sum_k l_k 2^(m_k - M),  out = sum_k O_k 2^(m_k - M) / L
+// ---------------------------------------------------------------------------
+struct MergeParams {
+    void* out;
+    const int32_t* context_lens;
+    const int32_t* query_start_loc;
+    const float2* part_ml;
+    const float* part_o;
+    int32_t num_seqs;
+    int32_t num_q_heads;
+    int32_t max_splits;
+    int32_t max_context_len;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(128) decode_merge_kernel(MergeParams p) {
+    constexpr int DPL = D / 32;
+    const int lane = threadIdx.x & 31;
+    const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (wid >= p.num_seqs * p.num_q_heads) return;
+    const int seq = wid / p.num_q_heads, h = wid % p.num_q_heads;
+    int qrow = seq;
+    if (p.query_start_loc) {
+        qrow = p.query_start_loc[seq];
+        if (p.query_start_loc[seq + 1] - qrow != 1) return;  // not a decode row
+    }
+    const int ctx = p.context_lens[seq];
+    if (ctx < 1 || ctx > p.max_context_len) return;          // flagged by the planner
+    const int n = (ctx + kSplitTokens - 1) / kSplitTokens;
+    if (n <= 1) return;                                     // written by the split kernel
+    const size_t base = (size_t(seq) * p.num_q_heads + h) * p.max_splits;
+    float M = -INFINITY;
+    for (int k = lane; k < n; k += 32) M = fmaxf(M, p.part_ml[base + k].x);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+    float L = 0.f;
+    for (int k = lane; k < n; k += 32) {
+        const float2 ml = p.part_ml[base + k];
+        L = fmaf(ml.y, exp2f(ml.x - M), L);
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
+    float acc[DPL];
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) acc[d] = 0.f;
+    for (int k = 0; k < n; ++k) {
+        const float w = exp2f(p.part_ml[base + k].x - M);
+        float ov[DPL];
+        Elem<float>::template load<DPL>(p.part_o + (base + k) * D + lane * DPL, ov);
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) acc[d] = fmaf(w, ov[d], acc[d]);
+    }
+    const float inv = 1.f / L;
+    T* o = static_cast<T*>(p.out) + (size_t(qrow) * p.num_q_heads + h) * D + lane * DPL;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) o[d] = Elem<T>::store_val(acc[d] * inv);
+}
+
+// ---------------------------------------------------------------------------
+// Host launchers
+// ---------------------------------------------------------------------------
+namespace {
+
+int num_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+template <typename T, int D, int G>
+int launch_split_t(const AttnArgs& a) {
+    using C = SplitCfg<T, D, G>;
+    auto kern = decode_split_kernel<T, D, G>;
+    // per-device attribute setup is cheap and idempotent
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(C::kSmem));
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::kThreads, C::kSmem);
+    if (e != cudaSuccess || per_sm < 1) return PKV_ERR_CUDA;
+    const int64_t bound_units =
+        int64_t(a.num_seqs) * a.ws.max_splits * a.desc->num_kv_heads;  // upper bound
+    const int64_t grid = std::min<int64_t>(int64_t(num_sms()) * per_sm, bound_units);
+    if (grid < 1) return PKV_OK;
+    SplitParams p;
+    p.q = a.q;
+    p.out = a.out;
+    p.k_cache = a.k_cache;
+    p.v_cache = a.v_cache;
+    p.block_tables = a.block_tables;
+    p.context_lens = a.context_lens;
+    p.query_start_loc = a.query_start_loc;
+    p.items = a.ws.items;
+    p.n_items = a.ws.counters;
+    p.part_ml = a.ws.part_ml;
+    p.part_o = a.ws.part_o;
+    p.table_stride = a.table_stride;
+    p.num_blocks = a.desc->num_blocks;
+    p.num_kv_heads = a.desc->num_kv_heads;
+    p.num_q_heads = a.desc->num_q_heads;
+    p.max_splits = a.ws.max_splits;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.err = a.err;
+    kern<<<unsigned(grid), C::kThreads, C::kSmem, a.stream>>>(p);
+    return cuda_status(cudaGetLastError());
+}
+
+template <typename T, int D>
+int launch_split_d(const AttnArgs& a, int g) {
+    switch (g) {
+        case 1: return launch_split_t<T, D, 1>(a);
+        case 2: return launch_split_t<T, D, 2>(a);
+        case 4: return launch_split_t<T, D, 4>(a);
+        case 8: return launch_split_t<T, D, 8>(a);
+        default: return PKV_ERR_UNSUPPORTED;
+    }
+}
+
+template <typename T, int D>
+int launch_merge_t(const AttnArgs& a) {
+    MergeParams p;
+    p.out = a.out;
+    p.context_lens = a.context_lens;
+    p.query_start_loc = a.query_start_loc;
+    p.part_ml = a.ws.part_ml;
+    p.part_o = a.ws.part_o;
+    p.num_seqs = a.num_seqs;
+    p.num_q_heads = a.desc->num_q_heads;
+    p.max_splits = a.ws.max_splits;
+    p.max_context_len = a.max_context_len;
+    const int64_t warps = int64_t(a.num_seqs) * a.desc->num_q_heads;
+    const int64_t blocks = (warps + 3) / 4;
+    if (blocks < 1) return PKV_OK;
+    decode_merge_kernel<T, D><<<unsigned(blocks), 128, 0, a.stream>>>(p);
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+int launch_decode_split(const AttnArgs& a) {
+    const int g = a.desc->num_q_heads / a.desc->num_kv_heads;
+    const bool bf = a.desc->dtype == PKV_BF16;
+    if (a.desc->head_dim == 128)
+        return bf ? launch_split_d<__nv_bfloat16, 128>(a, g) : launch_split_d<float, 128>(a, g);
+    if (a.desc->head_dim == 64)
+        return bf ? launch_split_d<__nv_bfloat16, 64>(a, g) : launch_split_d<float, 64>(a, g);
+    return PKV_ERR_UNSUPPORTED;
+}
+
+int launch_decode_merge(const AttnArgs& a) {
+    // a single split is finished by the split kernel itself
+    if (a.ws.max_splits <= 1) return PKV_OK;
+    const bool bf = a.desc->dtype == PKV_BF16;
+    if (a.desc->head_dim == 128)
+        return bf ? launch_merge_t<__nv_bfloat16, 128>(a) : launch_merge_t<float, 128>(a);
+    if (a.desc->head_dim == 64)
+        return bf ? launch_merge_t<__nv_bfloat16, 64>(a) : launch_merge_t<float, 64>(a);
+    return PKV_ERR_UNSUPPORTED;
+}
+
+}  // namespace pkv

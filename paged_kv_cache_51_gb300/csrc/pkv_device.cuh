@@ -1,0 +1,130 @@
+// Device helpers shared by the kernels: mbarriers, bulk (TMA) copies, bounded
+// waits, element conversion and the device error word.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "../../include/pagedkv.h"
+
+namespace pkv {
+
+constexpr int kBlockTokens = 16;          // tokens per cache block the kernels implement
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: a pipeline wait this long is a fault
+
+// ---- device error word ------------------------------------------------------
+// First fault wins; kernels skip the offending access and carry on, so the
+// context stays usable and the host reads the code with pkv_device_error.
+__device__ __forceinline__ void flag_error(int* err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---- shared-memory addresses and mbarriers ----------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete.  Gives up after
+// kWaitLimitNs, records PKV_DEV_WAIT_TIMEOUT and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try(bar, parity)) {
+        if (global_ns() - t0 > kWaitLimitNs) {
+            flag_error(err, PKV_DEV_WAIT_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// 1-D bulk copy global -> shared (TMA engine), completing on `bar` with
+// `bytes` of transaction count.  src, dst 16-byte aligned; bytes % 16 == 0.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// ---- element conversion -------------------------------------------------------
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<float> {
+    // load N consecutive values (N = 2 or 4) from shared memory as fp32
+    template <int N>
+    __device__ __forceinline__ static void load(const float* p, float (&out)[N]) {
+        if constexpr (N == 4) {
+            float4 v = *reinterpret_cast<const float4*>(p);
+            out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
+        } else {
+            float2 v = *reinterpret_cast<const float2*>(p);
+            out[0] = v.x; out[1] = v.y;
+        }
+    }
+    __device__ __forceinline__ static float store_val(float x) { return x; }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+    template <int N>
+    __device__ __forceinline__ static void load(const __nv_bfloat16* p, float (&out)[N]) {
+        // a bf16 is the high half of an fp32: widening is a shift / mask
+        if constexpr (N == 4) {
+            uint2 v = *reinterpret_cast<const uint2*>(p);
+            out[0] = __uint_as_float(v.x << 16);
+            out[1] = __uint_as_float(v.x & 0xffff0000u);
+            out[2] = __uint_as_float(v.y << 16);
+            out[3] = __uint_as_float(v.y & 0xffff0000u);
+        } else {
+            uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+            out[0] = __uint_as_float(v << 16);
+            out[1] = __uint_as_float(v & 0xffff0000u);
+        }
+    }
+    __device__ __forceinline__ static __nv_bfloat16 store_val(float x) {
+        return __float2bfloat16_rn(x);
+    }
+};
+
+}  // namespace pkv

@@ -1,0 +1,73 @@
+// Host-side internals shared by the translation units of libpagedkv.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/pagedkv.h"
+
+namespace pkv {
+
+constexpr int kSplitTokens = 512;       // context span of one decode split
+constexpr int kPrefillRows = 128;       // query rows (tokens x group heads) per prefill tile
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline int ceil_div(int64_t a, int64_t b) { return int((a + b - 1) / b); }
+
+inline size_t elem_bytes(int dtype) { return dtype == PKV_F32 ? 4 : 2; }
+
+// Validates a cache descriptor; `attention` additionally checks the head
+// grouping and head_dim the attention kernels implement.
+int check_desc(const pkv_cache_desc* d, bool attention);
+
+// Address of this device's error word (looked up once per device).
+int* device_error_ptr(int* status);
+
+// Status for a CUDA error (clears sticky-free errors from the runtime's slot).
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+
+// Workspace carve-up shared by decode and varlen.
+struct Workspace {
+    int32_t* counters;   // [0] decode items, [1] prefill items
+    int2* items;         // decode items (seq, split)
+    int2* prefill_items; // prefill items (seq, row tile)
+    float2* part_ml;     // [num_seqs][num_q_heads][max_splits] (max, sum), log2 domain
+    float* part_o;       // [num_seqs][num_q_heads][max_splits][head_dim]
+    int32_t max_splits;
+    int32_t max_prefill_items;
+};
+
+size_t workspace_layout(const pkv_cache_desc* d, int32_t num_seqs, int32_t max_context_len,
+                        int32_t num_prefill_items, void* base, Workspace* ws);
+
+struct AttnArgs {
+    void* out;
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const pkv_cache_desc* desc;
+    const int32_t* block_tables;
+    int32_t table_stride;
+    const int32_t* query_start_loc;  // nullptr: one query per sequence
+    const int32_t* context_lens;
+    int32_t num_seqs;
+    int32_t num_query_tokens;
+    int32_t max_query_len;
+    int32_t max_context_len;
+    float scale;
+    Workspace ws;
+    cudaStream_t stream;
+    int* err;
+};
+
+// decode.cu
+int launch_plan(const AttnArgs& a);
+int launch_decode_split(const AttnArgs& a);
+int launch_decode_merge(const AttnArgs& a);
+// prefill_tc.cu
+int prefill_supported(const pkv_cache_desc* d);
+int launch_prefill(const AttnArgs& a);
+int prefill_item_bound(int32_t num_seqs, int32_t num_query_tokens, int32_t group);
+
+}  // namespace pkv

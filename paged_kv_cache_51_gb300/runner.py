@@ -1,0 +1,183 @@
+"""Drive a batch through the library: host block pool -> copy-on-write -> append -> attention.
+
+``DeviceCache`` owns one layer's K and V pools on the GPU and a host
+``BlockPool``.  Pool operations are planned on the host; the device work they
+imply (copy-on-write block copies, then K/V appends) is queued and issued in
+batches: all copies of a batch before all of its appends.  That order equals
+applying the operations one token at a time because, between two flushes, a
+block that is copied from is shared and therefore not written in place, and a
+copy destination is fresh.  A fork or a free makes blocks shared or reusable,
+so pending work is flushed before either.
+
+Operations use the tuple format of the ``workloads`` package:
+("add", seq, n, row), ("grow", seq, n, row), ("fork", parent, child), ("free", seq).
+"""
+
+import math
+
+import numpy as np
+import torch
+
+from . import (BlockPool, cache_desc, paged_attention_decode, paged_attention_varlen,
+               paged_kv_append, pkv_copy_blocks, varlen_workspace_bytes, decode_workspace_bytes,
+               workspace)
+
+
+def _torch_rows(rows, dtype):
+    """Host value rows (float32, or uint16 bf16 bits) -> torch tensor of the cache dtype."""
+    if dtype == "f32":
+        return torch.from_numpy(np.ascontiguousarray(rows))
+    return torch.from_numpy(np.ascontiguousarray(rows).view(np.int16)).view(torch.bfloat16)
+
+
+class DeviceCache:
+    def __init__(self, w, device="cuda"):
+        self.w = w
+        self.device = torch.device(device)
+        tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+        shape = (w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim)
+        self.k_cache = torch.zeros(shape, dtype=tdt, device=self.device)
+        self.v_cache = torch.zeros(shape, dtype=tdt, device=self.device)
+        self.desc = cache_desc(self.k_cache, w.num_q_heads)
+        self.pool = BlockPool(w.num_blocks, w.block_size, 0, w.free_order)
+        self._slots, self._rows, self._pairs = [], [], []
+        self.step_slots, self.step_rows, self.step_pairs = [], [], []
+
+    # ---- planning -------------------------------------------------------
+    def _apply(self, op, record):
+        kind = op[0]
+        if kind == "add":
+            _, seq, n, row = op
+            slots = self.pool.add(seq, n)
+            self._slots += slots
+            self._rows += range(row, row + n)
+            if record:
+                self.step_slots += slots
+                self.step_rows += range(row, row + n)
+        elif kind == "grow":
+            _, seq, n, row = op
+            for i in range(n):
+                slot, cow = self.pool.append_slot(seq)
+                if cow is not None:
+                    self._pairs.append(cow)
+                    if record:
+                        self.step_pairs.append(cow)
+                self._slots.append(slot)
+                self._rows.append(row + i)
+                if record:
+                    self.step_slots.append(slot)
+                    self.step_rows.append(row + i)
+        elif kind == "fork":
+            self.flush()
+            self.pool.fork(op[1], op[2])
+        elif kind == "free":
+            self.flush()
+            self.pool.free(op[1])
+        else:
+            raise ValueError(f"unknown operation {kind!r}")
+
+    # ---- device work ----------------------------------------------------
+    def flush(self, chunk_tokens=1 << 16):
+        w = self.w
+        if self._pairs:
+            pairs = torch.tensor(self._pairs, dtype=torch.int32).to(self.device)
+            pkv_copy_blocks(pairs, self.k_cache, self.v_cache, self.desc)
+        self._pairs = []
+        slots, rows = self._slots, self._rows
+        for a in range(0, len(slots), chunk_tokens):
+            s = torch.tensor(slots[a:a + chunk_tokens], dtype=torch.int64).to(self.device)
+            r = np.asarray(rows[a:a + chunk_tokens])
+            k = _torch_rows(w.k_rows[r], w.dtype).to(self.device)
+            v = _torch_rows(w.v_rows[r], w.dtype).to(self.device)
+            paged_kv_append(k, v, s, self.k_cache, self.v_cache, self.desc)
+        self._slots, self._rows = [], []
+
+    def run_setup(self):
+        for op in self.w.setup:
+            self._apply(op, record=False)
+        self.flush()
+
+    def plan_step(self):
+        """Plan the step's pool operations; returns the step's device inputs (not yet applied)."""
+        for op in self.w.step:
+            self._apply(op, record=True)
+        # the step's copies and appends stay queued: hand them to the caller
+        self._slots, self._rows, self._pairs = [], [], []
+        w = self.w
+        r = np.asarray(self.step_rows)
+        return {
+            "slot_mapping": torch.tensor(self.step_slots, dtype=torch.int64),
+            "k": _torch_rows(w.k_rows[r], w.dtype),
+            "v": _torch_rows(w.v_rows[r], w.dtype),
+            "pairs": torch.tensor(self.step_pairs, dtype=torch.int32).reshape(-1, 2),
+        }
+
+    def batch_metadata(self):
+        """Block tables [S, W] (padded -1), context lengths [S], query_start_loc [S+1] (host)."""
+        w = self.w
+        seqs = [s for s, _ in w.batch]
+        width = max(math.ceil(self.pool.seq_len(s) / w.block_size) for s in seqs)
+        tables, ctx = self.pool.block_tables(seqs, width)
+        qsl = torch.zeros(len(seqs) + 1, dtype=torch.int32)
+        qsl[1:] = torch.cumsum(torch.tensor([q for _, q in w.batch], dtype=torch.int32), 0)
+        return tables, ctx, qsl
+
+    def q_tensor(self):
+        return _torch_rows(self.w.q, self.w.dtype)
+
+
+class Step:
+    """Device-resident inputs of one step and the calls that run it."""
+
+    def __init__(self, dc, planned):
+        w = dc.w
+        dev = dc.device
+        self.dc = dc
+        self.slot_mapping = planned["slot_mapping"].to(dev)
+        self.k_new = planned["k"].to(dev)
+        self.v_new = planned["v"].to(dev)
+        self.pairs = planned["pairs"].to(dev)
+        tables, ctx, qsl = dc.batch_metadata()
+        self.tables = tables.to(dev)
+        self.ctx = ctx.to(dev)
+        self.qsl = qsl.to(dev)
+        self.max_ctx = int(ctx.max())
+        self.max_qlen = max(q for _, q in w.batch)
+        self.decode_only = self.max_qlen == 1
+        self.q = dc.q_tensor().to(dev)
+        self.out = torch.empty_like(self.q)
+        S = len(w.batch)
+        if self.decode_only:
+            nbytes = decode_workspace_bytes(dc.desc, S, self.max_ctx)
+        else:
+            nbytes = varlen_workspace_bytes(dc.desc, S, self.q.shape[0], self.max_qlen,
+                                            self.max_ctx)
+        self.ws = workspace(nbytes, dev)
+
+    def write_kv(self, stream=None):
+        dc = self.dc
+        pkv_copy_blocks(self.pairs, dc.k_cache, dc.v_cache, dc.desc, stream)
+        paged_kv_append(self.k_new, self.v_new, self.slot_mapping, dc.k_cache, dc.v_cache, dc.desc,
+                        stream)
+
+    def attend(self, stream=None):
+        dc = self.dc
+        if self.decode_only:
+            return paged_attention_decode(self.out, self.q, dc.k_cache, dc.v_cache, dc.desc,
+                                          self.tables, self.ctx, self.max_ctx, ws=self.ws,
+                                          stream=stream)
+        return paged_attention_varlen(self.out, self.q, dc.k_cache, dc.v_cache, dc.desc,
+                                      self.tables, self.qsl, self.ctx, self.max_qlen, self.max_ctx,
+                                      ws=self.ws, stream=stream)
+
+    def run(self, stream=None):
+        self.write_kv(stream)
+        return self.attend(stream)
+
+
+def prepare(w, device="cuda"):
+    """Set up a workload on the device; returns (DeviceCache, Step) ready to run."""
+    dc = DeviceCache(w, device)
+    dc.run_setup()
+    step = Step(dc, dc.plan_step())
+    return dc, step

@@ -1,0 +1,172 @@
+"""C-ABI library on the host (no GPU needed): exports and the C++ block pool.
+
+The C++ pool is checked operation by operation against the oracle's pool model
+(a separate implementation): slots, copy-on-write pairs, block tables,
+reference counts and admission statuses must match exactly.
+"""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle.block_pool import LATER, NEVER, OK, BlockPoolModel
+from tests.conftest import ROOT, read_kv, read_rows
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "pagedkv.h"), encoding="utf-8") as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^PKV_API\s+(?:const\s+)?\w+\*?\s+\**(\w+)\s*\(", text,
+                                 flags=re.M)))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert len(declared) >= 19
+    L = ctypes.CDLL(lib.LIB_PATH)
+    for name in declared:
+        assert hasattr(L, name), f"{name} declared in pagedkv.h but not exported"
+    assert sorted(lib.EXPORTS) == declared
+
+
+def test_status_strings(lib):
+    for st in (0, -1, -2, -3, -4, -5, -6, -7):
+        assert lib.status_string(st) not in ("", "unknown status")
+    assert lib.status_string(-99) == "unknown status"
+
+
+_STATUS = {0: OK, -2: LATER, -3: NEVER}
+
+
+def test_paging_example_through_abi(lib):
+    g = read_kv("paging_example_bs4.txt")
+    head = [int(x) for x in g["free_order_head"].split()]
+    order = head + [b for b in range(16) if b not in head]
+    pool = lib.BlockPool(16, int(g["block_size"]), 0, order)
+    assert pool.add(0, int(g["prompt_tokens"])) == [int(x) for x in g["prompt_slots"].split()]
+    slot, cow = pool.append_slot(0)
+    assert cow is None and slot == int(g["next_token_slot"])
+    tables, ctx = pool.block_tables([0], 4)
+    assert tables[0, :2].tolist() == [int(x) for x in g["table_after"].split()]
+    assert tables[0, 2:].tolist() == [-1, -1] and ctx.tolist() == [5]
+
+
+@pytest.mark.parametrize("row", read_rows("admission_cases.txt"))
+def test_admission_cases_through_abi(lib, row):
+    total, wm, used, bs, tokens = (int(x) for x in row[:5])
+    pool = lib.BlockPool(total, bs, wm)
+    if used:
+        pool.add(99, used * bs)
+    assert _STATUS[pool.can_allocate(tokens)] == row[5]
+    st, _ = pool.add_status(1, tokens)
+    assert _STATUS[st] == row[5]
+
+
+def test_cpp_pool_matches_oracle_model_on_random_traces(lib):
+    rng = np.random.default_rng(11)
+    for trial in range(6):
+        nb, bs = int(rng.integers(20, 120)), int(rng.choice([1, 4, 16]))
+        order = rng.permutation(nb)
+        wm = int(rng.integers(0, 3))
+        ref = BlockPoolModel(nb, bs, wm, order)
+        cpp = lib.BlockPool(nb, bs, wm, order)
+        next_id = 0
+        for _ in range(1500):
+            op = int(rng.integers(0, 4))
+            seqs = sorted(ref.tables)
+            if op == 0 or not seqs:
+                n = int(rng.integers(1, 5 * bs + 2))
+                st_ref, slots_ref = ref.add_sequence(next_id, n)
+                st_cpp, slots_cpp = cpp.add_status(next_id, n)
+                assert _STATUS[st_cpp] == st_ref
+                assert slots_cpp == slots_ref
+                if st_ref == OK:
+                    next_id += 1
+            elif op == 1:
+                s = seqs[int(rng.integers(len(seqs)))]
+                slot_ref, cow_ref = ref.append_slot(s)
+                st, slot, cow = cpp.append_slot_status(s)
+                if slot_ref is None:
+                    assert st == lib.PKV_ERR_NO_BLOCKS
+                else:
+                    assert st == 0 and slot == slot_ref and cow == cow_ref
+            elif op == 2 and len(seqs) < 30:
+                p = seqs[int(rng.integers(len(seqs)))]
+                ref.fork(p, next_id)
+                cpp.fork(p, next_id)
+                next_id += 1
+            elif op == 3:
+                s = seqs[int(rng.integers(len(seqs)))]
+                ref.free_sequence(s)
+                cpp.free(s)
+            assert cpp.num_free() == ref.num_free()
+        live = sorted(ref.tables)
+        if live:
+            width = max(len(t) for t in ref.tables.values())
+            tables, ctx = cpp.block_tables(live, width)
+            for i, s in enumerate(live):
+                t = ref.block_table(s)
+                assert tables[i, :len(t)].tolist() == t
+                assert ctx[i] == ref.context_len(s)
+        for b in range(nb):
+            assert cpp.ref_count(b) == ref.ref[b]
+
+
+def test_pool_errors_leave_state_unchanged(lib):
+    pool = lib.BlockPool(2, 4)
+    pool.add(0, 8)
+    st, slot, cow = pool.append_slot_status(0)
+    assert st == lib.PKV_ERR_NO_BLOCKS
+    assert pool.seq_len(0) == 8 and pool.num_free() == 0
+    with pytest.raises(lib.PagedKVError):
+        pool.fork(5, 6)             # unknown parent
+    with pytest.raises(lib.PagedKVError):
+        pool.add(0, 1)              # existing id
+    with pytest.raises(lib.PagedKVError):
+        pool.block_tables([0], 1)   # table wider than max_blocks
+    with pytest.raises(lib.PagedKVError):
+        lib.BlockPool(4, 4, 0, [0, 1, 1, 2])  # not a permutation
+
+
+def test_workspace_sizes_are_host_computable(lib):
+    import torch
+
+    desc = lib.CacheDesc(lib.PKV_BF16, 100, 16, 8, 32, 128)
+    a = lib.decode_workspace_bytes(desc, 64, 4096)
+    b = lib.decode_workspace_bytes(desc, 64, 512)
+    assert a > b > 0 and a % 256 == 0
+    # 64 seqs x 32 heads x 8 splits x (128 floats + (m, l))
+    assert a >= 64 * 32 * 8 * (128 * 4 + 8)
+    assert lib.varlen_workspace_bytes(desc, 515, 2048, 512, 3584) > 0
+    bad = lib.CacheDesc(7, 100, 16, 8, 32, 128)
+    assert lib.decode_workspace_bytes(bad, 1, 1) == 0
+    del torch
+
+
+def test_device_calls_reject_bad_arguments_before_launch(lib):
+    """Host-side validation returns an error without touching a GPU."""
+    L = lib.lib()
+    desc = lib.CacheDesc(lib.PKV_BF16, 100, 16, 8, 32, 128)
+    ref = ctypes.byref
+    # null pointers
+    assert L.paged_kv_append(None, None, None, 4, None, None, ref(desc), None) == lib.PKV_ERR_INVALID
+    assert L.paged_attention_decode(None, None, None, None, ref(desc), None, 4, None, 1, 16,
+                                    0.1, None, 0, None) == lib.PKV_ERR_INVALID
+    # unsupported shapes for attention
+    odd = lib.CacheDesc(lib.PKV_BF16, 100, 32, 8, 32, 128)   # block_size 32
+    fake = ctypes.c_void_p(1 << 20)
+    assert L.paged_attention_decode(fake, fake, fake, fake, ref(odd), fake, 4, fake, 1, 16, 0.1,
+                                    fake, 1 << 20, None) == lib.PKV_ERR_UNSUPPORTED
+    g3 = lib.CacheDesc(lib.PKV_BF16, 100, 16, 8, 24, 128)    # group of 3
+    assert L.paged_attention_decode(fake, fake, fake, fake, ref(g3), fake, 4, fake, 1, 16, 0.1,
+                                    fake, 1 << 20, None) == lib.PKV_ERR_UNSUPPORTED
+    # workspace too small
+    assert L.paged_attention_decode(fake, fake, fake, fake, ref(desc), fake, 4, fake, 64, 4096,
+                                    0.1, fake, 256, None) == lib.PKV_ERR_WORKSPACE
+    # zero-sized work is a no-op
+    assert L.paged_kv_append(None, None, None, 0, None, None, ref(desc), None) == 0
+    assert L.pkv_copy_blocks(None, 0, None, None, ref(desc), None) == 0
