@@ -247,7 +247,8 @@ def run_gpu(args):
 
         dist.init_process_group("nccl")
 
-    w = workloads.make(args.config, seed=rank)
+    kw = {"batch": args.batch} if args.batch and args.config in (2, 3) else {}
+    w = workloads.make(args.config, seed=rank, **kw)
     dc, step = runner.prepare(w)
     ctx_host = step.ctx.cpu().tolist()
     attn_b = attention_bytes(w, ctx_host)
@@ -368,6 +369,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="sequences in the batch (decode workloads; 0 = the workload's own)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-worker", action="store_true")
     ap.add_argument("--cpu-seqs", type=int, default=4)
