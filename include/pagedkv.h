@@ -198,6 +198,32 @@ PKV_API int paged_attention_decode(void* out, const void* q, const void* k_cache
                            int32_t num_seqs, int32_t max_context_len, float scale,
                            void* workspace, size_t workspace_bytes, void* stream);
 
+/* Decode attention for callers that cannot allocate device memory (no
+ * counterpart on the pages; it exists for library users).  Callers such as a
+ * plugin inside an engine that owns all device memory and offers no scratch
+ * allocator, or a server whose KV pool already took the rest of HBM, have no
+ * way to provide the workspace paged_attention_decode needs.  This entry point
+ * computes exactly what paged_attention_decode computes, with the same
+ * arguments minus the workspace, using a fixed scratch array of
+ * PKV_NOALLOC_SCRATCH_BYTES that the library holds in the device memory of
+ * every GPU that loads it until the process exits.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *   - PKV_ERR_WORKSPACE (nothing enqueued) when the batch's split partials
+ *     (pkv_decode_workspace_bytes) exceed PKV_NOALLOC_SCRATCH_BYTES.
+ *   - The first call on a device looks up the array's device address with that
+ *     device current; make that first call before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents
+ *     (nothing in it needs to start at zero).  Calls that overlap on the GPU
+ *     (other streams, other threads) race on it and corrupt each other's
+ *     results; serialize them. */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+PKV_API int paged_attention_decode_noalloc(void* out, const void* q, const void* k_cache,
+                                           const void* v_cache, const pkv_cache_desc* desc,
+                                           const int32_t* block_tables,
+                                           int32_t max_blocks_per_seq,
+                                           const int32_t* context_lens, int32_t num_seqs,
+                                           int32_t max_context_len, float scale, void* stream);
+
 /* Bytes of workspace paged_attention_varlen needs. */
 PKV_API size_t pkv_varlen_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs,
                                   int32_t num_query_tokens, int32_t max_query_len,

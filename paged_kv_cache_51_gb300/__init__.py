@@ -39,7 +39,8 @@ EXPORTS = (
     "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_num_free", "pkv_pool_can_allocate",
     "pkv_seq_add", "pkv_seq_fork", "pkv_seq_append_slot", "pkv_seq_free", "pkv_seq_len",
     "pkv_block_ref_count", "pkv_block_tables", "pkv_copy_blocks", "paged_kv_append",
-    "pkv_decode_workspace_bytes", "paged_attention_decode", "pkv_varlen_workspace_bytes",
+    "pkv_decode_workspace_bytes", "paged_attention_decode", "paged_attention_decode_noalloc",
+    "pkv_varlen_workspace_bytes",
     "paged_attention_varlen", "pkv_device_error", "pkv_status_string",
 )
 
@@ -86,6 +87,8 @@ def lib():
         "pkv_decode_workspace_bytes": (sz, [P(CacheDesc), i32, i32]),
         "paged_attention_decode": (ctypes.c_int, [p, p, p, p, P(CacheDesc), p, i32, p, i32, i32,
                                                   ctypes.c_float, p, sz, p]),
+        "paged_attention_decode_noalloc": (ctypes.c_int, [p, p, p, p, P(CacheDesc), p, i32, p,
+                                                          i32, i32, ctypes.c_float, p]),
         "pkv_varlen_workspace_bytes": (sz, [P(CacheDesc), i32, i32, i32, i32]),
         "paged_attention_varlen": (ctypes.c_int, [p, p, p, p, P(CacheDesc), p, i32, p, p, i32,
                                                   i32, i32, i32, ctypes.c_float, p, sz, p]),
@@ -283,6 +286,32 @@ def paged_attention_decode(out, q, k_cache, v_cache, desc, block_tables, context
                                         block_tables.shape[1], _ptr(context_lens), S,
                                         max_context_len, scale, _ptr(ws), ws.numel(),
                                         _stream(stream)), "paged_attention_decode")
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def paged_attention_decode_noalloc(out, q, k_cache, v_cache, desc, block_tables, context_lens,
+                                   max_context_len, scale=None, stream=None):
+    """paged_attention_decode without a workspace argument, for callers that cannot
+    allocate device memory when they call (see include/pagedkv.h).  The library
+    keeps a fixed NOALLOC_SCRATCH_BYTES scratch area per device instead; batches
+    whose split partials need more raise PagedKVError(PKV_ERR_WORKSPACE).  Calls
+    share that area, so calls that overlap on the GPU race: serialize them."""
+    S = q.shape[0]
+    dt = _TORCH_DTYPE[desc.dtype]
+    for t, nm in ((out, "out"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, dt, nm)
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    if scale is None:
+        scale = 1.0 / math.sqrt(desc.head_dim)
+    _check(lib().paged_attention_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                                ctypes.byref(desc), _ptr(block_tables),
+                                                block_tables.shape[1], _ptr(context_lens), S,
+                                                max_context_len, scale, _stream(stream)),
+           "paged_attention_decode_noalloc")
     return out
 
 
