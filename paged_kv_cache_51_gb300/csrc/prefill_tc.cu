@@ -1,16 +1,620 @@
-// Prefill-chunk attention for ragged mixed batches (placeholder until the
-// tensor-core kernel lands): reports the shape as unsupported.
+// Prefill-chunk attention on the tcgen05 tensor cores (ragged mixed batches).
+//
+// What is computed: for a chunk of qlen new tokens of one sequence whose K/V
+// are already appended after a cached prefix, query i attends causally to keys
+// 0 .. ctx - qlen + i ("第 15 章：推理引擎与部署" §15.6 两阶段与 Chunked Prefill;
+// "DeepSpeed-FastGen 深度解析" §3.2 动态分割融合).  Softmax is exact and is
+// accumulated tile by tile with the online recurrence of §15.1 算法详解
+// (running max m, running sum l, O rescaled by alpha), in base 2.
+//
+// Both products are dense contractions, so they run on the 5th-generation
+// tensor cores:
+//   S = Q K^T   M = 128 query rows, N = 128 keys, K = 128 dims
+//   O += P V    M = 128 query rows, N = 128 dims, K = 128 keys
+// with bf16 operands in shared memory and fp32 accumulators in TMEM.
+//
+// Tile shapes.  A tile's 128 rows are 128/G tokens x the G query heads of one
+// KV head (GQA packing, "大模型部署.md" §4.1 4. MQA 与 GQA), so every K/V byte
+// staged is used by all G heads.  A key tile is 8 paged blocks (128 keys).
+// Operands use the 128-byte-swizzled K-major layout (Q, K, P) and the 128-byte
+// swizzled MN-major layout (V); TMA tensor copies write K and V blocks straight
+// into that layout, one (block, 64-dim half) box of 16 x 128 B per copy.
+//
+// Warp roles (192 threads, one CTA per SM, persistent over work units):
+//   warps 0-3  one query row per thread: load Q, read S from TMEM, mask,
+//              online softmax, write P (bf16) to shared memory, rescale O in
+//              TMEM when the running max grows by more than 2^8, epilogue
+//   warp 4     TMA producer: K/V blocks of each key tile into a 2-stage ring
+//   warp 5     TMEM owner and MMA issuer (one thread issues tcgen05.mma)
+// Every wait is bounded; on a timeout the kernel records an error, stops
+// issuing work, drains its copies and MMAs and frees TMEM before it returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "pkv_device.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
+namespace {
 
-int prefill_supported(const pkv_cache_desc*) { return 0; }
+constexpr int kRows = 128;                   // query rows per tile
+constexpr int kDim = 128;                    // head dim
+constexpr int kKeys = 128;                   // keys per key tile
+constexpr int kBlkPerTile = kKeys / kBlockTokens;  // 8 cache blocks
+constexpr int kStages = 2;
+constexpr int kSub = kRows * 128;            // one 64-column half of a 128-row operand (16 KiB)
+constexpr int kQOff = 0;                     // Q: 2 halves (dims 0-63, 64-127)
+constexpr int kPOff = 2 * kSub;              // P: 2 halves (keys 0-63, 64-127)
+constexpr int kKVOff = 4 * kSub;             // stages
+constexpr int kKBytes = 2 * kKeys * 128;     // K of one stage (2 halves of 128 key rows x 128 B)
+constexpr int kStageBytes = 2 * kKBytes;     // K + V
+constexpr int kBarOff = kKVOff + kStages * kStageBytes;
+constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + 1 KiB alignment slack
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;          // S double buffer (2 x 128) + O (128)
+constexpr uint32_t kOCol = 256;
+constexpr float kRescaleThreshold = 8.0f;    // log2 units: rescale O only when max grows > 2^8
+constexpr int kBoxBytes = kBlockTokens * 128;  // one TMA box: 16 rows x 64 bf16
+
+// barrier indices
+enum {
+    B_KV_FULL = 0,
+    B_KV_EMPTY = B_KV_FULL + kStages,
+    B_S_FULL = B_KV_EMPTY + kStages,
+    B_S_EMPTY = B_S_FULL + 2,
+    B_P_FULL = B_S_EMPTY + 2,
+    B_O_DONE,
+    B_Q_FULL,
+    B_O_EMPTY,
+    B_DRAIN,
+    B_COUNT
+};
+
+// instruction descriptor, kind::f16: bf16 x bf16 -> fp32, M = 128, N = 128
+constexpr uint32_t idesc_bf16(bool b_mn_major) {
+    return (1u << 4)                        // D format: f32
+           | (1u << 7)                      // A format: bf16
+           | (1u << 10)                     // B format: bf16
+           | (0u << 15)                     // A K-major
+           | ((b_mn_major ? 1u : 0u) << 16) // B K-major / MN-major
+           | (uint32_t(kKeys >> 3) << 17)   // N / 8
+           | (uint32_t(kRows >> 4) << 24);  // M / 16
+}
+constexpr uint32_t kIdescQK = idesc_bf16(false);
+constexpr uint32_t kIdescPV = idesc_bf16(true);
+
+// shared-memory matrix descriptor, 128-byte swizzle
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= uint64_t((saddr >> 4) & 0x3FFFu);
+    d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
+    d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
+    d |= uint64_t(1) << 46;  // descriptor version for tcgen05
+    d |= uint64_t(2) << 61;  // SWIZZLE_128B
+    return d;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                     uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+#define PKV_R32(r)                                                                              \
+    "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),         \
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), \
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),           \
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),           \
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+#define PKV_W32(r)                                                                          \
+    "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), \
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),   \
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), \
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), \
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+
+// 32 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : PKV_R32(r)
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+            taddr),
+        PKV_W32(r)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);  // a -> low half, b -> high half
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// byte offset of 16-byte chunk `c` (0..7) of row `r` in a 128-byte-swizzled half
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+    return uint32_t(r) * 128u + uint32_t((c ^ (r & 7)) << 4);
+}
+
+struct PrefillParams {
+    const __nv_bfloat16* q;
+    __nv_bfloat16* out;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    const int32_t* query_start_loc;
+    const int2* items;
+    const int32_t* n_items;
+    int32_t table_stride;
+    int32_t num_blocks;
+    int32_t num_kv_heads;
+    int32_t num_q_heads;
+    int32_t group;
+    int32_t tokens_per_tile;
+    float scale_log2;
+    int* err;
+};
+
+// Per-unit geometry shared by all roles.
+struct Unit {
+    int seq, kvh, q0, qlen, ctx, t0, nt, n_keys, n_tiles, nblk;
+};
+
+__device__ __forceinline__ Unit unit_of(const PrefillParams& p, int u) {
+    Unit x;
+    const int2 item = p.items[u / p.num_kv_heads];
+    x.kvh = u % p.num_kv_heads;
+    x.seq = item.x;
+    x.q0 = p.query_start_loc[x.seq];
+    x.qlen = p.query_start_loc[x.seq + 1] - x.q0;
+    x.ctx = p.context_lens[x.seq];
+    x.t0 = item.y * p.tokens_per_tile;
+    x.nt = min(p.tokens_per_tile, x.qlen - x.t0);
+    x.n_keys = x.ctx - x.qlen + x.t0 + x.nt;  // keys visible to the tile's last token
+    x.n_tiles = (x.n_keys + kKeys - 1) / kKeys;
+    x.nblk = (x.n_keys + kBlockTokens - 1) / kBlockTokens;
+    return x;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                   const __grid_constant__ CUtensorMap tmap_v, PrefillParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;           // 1 KiB aligned for the swizzle
+    unsigned char* smem = smem_raw + (base - raw);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + B_COUNT * 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + B_COUNT * 8 + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_units = p.n_items[0] * p.num_kv_heads;
+
+    // zero the operand area once so no stale bit pattern can be NaN
+    for (int i = threadIdx.x; i < kBarOff / 16; i += kThreads)
+        reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars[B_KV_FULL + s], 1);
+            mbar_init(&bars[B_KV_EMPTY + s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars[B_S_FULL + s], 1);
+            mbar_init(&bars[B_S_EMPTY + s], 4);
+        }
+        mbar_init(&bars[B_P_FULL], 4);
+        mbar_init(&bars[B_O_DONE], 1);
+        mbar_init(&bars[B_Q_FULL], 4);
+        mbar_init(&bars[B_O_EMPTY], 4);
+        mbar_init(&bars[B_DRAIN], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_async_smem();
+    tc_before();
+    __syncthreads();
+    tc_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        // ------------------------------ TMA producer ------------------------------
+        uint32_t kt = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            const Unit x = unit_of(p, u);
+            const int32_t* bt = p.block_tables + size_t(x.seq) * p.table_stride;
+            for (int j = 0; j < x.n_tiles && ok; ++j, ++kt) {
+                const int st = kt % kStages;
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&bars[B_KV_EMPTY + st], ((kt / kStages) & 1) ^ 1, p.err));
+                if (!ok || *abort_flag) {
+                    ok = false;
+                    break;
+                }
+                const int nb = min(kBlkPerTile, x.nblk - j * kBlkPerTile);
+                int blk = -1;
+                if (lane < nb) blk = bt[j * kBlkPerTile + lane];
+                const bool good = lane < nb && blk >= 0 && blk < p.num_blocks;
+                if (lane < nb && !good) flag_error(p.err, PKV_DEV_BAD_BLOCK_ID);
+                const unsigned mask = __ballot_sync(0xffffffffu, good);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bars[B_KV_FULL + st],
+                                          uint32_t(__popc(mask)) * 4u * kBoxBytes);
+                }
+                __syncwarp();
+                if (good) {
+                    // each lane issues its own block's four boxes
+                    const uint32_t sk = base + kKVOff + st * kStageBytes;
+                    const int row = (blk * p.num_kv_heads + x.kvh) * kBlockTokens;
+                    const uint32_t off = uint32_t(lane) * kBoxBytes;
+                    tma_load_2d(sk + off, &tmap_k, 0, row, &bars[B_KV_FULL + st]);
+                    tma_load_2d(sk + kKeys * 128 + off, &tmap_k, 64, row, &bars[B_KV_FULL + st]);
+                    tma_load_2d(sk + kKBytes + off, &tmap_v, 0, row, &bars[B_KV_FULL + st]);
+                    tma_load_2d(sk + kKBytes + kKeys * 128 + off, &tmap_v, 64, row,
+                                &bars[B_KV_FULL + st]);
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok) *abort_flag = 1;
+        // never leave with copies in flight: wait for the last fill of each stage
+        if (lane == 0) {
+            for (int k = 0; k < kStages && uint32_t(k) < kt; ++k) {
+                const uint32_t last = kt - 1 - k;
+                mbar_wait(&bars[B_KV_FULL + last % kStages], (last / kStages) & 1, p.err);
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------ MMA issuer ------------------------------
+        if (lane == 0) {
+            uint32_t kt = 0, it = 0;
+            bool ok = true;
+            const uint32_t q_addr = base + kQOff, p_addr = base + kPOff;
+            auto pv = [&](uint32_t g, int j) -> bool {
+                if (!mbar_wait(&bars[B_P_FULL], g & 1, p.err)) return false;
+                if (j == 0 && !mbar_wait(&bars[B_O_EMPTY], (it & 1) ^ 1, p.err)) return false;
+                tc_after();
+                const uint32_t vs = base + kKVOff + (g % kStages) * kStageBytes + kKBytes;
+#pragma unroll
+                for (int kk = 0; kk < kKeys / 16; ++kk) {
+                    const uint64_t a = sdesc(p_addr + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b = sdesc(vs + kk * 16 * 128, kKeys * 128, 1024);
+                    umma(tmem + kOCol, a, b, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(&bars[B_O_DONE]);
+                umma_commit(&bars[B_KV_EMPTY + g % kStages]);
+                return true;
+            };
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++it) {
+                const Unit x = unit_of(p, u);
+                ok = mbar_wait(&bars[B_Q_FULL], it & 1, p.err) && !*abort_flag;
+                if (!ok) break;
+                tc_after();
+                for (int j = 0; j < x.n_tiles && ok; ++j) {
+                    const uint32_t g = kt + j;
+                    ok = mbar_wait(&bars[B_KV_FULL + g % kStages], (g / kStages) & 1, p.err) &&
+                         mbar_wait(&bars[B_S_EMPTY + (g & 1)], ((g >> 1) & 1) ^ 1, p.err) &&
+                         !*abort_flag;
+                    if (!ok) break;
+                    tc_after();
+                    const uint32_t ks = base + kKVOff + (g % kStages) * kStageBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kDim / 16; ++kk) {
+                        const uint64_t a = sdesc(q_addr + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
+                        const uint64_t b = sdesc(ks + (kk >> 2) * (kKeys * 128) + (kk & 3) * 32, 16,
+                                                 1024);
+                        umma(tmem + (g & 1) * kKeys, a, b, kIdescQK, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(&bars[B_S_FULL + (g & 1)]);
+                    if (j > 0) ok = pv(g - 1, j - 1) && !*abort_flag;
+                }
+                if (ok) ok = pv(kt + x.n_tiles - 1, x.n_tiles - 1);
+                kt += x.n_tiles;
+            }
+            if (!ok) *abort_flag = 1;
+            // wait until every MMA issued here has completed before TMEM is freed
+            umma_commit(&bars[B_DRAIN]);
+            mbar_wait(&bars[B_DRAIN], 0, p.err);
+        }
+        __syncwarp();
+    } else {
+        // ------------------- softmax / correction / epilogue (rows) -------------------
+        const int r = threadIdx.x;                      // query row = TMEM lane
+        const uint32_t lane_base = uint32_t(warp * 32) << 16;
+        const int G = p.group;
+        uint32_t kt = 0, it = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
+            const Unit x = unit_of(p, u);
+            const int tok = r / G, g_head = r % G;
+            const bool row_valid = tok < x.nt;
+            const int t = x.t0 + tok;
+            const int limit = row_valid ? x.ctx - x.qlen + t : x.ctx - 1;  // last visible key
+            // ---- Q row -> shared memory (swizzled K-major) ----
+            {
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    p.q + (size_t(x.q0 + t) * p.num_q_heads + x.kvh * G + g_head) * kDim);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const uint4 v = row_valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4*>(smem + kQOff + (c >> 3) * kSub + swz(r, c & 7)) = v;
+                }
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_Q_FULL]);
+
+            float m_used = -INFINITY, l = 0.f;
+            for (int j = 0; j < x.n_tiles; ++j) {
+                const uint32_t g = kt + j;
+                if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_S_FULL + (g & 1)],
+                                                               (g >> 1) & 1, p.err));
+                if (!ok || *abort_flag) {
+                    ok = false;
+                    break;
+                }
+                tc_after();
+                float s[kKeys];
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_base + (g & 1) * kKeys + c4 * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s[c4 * 32 + i] = __uint_as_float(v[i]);
+                }
+                tc_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_S_EMPTY + (g & 1)]);
+
+                // scale to log2 units and mask keys beyond this row's causal limit
+                const int key0 = j * kKeys;
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < kKeys; ++c) {
+                    s[c] = (key0 + c <= limit) ? s[c] * p.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, s[c]);
+                }
+                const float m_new = fmaxf(m_used, mx);
+                const bool need = m_new > m_used + kRescaleThreshold;  // always on the first tile
+                const bool warp_need = __any_sync(0xffffffffu, need);
+                float alpha = 1.f;
+                if (need) {
+                    alpha = exp2f(m_used - m_new);  // 0 on the first tile (O, l still empty)
+                    m_used = m_new;
+                    l *= alpha;
+                }
+                if (j > 0) {
+                    // PV of the previous tile must be done: P buffer free, O current
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE], (g - 1) & 1, p.err));
+                    if (!ok) break;
+                    tc_after();
+                    if (warp_need) {
+#pragma unroll 1
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            uint32_t v[32];
+                            const uint32_t ta = tmem + lane_base + kOCol + c4 * 32;
+                            tmem_ld32(ta, v);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                            tmem_st32(ta, v);
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                // P = 2^(s - m) in bf16, row r of the K-major swizzled P tile
+                float rowsum = 0.f;
+#pragma unroll
+                for (int c8 = 0; c8 < 16; ++c8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float p0 = exp2f(s[c8 * 8 + 2 * e] - m_used);
+                        const float p1 = exp2f(s[c8 * 8 + 2 * e + 1] - m_used);
+                        rowsum += p0 + p1;
+                        w[e] = pack_bf16(p0, p1);
+                    }
+                    *reinterpret_cast<uint4*>(smem + kPOff + (c8 >> 3) * kSub + swz(r, c8 & 7)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                l += rowsum;
+                // rows of the last staged block that lie beyond the context were
+                // never written: zero their V so 0 * (anything) cannot become NaN
+                const int rows_last = x.ctx - (x.nblk - 1) * kBlockTokens;  // valid rows, 1..16+
+                if (j == x.n_tiles - 1 && rows_last < kBlockTokens) {
+                    const int slot = (x.nblk - 1) - j * kBlkPerTile;
+                    const int nz = (kBlockTokens - rows_last) * 2 * 8;  // rows x halves x chunks
+                    unsigned char* vs = smem + kKVOff + (g % kStages) * kStageBytes + kKBytes;
+                    for (int i = r; i < nz; i += 128) {
+                        const int row = rows_last + i / 16, half = (i / 8) & 1, c = i & 7;
+                        *reinterpret_cast<uint4*>(vs + half * (kKeys * 128) +
+                                                  (slot * kBlockTokens + row) * 128 + c * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                }
+                fence_async_smem();
+                tc_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_P_FULL]);
+            }
+            if (!ok) break;
+            // ---- epilogue: O / l -> out ----
+            const uint32_t glast = kt + x.n_tiles - 1;
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE], glast & 1, p.err));
+            if (!ok) break;
+            tc_after();
+            const float inv = 1.f / l;
+            uint4* dst = reinterpret_cast<uint4*>(
+                p.out + (size_t(x.q0 + t) * p.num_q_heads + x.kvh * G + g_head) * kDim);
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + kOCol + c4 * 32, v);
+                tmem_wait_ld();
+                if (row_valid) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            w[k] = pack_bf16(__uint_as_float(v[e * 8 + 2 * k]) * inv,
+                                             __uint_as_float(v[e * 8 + 2 * k + 1]) * inv);
+                        dst[c4 * 4 + e] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+            tc_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_O_EMPTY]);
+            kt += x.n_tiles;
+        }
+        if (!ok) *abort_flag = 1;
+    }
+
+    tc_before();
+    __syncthreads();
+    tc_after();
+    if (warp == 5) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// ---- host side -------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// The cache viewed as 2-D [num_blocks * Hkv * 16 rows][128 dims] of bf16; a
+// box is 16 rows (one block of one head) x 64 dims, written 128-byte swizzled.
+bool make_cache_map(CUtensorMap* m, const void* cache, const pkv_cache_desc* d) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t rows = cuuint64_t(d->num_blocks) * d->num_kv_heads * kBlockTokens;
+    const cuuint64_t gdim[2] = {cuuint64_t(kDim), rows};
+    const cuuint64_t gstride[1] = {cuuint64_t(kDim) * 2};
+    const cuuint32_t box[2] = {64, cuuint32_t(kBlockTokens)};
+    const cuuint32_t estride[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), gdim, gstride, box,
+              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+}  // namespace
+
+int prefill_supported(const pkv_cache_desc* d) {
+    const int g = d->num_q_heads / d->num_kv_heads;
+    return d->dtype == PKV_BF16 && d->head_dim == kDim && d->block_size == kBlockTokens &&
+           (g == 1 || g == 2 || g == 4 || g == 8) &&
+           int64_t(d->num_blocks) * d->num_kv_heads * kBlockTokens < (int64_t(1) << 31);
+}
 
 int prefill_item_bound(int32_t num_seqs, int32_t num_query_tokens, int32_t group) {
     const int32_t tokens_per_tile = kPrefillRows / group;
     return ceil_div(num_query_tokens, tokens_per_tile) + num_seqs;
 }
 
-int launch_prefill(const AttnArgs&) { return PKV_ERR_UNSUPPORTED; }
+int launch_prefill(const AttnArgs& a) {
+    const pkv_cache_desc* d = a.desc;
+    if (!prefill_supported(d)) return PKV_ERR_UNSUPPORTED;
+    CUtensorMap mk, mv;
+    if (!make_cache_map(&mk, a.k_cache, d) || !make_cache_map(&mv, a.v_cache, d))
+        return PKV_ERR_CUDA;
+    PrefillParams p;
+    p.q = static_cast<const __nv_bfloat16*>(a.q);
+    p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.block_tables = a.block_tables;
+    p.context_lens = a.context_lens;
+    p.query_start_loc = a.query_start_loc;
+    p.items = a.ws.prefill_items;
+    p.n_items = a.ws.counters + 1;
+    p.table_stride = a.table_stride;
+    p.num_blocks = d->num_blocks;
+    p.num_kv_heads = d->num_kv_heads;
+    p.num_q_heads = d->num_q_heads;
+    p.group = d->num_q_heads / d->num_kv_heads;
+    p.tokens_per_tile = kPrefillRows / p.group;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.err = a.err;
+    if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    const int64_t bound = int64_t(a.ws.max_prefill_items) * d->num_kv_heads;
+    const int64_t grid = std::min<int64_t>(sm_count(), bound);
+    if (grid < 1) return PKV_OK;
+    prefill_kernel<<<unsigned(grid), kThreads, kSmemBytes, a.stream>>>(mk, mv, p);
+    return cuda_status(cudaGetLastError());
+}
 
 }  // namespace pkv

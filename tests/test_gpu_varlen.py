@@ -1,0 +1,113 @@
+"""GPU parity for ragged mixed batches (prefill chunks on tcgen05 + decode rows) vs the oracle."""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import workloads  # noqa: E402
+from oracle.run import execute  # noqa: E402
+from tests.gpu_parity import TOL, cache_bytes_equal, errors, out_f64, run_both  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rt(lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_51_gb300 import runner
+
+    lib.device_error(clear=True)
+    return runner
+
+
+def _check(w, rt, lib, rows=None):
+    ost, oout, dc, step, out = run_both(w, rt)
+    assert lib.device_error() == 0
+    assert cache_bytes_equal(dc.k_cache, ost.k_cache), "K cache bytes differ"
+    assert cache_bytes_equal(dc.v_cache, ost.v_cache), "V cache bytes differ"
+    got = out_f64(out)
+    live = ~np.isnan(oout[:, 0, 0])          # rows that belong to a sequence
+    d = np.abs(got[live] - oout[live])
+    tmax, tmean = TOL[w.dtype]
+    assert float(d.max()) <= tmax and float(d.mean()) <= tmean, (float(d.max()), float(d.mean()))
+    return ost, oout, dc, step, out
+
+
+def test_config4_splitfuse_2048_full(rt, lib):
+    ost, oout, dc, step, out = _check(workloads.config4(), rt, lib)
+    # the batch is 3 chunks of 512 + 512 decode rows = 2048 query tokens
+    assert step.q.shape[0] == 2048 and step.max_qlen == 512
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (32, 8), (64, 8)])
+def test_ragged_spans_every_group_size(rt, lib, hq, hkv):
+    spans = [(0, 2), (5, 3), (100, 129), (17, 16), (300, 1), (1000, 300), (0, 1), (33, 64),
+             (2047, 130)]
+    _check(workloads.random_varlen(11, "bf16", hq, hkv, 128, 16, spans, scale=0.5), rt, lib)
+
+
+def test_chunk_ending_mid_block_and_long_prefix(rt, lib):
+    spans = [(4093, 7), (4096, 17), (12, 500), (1, 1)]
+    _check(workloads.random_varlen(12, "bf16", 32, 8, 128, 16, spans, scale=0.5), rt, lib)
+
+
+def test_sequence_without_queries_is_skipped(rt, lib):
+    spans = [(40, 0), (20, 9), (64, 0), (7, 1)]
+    _check(workloads.random_varlen(13, "bf16", 16, 4, 128, 16, spans, scale=0.5), rt, lib)
+
+
+def test_never_written_rows_may_hold_nan(rt, lib):
+    """Rows of a last block beyond the context were never written; their contents
+    (here NaN) must not reach any output."""
+    from paged_kv_cache_51_gb300 import runner
+
+    spans = [(0, 20), (5, 3), (33, 100), (300, 1), (44, 1)]
+    w = workloads.random_varlen(14, "bf16", 32, 8, 128, 16, spans, scale=0.5)
+    _, ref = execute(w)
+    dc = runner.DeviceCache(w)
+    dc.k_cache.fill_(float("nan"))
+    dc.v_cache.fill_(float("nan"))
+    dc.run_setup()
+    step = runner.Step(dc, dc.plan_step())
+    out = step.run()
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0
+    got = out_f64(out)
+    assert np.isfinite(got).all()
+    mx, mean = errors(out, ref)
+    assert mx <= TOL["bf16"][0] and mean <= TOL["bf16"][1]
+
+
+def test_large_scores_use_lazy_rescale_correctly(rt, lib):
+    # scale 6: scores of a few hundred; the running max keeps growing across tiles
+    spans = [(600, 200), (0, 256)]
+    w = workloads.random_varlen(15, "bf16", 32, 8, 128, 16, spans, scale=3.0)
+    ost, oout, dc, step, out = run_both(w, rt)
+    assert lib.device_error() == 0
+    got = out_f64(out)
+    assert np.isfinite(got).all()
+    # values up to ~10 in magnitude: compare relative to the output scale
+    d = np.abs(got - oout)
+    assert float(d.max()) <= 2e-2 * max(1.0, float(np.abs(oout).max()))
+
+
+def test_unsupported_prefill_shapes_are_refused(rt, lib):
+    from paged_kv_cache_51_gb300 import PagedKVError, paged_attention_varlen
+
+    w = workloads.random_varlen(16, "f32", 8, 8, 64, 16, [(3, 4)])
+    dc = rt.DeviceCache(w)
+    dc.run_setup()
+    step = rt.Step(dc, dc.plan_step())
+    with pytest.raises(PagedKVError) as e:
+        step.run()
+    assert e.value.status == lib.PKV_ERR_UNSUPPORTED
+    # decode rows alone are fine in fp32
+    out = torch.empty_like(step.q)
+    qsl = torch.tensor([0, 1], dtype=torch.int32, device="cuda")
+    ctx = torch.tensor([7], dtype=torch.int32, device="cuda")
+    paged_attention_varlen(out, step.q[:1].contiguous(), dc.k_cache, dc.v_cache, dc.desc,
+                           step.tables, qsl, ctx, 1, 7)
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0
