@@ -227,6 +227,101 @@ def run_reference(args):
 # ----------------------------------------------------------------------------
 # GPU arm
 # ----------------------------------------------------------------------------
+def accounting(w, step):
+    """Algorithmic bytes and flops of one step of a prepared workload."""
+    ctx = [int(c) for c in step.ctx.cpu().tolist()]
+    qlens = [q for _, q in w.batch]
+    es, hkv, hq, d, bs = w.elem_bytes, w.num_kv_heads, w.num_q_heads, w.head_dim, w.block_size
+    kv = sum(c for c, q in zip(ctx, qlens) if q > 0) * hkv * d * es * 2
+    qo = sum(qlens) * hq * d * es * 2
+    tables = sum(math.ceil(c / bs) for c in ctx) * 4 + 4 * len(ctx)
+    if max(qlens) > 1:
+        tables += 4 * (len(ctx) + 1)
+    pre_flops = sum(4 * d * hq * sum(c - q + i + 1 for i in range(q))
+                    for c, q in zip(ctx, qlens) if q >= 2)
+    dec_flops = sum(4 * d * hq * c for c, q in zip(ctx, qlens) if q == 1)
+    pre_kv = sum(c for c, q in zip(ctx, qlens) if q >= 2) * hkv * d * es * 2
+    return {"attn_bytes": kv + qo + tables, "append_bytes": append_bytes(
+        w, step.slot_mapping.numel(), step.pairs.shape[0]), "prefill_flops": pre_flops,
+        "decode_flops": dec_flops, "prefill_kv_bytes": pre_kv, "query_tokens": sum(qlens),
+        "context_tokens": sum(ctx)}
+
+
+def time_steps(step, steps, warmup):
+    """Device time of `steps` steps and the mean time of the attention call inside them."""
+    import torch
+
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        step.run()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    a_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(steps)]
+    ev0.record(stream)
+    for i in range(steps):
+        step.write_kv()
+        a_ev[i][0].record(stream)
+        step.attend()
+        a_ev[i][1].record(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    return ev0.elapsed_time(ev1) / steps, statistics.mean(a.elapsed_time(b) for a, b in a_ev)
+
+
+def peaks():
+    bw, kind = measured_peak()
+    tc, tc_kind = 1900.0, "fallback"
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tc, tc_kind = float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        pass
+    return bw, kind, tc, tc_kind
+
+
+def mixed_batch_summary(steps, warmup):
+    """The SplitFuse 2048-token step (config 4) and its prefill chunks alone."""
+    import torch
+
+    import paged_kv_cache_51_gb300 as pkv
+    import workloads
+    from paged_kv_cache_51_gb300 import runner
+
+    bw, _, tc, _ = peaks()
+    w = workloads.config4()
+    dc, step = runner.prepare(w)
+    acc = accounting(w, step)
+    ms, attn_ms = time_steps(step, steps, warmup)
+    if pkv.device_error() != 0:
+        raise SystemExit("device error in the mixed batch")
+    total_bytes = acc["attn_bytes"] + acc["append_bytes"]
+    t_roof = max(total_bytes / (bw * 1e9), acc["prefill_flops"] / (tc * 1e12))
+    del dc, step
+    torch.cuda.empty_cache()
+    # prefill chunks alone: tensor-core throughput of the tcgen05 kernel
+    spans = [(p, 512) for p in w.notes["prefixes"]]
+    wp = workloads.random_varlen(1, "bf16", 32, 8, 128, 16, spans, scale=0.5)
+    dcp, stp = runner.prepare(wp)
+    accp = accounting(wp, stp)
+    _, pre_ms = time_steps(stp, steps, warmup)
+    del dcp, stp
+    torch.cuda.empty_cache()
+    return {
+        "workload": w.name, "query_tokens": acc["query_tokens"], "ms_per_step": ms,
+        "tokens_per_s": acc["query_tokens"] / (ms * 1e-3),
+        "attention_ms": attn_ms, "bytes_per_step": total_bytes,
+        "prefill_gflop": acc["prefill_flops"] / 1e9,
+        "roofline_ms": t_roof * 1e3, "roofline_frac": t_roof / (ms * 1e-3),
+        "roofline_note": "max(bytes / HBM peak, prefill flops / bf16 peak) over the step time",
+        "prefill_chunks_alone": {
+            "spans": spans, "ms": pre_ms, "tflops": accp["prefill_flops"] / (pre_ms * 1e-3) / 1e12,
+            "tensor_frac": accp["prefill_flops"] / (pre_ms * 1e-3) / (tc * 1e12),
+            "note": "attention call on the three 512-token chunks only (planner + tcgen05 kernel)"},
+    }
+
+
 def run_gpu(args):
     import torch
 
@@ -250,10 +345,9 @@ def run_gpu(args):
     kw = {"batch": args.batch} if args.batch and args.config in (2, 3) else {}
     w = workloads.make(args.config, seed=rank, **kw)
     dc, step = runner.prepare(w)
-    ctx_host = step.ctx.cpu().tolist()
-    attn_b = attention_bytes(w, ctx_host)
-    app_b = append_bytes(w, step.slot_mapping.numel(), step.pairs.shape[0])
-    step_bytes = attn_b + app_b
+    acc = accounting(w, step)
+    attn_b = acc["attn_bytes"]
+    step_bytes = attn_b + acc["append_bytes"]
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
@@ -267,35 +361,23 @@ def run_gpu(args):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    a_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(args.steps)]
     t_wall0 = time.time()
-    ev0.record(stream)
-    for i in range(args.steps):
-        step.write_kv()
-        a_ev[i][0].record(stream)
-        step.attend()
-        a_ev[i][1].record(stream)
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    ms_per_step, attn_ms = time_steps(step, args.steps, 0)
     t_wall1 = time.time()
     if dist:
         dist.barrier()
     sampler.stop()
-    total_ms = ev0.elapsed_time(ev1)
-    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in a_ev)
     if dist:
-        t = torch.tensor([total_ms], device="cuda")
+        t = torch.tensor([ms_per_step], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+        ms_per_step = float(t.item())
     if pkv.device_error() != 0:
         raise SystemExit("device error during the timed region")
 
     # ---- end to end through host buffers ----
     host_in = {name: getattr(step, name).cpu().pin_memory()
-               for name in ("q", "k_new", "v_new", "slot_mapping", "tables", "ctx", "pairs")}
+               for name in ("q", "k_new", "v_new", "slot_mapping", "tables", "ctx", "qsl",
+                            "pairs")}
     host_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = host_out.numel() * host_out.element_size()
@@ -319,18 +401,24 @@ def run_gpu(args):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / k_e2e
 
-    ms_per_step = total_ms / args.steps
     value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
-    peak, peak_kind = measured_peak()
+    peak, peak_kind, tc_peak, _ = peaks()
     achieved = attn_b / (attn_ms * 1e-3) / 1e9
-    launches_per_step = (1 if step.pairs.shape[0] else 0) + 1 + 2 + (
-        1 if math.ceil(step.max_ctx / 512) > 1 else 0)
+    launches_per_step = ((1 if step.pairs.shape[0] else 0) + 1 + 2
+                         + (1 if math.ceil(step.max_ctx / 512) > 1 else 0)
+                         + (1 if step.max_qlen > 1 else 0))
     clocks = sampler.summary(t_wall0, t_wall1)
+    del dc, step
+    torch.cuda.empty_cache()
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return 0
-    cpu = cpu_baseline(args.config) if world == 1 and not args.no_cpu else None
+    mixed = None
+    if world == 1 and args.config == 2 and not args.no_mixed:
+        mixed = mixed_batch_summary(min(args.steps, 200), args.warmup)
+    cpu = cpu_baseline(args.config if args.config in (2, 3) else 2) if (
+        world == 1 and not args.no_cpu) else None
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -339,23 +427,33 @@ def run_gpu(args):
             "workload": w.name, "batch": len(w.batch), "num_q_heads": w.num_q_heads,
             "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
             "block_size": w.block_size, "num_blocks": w.num_blocks,
-            "context_tokens": int(sum(ctx_host)), "max_context": int(step.max_ctx),
-            "step": "copy-on-write + append of the step's tokens + paged decode attention",
+            "context_tokens": acc["context_tokens"], "query_tokens": acc["query_tokens"],
+            "step": "copy-on-write + append of the step's tokens + paged attention",
             "l2": f"inputs larger than L2 (KV {attn_b / 1e9:.2f} GB read per step vs 129 MB L2)",
             "parallelism": f"replicas x{world}",
         },
         "pct_hbm_peak": achieved / peak,
+        "tokens_per_s": acc["query_tokens"] * world / (ms_per_step * 1e-3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": ncu_traffic("decode.cu"),
-                     "kernel": "paged_attention_decode (plan + split + merge)",
+                     "frac": achieved / peak,
+                     "traffic": ncu_traffic("decode.cu") if args.config == 2 and not args.batch
+                     else None,
+                     "kernel": "paged attention call (planner + split + merge"
+                               + (" + tcgen05 prefill)" if acc["prefill_flops"] else ")"),
                      "bytes_per_launch": attn_b, "ms_per_launch": attn_ms,
                      "peak_kind": f"{peak_kind} hbm_gbs (burst copy)"},
+        "mixed_batch": mixed,
         "cpu_baseline": cpu,
         "e2e": {"value": step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
+    if acc["prefill_flops"]:
+        line["prefill_gflop_per_step"] = acc["prefill_flops"] / 1e9
+        t_roof = max((attn_b + acc["append_bytes"]) / (peak * 1e9),
+                     acc["prefill_flops"] / (tc_peak * 1e12))
+        line["step_roofline_frac"] = t_roof / (ms_per_step * 1e-3)
     print(json.dumps(line))
     if dist:
         dist.destroy_process_group()
@@ -372,6 +470,8 @@ def main():
     ap.add_argument("--batch", type=int, default=0,
                     help="sequences in the batch (decode workloads; 0 = the workload's own)")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-mixed", action="store_true",
+                    help="skip the mixed-batch (SplitFuse) sub-measurement")
     ap.add_argument("--cpu-worker", action="store_true")
     ap.add_argument("--cpu-seqs", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
