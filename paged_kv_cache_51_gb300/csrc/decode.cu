@@ -602,6 +602,7 @@ int launch_merge_t(const AttnArgs& a) {
 }  // namespace
 
 int launch_decode_split(const AttnArgs& a) {
+    if (decode_mma_eligible(a.desc)) return launch_decode_split_mma(a);
     const int g = a.desc->num_q_heads / a.desc->num_kv_heads;
     const bool bf = a.desc->dtype == PKV_BF16;
     if (a.desc->head_dim == 128)

@@ -74,6 +74,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
     return true;
 }
 
+// Order this thread's generic-proxy shared-memory accesses before later
+// async-proxy (TMA, tensor core) accesses of the same memory.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // 1-D bulk copy global -> shared (TMA engine), completing on `bar` with
 // `bytes` of transaction count.  src, dst 16-byte aligned; bytes % 16 == 0.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,

@@ -61,6 +61,13 @@ struct AttnArgs {
     int* err;
 };
 
+// tmap.cpp: tensor map of a bf16 cache viewed as 2-D [num_blocks * Hkv * bs rows][head_dim],
+// box = one block of one head (bs rows) x 64 dims, 128-byte swizzled in shared memory.
+bool make_cache_tensor_map(struct CUtensorMap_st* map, const void* cache, const pkv_cache_desc* d);
+
+// decode_mma.cu: tensor-core split kernel for bf16 GQA groups of 2, 4 or 8
+bool decode_mma_eligible(const pkv_cache_desc* d);
+int launch_decode_split_mma(const AttnArgs& a);
 // decode.cu
 int launch_plan(const AttnArgs& a);
 int launch_decode_split(const AttnArgs& a);

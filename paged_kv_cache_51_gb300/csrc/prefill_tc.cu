@@ -33,7 +33,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <mutex>
 
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
@@ -534,36 +533,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- host side -------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
-
-// The cache viewed as 2-D [num_blocks * Hkv * 16 rows][128 dims] of bf16; a
-// box is 16 rows (one block of one head) x 64 dims, written 128-byte swizzled.
-bool make_cache_map(CUtensorMap* m, const void* cache, const pkv_cache_desc* d) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t rows = cuuint64_t(d->num_blocks) * d->num_kv_heads * kBlockTokens;
-    const cuuint64_t gdim[2] = {cuuint64_t(kDim), rows};
-    const cuuint64_t gstride[1] = {cuuint64_t(kDim) * 2};
-    const cuuint32_t box[2] = {64, cuuint32_t(kBlockTokens)};
-    const cuuint32_t estride[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), gdim, gstride, box,
-              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
-}
-
 int sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -589,7 +558,7 @@ int launch_prefill(const AttnArgs& a) {
     const pkv_cache_desc* d = a.desc;
     if (!prefill_supported(d)) return PKV_ERR_UNSUPPORTED;
     CUtensorMap mk, mv;
-    if (!make_cache_map(&mk, a.k_cache, d) || !make_cache_map(&mv, a.v_cache, d))
+    if (!make_cache_tensor_map(&mk, a.k_cache, d) || !make_cache_tensor_map(&mv, a.v_cache, d))
         return PKV_ERR_CUDA;
     PrefillParams p;
     p.q = static_cast<const __nv_bfloat16*>(a.q);

@@ -1,0 +1,48 @@
+// Host helper: TMA tensor maps over a paged cache pool.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+}  // namespace
+
+// The pool [num_blocks][Hkv][bs][D] (bf16) as a 2-D tensor of rows of D
+// elements; a box is the bs rows of one (block, head) tile by 64 columns, so a
+// 128-dim tile is two boxes.  Copies land 128-byte swizzled (16-byte chunk c of
+// row r at chunk position c ^ (r % 8)), the layout the tensor-core operand
+// descriptors and conflict-free ldmatrix reads expect.
+bool make_cache_tensor_map(CUtensorMap* m, const void* cache, const pkv_cache_desc* d) {
+    auto fn = encode_fn();
+    if (!fn || d->dtype != PKV_BF16 || (d->head_dim != 64 && d->head_dim != 128)) return false;
+    const cuuint64_t rows = cuuint64_t(d->num_blocks) * d->num_kv_heads * d->block_size;
+    if (rows >= (cuuint64_t(1) << 31)) return false;
+    const cuuint64_t gdim[2] = {cuuint64_t(d->head_dim), rows};
+    const cuuint64_t gstride[1] = {cuuint64_t(d->head_dim) * 2};
+    const cuuint32_t box[2] = {64, cuuint32_t(d->block_size)};
+    const cuuint32_t estride[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), gdim, gstride, box,
+              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+}  // namespace pkv

@@ -197,3 +197,25 @@ def test_varlen_with_only_decode_rows_matches_decode(rt, lib):
     torch.cuda.synchronize()
     assert torch.equal(out_dec, out_var)
     assert lib.device_error() == 0
+
+
+@pytest.mark.parametrize("hq,hkv,dtype", [(8, 8, "bf16"), (32, 8, "bf16"), (64, 8, "bf16"),
+                                          (16, 8, "bf16"), (8, 8, "f32")])
+def test_never_written_rows_may_hold_nan_decode(rt, lib, hq, hkv, dtype):
+    """Rows of a partial last block past the context were never written; whatever they
+    hold (NaN here) must not reach the output of any decode path."""
+    from oracle.run import execute
+
+    w = workloads.random_decode(21, dtype, hq, hkv, 128, 16, [3, 17, 530, 1000], scale=0.5)
+    _, ref = execute(w)
+    dc = rt.DeviceCache(w)
+    dc.k_cache.fill_(float("nan"))
+    dc.v_cache.fill_(float("nan"))
+    dc.run_setup()
+    step = rt.Step(dc, dc.plan_step())
+    out = step.run()
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0
+    assert np.isfinite(out_f64(out)).all()
+    mx, mean = errors(out, ref)
+    assert mx <= TOL[dtype][0] and mean <= TOL[dtype][1]
