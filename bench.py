@@ -342,8 +342,13 @@ def run_gpu(args):
 
         dist.init_process_group("nccl")
 
-    kw = {"batch": args.batch} if args.batch and args.config in (2, 3) else {}
-    w = workloads.make(args.config, seed=rank, **kw)
+    if args.prefill_chunks:
+        # the three 512-token chunks of the SplitFuse batch (prefixes 0/1024/3072), no decode rows
+        w = workloads.random_varlen(rank, "bf16", 32, 8, 128, 16,
+                                    [(0, 512), (1024, 512), (3072, 512)], scale=0.5)
+    else:
+        kw = {"batch": args.batch} if args.batch and args.config in (2, 3) else {}
+        w = workloads.make(args.config, seed=rank, **kw)
     dc, step = runner.prepare(w)
     acc = accounting(w, step)
     attn_b = acc["attn_bytes"]
@@ -415,7 +420,7 @@ def run_gpu(args):
             dist.destroy_process_group()
         return 0
     mixed = None
-    if world == 1 and args.config == 2 and not args.no_mixed:
+    if world == 1 and args.config == 2 and not args.no_mixed and not args.prefill_chunks:
         mixed = mixed_batch_summary(min(args.steps, 200), args.warmup)
     cpu = cpu_baseline(args.config if args.config in (2, 3) else 2) if (
         world == 1 and not args.no_cpu) else None
@@ -454,6 +459,7 @@ def run_gpu(args):
         t_roof = max((attn_b + acc["append_bytes"]) / (peak * 1e9),
                      acc["prefill_flops"] / (tc_peak * 1e12))
         line["step_roofline_frac"] = t_roof / (ms_per_step * 1e-3)
+        line["prefill_tflops"] = acc["prefill_flops"] / (attn_ms * 1e-3) / 1e12
     print(json.dumps(line))
     if dist:
         dist.destroy_process_group()
@@ -469,6 +475,8 @@ def main():
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--batch", type=int, default=0,
                     help="sequences in the batch (decode workloads; 0 = the workload's own)")
+    ap.add_argument("--prefill-chunks", action="store_true",
+                    help="time only the SplitFuse batch's three 512-token prefill chunks")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-mixed", action="store_true",
                     help="skip the mixed-batch (SplitFuse) sub-measurement")

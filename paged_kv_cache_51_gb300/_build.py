@@ -25,6 +25,10 @@ CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-fvisibility=hidden", "-I",
              os.path.join(ROOT, "include")]
 
 
+# per-file extra flags: the prefill softmax uses the hardware exp2 directly
+EXTRA_FLAGS = {"prefill_tc.cu": ["--use_fast_math"]}
+
+
 def _nvcc():
     for cand in (os.environ.get("NVCC"), "/usr/local/cuda/bin/nvcc", "nvcc"):
         if cand and (os.path.isabs(cand) and os.path.exists(cand) or not os.path.isabs(cand)):
@@ -45,7 +49,7 @@ def _stamp(srcs, hdrs):
             h.update(f.encode() + fh.read())
     with open(os.path.join(ROOT, "include", "pagedkv.h"), "rb") as fh:
         h.update(fh.read())
-    h.update(" ".join(NVCC_FLAGS + CXX_FLAGS).encode())
+    h.update(" ".join(NVCC_FLAGS + CXX_FLAGS).encode() + repr(sorted(EXTRA_FLAGS.items())).encode())
     return h.hexdigest()
 
 
@@ -65,7 +69,7 @@ def build(force=False, verbose=False):
         obj = os.path.join(BUILD, src + ".o")
         path = os.path.join(CSRC, src)
         if src.endswith(".cu"):
-            cmd = [nvcc] + NVCC_FLAGS + ["-c", path, "-o", obj]
+            cmd = [nvcc] + NVCC_FLAGS + EXTRA_FLAGS.get(src, []) + ["-c", path, "-o", obj]
         else:
             cmd = ["g++"] + CXX_FLAGS + ["-c", path, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)

@@ -15,7 +15,7 @@
 #include <unordered_map>
 #include <vector>
 
-#include "../../include/pagedkv.h"
+#include "pagedkv.h"
 
 struct pkv_pool {
     int32_t num_blocks = 0;

@@ -5,7 +5,7 @@
 #include <cuda_bf16.h>
 #include <cstdint>
 
-#include "../../include/pagedkv.h"
+#include "pagedkv.h"
 
 namespace pkv {
 

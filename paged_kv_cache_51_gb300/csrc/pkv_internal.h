@@ -5,7 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 
-#include "../../include/pagedkv.h"
+#include "pagedkv.h"
 
 namespace pkv {
 

@@ -20,12 +20,20 @@
 // swizzled MN-major layout (V); TMA tensor copies write K and V blocks straight
 // into that layout, one (block, 64-dim half) box of 16 x 128 B per copy.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over work units):
-//   warps 0-3  one query row per thread: load Q, read S from TMEM, mask,
-//              online softmax, write P (bf16) to shared memory, rescale O in
-//              TMEM when the running max grows by more than 2^8, epilogue
-//   warp 4     TMA producer: K/V blocks of each key tile into a 2-stage ring
-//   warp 5     TMEM owner and MMA issuer (one thread issues tcgen05.mma)
+// Warp roles (352 threads, one CTA per SM, persistent over work units):
+//   warps 0-7  softmax: two threads per query row, one per 64-key half of each
+//              key tile.  Each half keeps its own running max and sum and its
+//              own O accumulator in TMEM (O = O_0 + O_1 after rescaling, like a
+//              split over keys), so the two never exchange data inside the
+//              loop.  A thread reads its 64 scores from TMEM, masks, computes P
+//              (bf16) while the previous P V product is still running, writes
+//              P to shared memory, and rescales its O half only when its
+//              running max grows by more than 2^8.  The epilogue merges the
+//              halves.
+//   warp 8     TMA producer for K: blocks of each key tile into a 2-stage K ring;
+//              a K stage is released as soon as its Q K^T product is done
+//   warp 9     TMA producer for V: a 2-stage V ring released by the P V product
+//   warp 10    TMEM owner and MMA issuer (one thread issues tcgen05.mma)
 // Every wait is bounded; on a timeout the kernel records an error, stops
 // issuing work, drains its copies and MMAs and frees TMEM before it returns.
 #include <cuda.h>
@@ -50,25 +58,33 @@ constexpr int kQOff = 0;                     // Q: 2 halves (dims 0-63, 64-127)
 constexpr int kPOff = 2 * kSub;              // P: 2 halves (keys 0-63, 64-127)
 constexpr int kKVOff = 4 * kSub;             // stages
 constexpr int kKBytes = 2 * kKeys * 128;     // K of one stage (2 halves of 128 key rows x 128 B)
-constexpr int kStageBytes = 2 * kKBytes;     // K + V
-constexpr int kBarOff = kKVOff + kStages * kStageBytes;
+constexpr int kStageBytes = 2 * kKBytes;     // K stage s at s * kStageBytes, V stage s after it
+constexpr int kStatOff = kKVOff + kStages * kStageBytes;  // (m, l) per half and row, 2 sets
+constexpr int kBarOff = kStatOff + 2 * 2 * kRows * 8;
 constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + 1 KiB alignment slack
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 512;          // S double buffer (2 x 128) + O (128)
-constexpr uint32_t kOCol = 256;
+constexpr int kSoftWarps = 8;
+constexpr int kKProducerWarp = 8;
+constexpr int kVProducerWarp = 9;
+constexpr int kMmaWarp = 10;
+constexpr int kThreads = 352;
+constexpr uint32_t kTmemCols = 512;          // S double buffer (2 x 128) + O halves (2 x 128)
+constexpr uint32_t kOCol = 256;              // O half h at kOCol + 128 h
 constexpr float kRescaleThreshold = 8.0f;    // log2 units: rescale O only when max grows > 2^8
 constexpr int kBoxBytes = kBlockTokens * 128;  // one TMA box: 16 rows x 64 bf16
 
 // barrier indices
 enum {
-    B_KV_FULL = 0,
-    B_KV_EMPTY = B_KV_FULL + kStages,
-    B_S_FULL = B_KV_EMPTY + kStages,
+    B_K_FULL = 0,
+    B_K_EMPTY = B_K_FULL + kStages,
+    B_V_FULL = B_K_EMPTY + kStages,
+    B_V_EMPTY = B_V_FULL + kStages,
+    B_S_FULL = B_V_EMPTY + kStages,
     B_S_EMPTY = B_S_FULL + 2,
-    B_P_FULL = B_S_EMPTY + 2,
-    B_O_DONE,
-    B_Q_FULL,
+    B_P_FULL = B_S_EMPTY + 2,       // per key half
+    B_O_DONE = B_P_FULL + 2,        // per key half
+    B_Q_FULL = B_O_DONE + 2,
     B_O_EMPTY,
+    B_STAT,                         // both halves' (m, l) of the current unit are published
     B_DRAIN,
     B_COUNT
 };
@@ -227,31 +243,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + B_COUNT * 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + B_COUNT * 8 + 4);
+    float2* stat = reinterpret_cast<float2*>(smem + kStatOff);  // [set][half][row]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_units = p.n_items[0] * p.num_kv_heads;
 
     // zero the operand area once so no stale bit pattern can be NaN
-    for (int i = threadIdx.x; i < kBarOff / 16; i += kThreads)
+    for (int i = threadIdx.x; i < kStatOff / 16; i += kThreads)
         reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bars[B_KV_FULL + s], 1);
-            mbar_init(&bars[B_KV_EMPTY + s], 1);
+            mbar_init(&bars[B_K_FULL + s], 1);
+            mbar_init(&bars[B_K_EMPTY + s], 1);
+            mbar_init(&bars[B_V_FULL + s], 1);
+            mbar_init(&bars[B_V_EMPTY + s], 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars[B_S_FULL + s], 1);
-            mbar_init(&bars[B_S_EMPTY + s], 4);
+            mbar_init(&bars[B_S_EMPTY + s], kSoftWarps);
+            mbar_init(&bars[B_P_FULL + s], kSoftWarps / 2);
+            mbar_init(&bars[B_O_DONE + s], 1);
         }
-        mbar_init(&bars[B_P_FULL], 4);
-        mbar_init(&bars[B_O_DONE], 1);
-        mbar_init(&bars[B_Q_FULL], 4);
-        mbar_init(&bars[B_O_EMPTY], 4);
+        mbar_init(&bars[B_Q_FULL], kSoftWarps);
+        mbar_init(&bars[B_O_EMPTY], kSoftWarps);
+        mbar_init(&bars[B_STAT], kSoftWarps);
         mbar_init(&bars[B_DRAIN], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_slot)),
                      "r"(kTmemCols)
@@ -264,8 +284,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
-        // ------------------------------ TMA producer ------------------------------
+    if (warp == kKProducerWarp || warp == kVProducerWarp) {
+        // ------------------- TMA producers (K ring, V ring) -------------------
+        const bool is_v = warp == kVProducerWarp;
+        const CUtensorMap* map = is_v ? &tmap_v : &tmap_k;
+        uint64_t* full = bars + (is_v ? B_V_FULL : B_K_FULL);
+        uint64_t* empty = bars + (is_v ? B_V_EMPTY : B_K_EMPTY);
+        const uint32_t ring = base + kKVOff + (is_v ? kKBytes : 0);
         uint32_t kt = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -273,33 +298,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t* bt = p.block_tables + size_t(x.seq) * p.table_stride;
             for (int j = 0; j < x.n_tiles && ok; ++j, ++kt) {
                 const int st = kt % kStages;
+                // read the tile's block ids first: the load overlaps the wait for a free stage
+                const int nb = min(kBlkPerTile, x.nblk - j * kBlkPerTile);
+                int blk = -1;
+                if (lane < nb) blk = bt[j * kBlkPerTile + lane];
                 ok = __all_sync(0xffffffffu,
-                                mbar_wait(&bars[B_KV_EMPTY + st], ((kt / kStages) & 1) ^ 1, p.err));
+                                mbar_wait(&empty[st], ((kt / kStages) & 1) ^ 1, p.err));
                 if (!ok || *abort_flag) {
                     ok = false;
                     break;
                 }
-                const int nb = min(kBlkPerTile, x.nblk - j * kBlkPerTile);
-                int blk = -1;
-                if (lane < nb) blk = bt[j * kBlkPerTile + lane];
                 const bool good = lane < nb && blk >= 0 && blk < p.num_blocks;
-                if (lane < nb && !good) flag_error(p.err, PKV_DEV_BAD_BLOCK_ID);
+                if (lane < nb && !good && !is_v) flag_error(p.err, PKV_DEV_BAD_BLOCK_ID);
                 const unsigned mask = __ballot_sync(0xffffffffu, good);
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&bars[B_KV_FULL + st],
-                                          uint32_t(__popc(mask)) * 4u * kBoxBytes);
-                }
+                if (lane == 0) mbar_arrive_expect_tx(&full[st], uint32_t(__popc(mask)) * 2u * kBoxBytes);
                 __syncwarp();
                 if (good) {
-                    // each lane issues its own block's four boxes
-                    const uint32_t sk = base + kKVOff + st * kStageBytes;
+                    // each lane issues its own block's two 64-dim boxes
+                    const uint32_t dst = ring + st * kStageBytes + uint32_t(lane) * kBoxBytes;
                     const int row = (blk * p.num_kv_heads + x.kvh) * kBlockTokens;
-                    const uint32_t off = uint32_t(lane) * kBoxBytes;
-                    tma_load_2d(sk + off, &tmap_k, 0, row, &bars[B_KV_FULL + st]);
-                    tma_load_2d(sk + kKeys * 128 + off, &tmap_k, 64, row, &bars[B_KV_FULL + st]);
-                    tma_load_2d(sk + kKBytes + off, &tmap_v, 0, row, &bars[B_KV_FULL + st]);
-                    tma_load_2d(sk + kKBytes + kKeys * 128 + off, &tmap_v, 64, row,
-                                &bars[B_KV_FULL + st]);
+                    tma_load_2d(dst, map, 0, row, &full[st]);
+                    tma_load_2d(dst + kKeys * 128, map, 64, row, &full[st]);
                 }
                 __syncwarp();
             }
@@ -309,28 +328,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             for (int k = 0; k < kStages && uint32_t(k) < kt; ++k) {
                 const uint32_t last = kt - 1 - k;
-                mbar_wait(&bars[B_KV_FULL + last % kStages], (last / kStages) & 1, p.err);
+                mbar_wait(&full[last % kStages], (last / kStages) & 1, p.err);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
             uint32_t kt = 0, it = 0;
             bool ok = true;
             const uint32_t q_addr = base + kQOff, p_addr = base + kPOff;
+            // O_h += P_h V_h over the 64 keys of half h, for both halves
             auto pv = [&](uint32_t g, int j) -> bool {
-                if (!mbar_wait(&bars[B_P_FULL], g & 1, p.err)) return false;
-                if (j == 0 && !mbar_wait(&bars[B_O_EMPTY], (it & 1) ^ 1, p.err)) return false;
-                tc_after();
                 const uint32_t vs = base + kKVOff + (g % kStages) * kStageBytes + kKBytes;
+                if (!mbar_wait(&bars[B_V_FULL + g % kStages], (g / kStages) & 1, p.err)) return false;
+                for (int h = 0; h < 2; ++h) {
+                    if (!mbar_wait(&bars[B_P_FULL + h], g & 1, p.err)) return false;
+                    if (j == 0 && h == 0 && !mbar_wait(&bars[B_O_EMPTY], (it & 1) ^ 1, p.err))
+                        return false;
+                    tc_after();
 #pragma unroll
-                for (int kk = 0; kk < kKeys / 16; ++kk) {
-                    const uint64_t a = sdesc(p_addr + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = sdesc(vs + kk * 16 * 128, kKeys * 128, 1024);
-                    umma(tmem + kOCol, a, b, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t a = sdesc(p_addr + h * kSub + kk * 32, 16, 1024);
+                        const uint64_t b = sdesc(vs + (h * 4 + kk) * 16 * 128, kKeys * 128, 1024);
+                        umma(tmem + kOCol + h * 128, a, b, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&bars[B_O_DONE + h]);
                 }
-                umma_commit(&bars[B_O_DONE]);
-                umma_commit(&bars[B_KV_EMPTY + g % kStages]);
+                umma_commit(&bars[B_V_EMPTY + g % kStages]);
                 return true;
             };
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++it) {
@@ -340,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_after();
                 for (int j = 0; j < x.n_tiles && ok; ++j) {
                     const uint32_t g = kt + j;
-                    ok = mbar_wait(&bars[B_KV_FULL + g % kStages], (g / kStages) & 1, p.err) &&
+                    ok = mbar_wait(&bars[B_K_FULL + g % kStages], (g / kStages) & 1, p.err) &&
                          mbar_wait(&bars[B_S_EMPTY + (g & 1)], ((g >> 1) & 1) ^ 1, p.err) &&
                          !*abort_flag;
                     if (!ok) break;
@@ -354,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         umma(tmem + (g & 1) * kKeys, a, b, kIdescQK, kk > 0 ? 1u : 0u);
                     }
                     umma_commit(&bars[B_S_FULL + (g & 1)]);
+                    umma_commit(&bars[B_K_EMPTY + g % kStages]);
                     if (j > 0) ok = pv(g - 1, j - 1) && !*abort_flag;
                 }
                 if (ok) ok = pv(kt + x.n_tiles - 1, x.n_tiles - 1);
@@ -366,9 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // ------------------- softmax / correction / epilogue (rows) -------------------
-        const int r = threadIdx.x;                      // query row = TMEM lane
-        const uint32_t lane_base = uint32_t(warp * 32) << 16;
+        // -------------- softmax: thread = (query row r, key half h) --------------
+        const int r = (warp & 3) * 32 + lane;            // query row = TMEM lane
+        const int h = warp >> 2;                          // key half of each 128-key tile
+        const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
         const int G = p.group;
         uint32_t kt = 0, it = 0;
         bool ok = true;
@@ -378,21 +404,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool row_valid = tok < x.nt;
             const int t = x.t0 + tok;
             const int limit = row_valid ? x.ctx - x.qlen + t : x.ctx - 1;  // last visible key
-            // ---- Q row -> shared memory (swizzled K-major) ----
+            // ---- Q row, dims 64h..64h+63 -> Q half h (swizzled K-major) ----
             {
                 const uint4* src = reinterpret_cast<const uint4*>(
-                    p.q + (size_t(x.q0 + t) * p.num_q_heads + x.kvh * G + g_head) * kDim);
+                    p.q + (size_t(x.q0 + t) * p.num_q_heads + x.kvh * G + g_head) * kDim + h * 64);
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
+                for (int c = 0; c < 8; ++c) {
                     const uint4 v = row_valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4*>(smem + kQOff + (c >> 3) * kSub + swz(r, c & 7)) = v;
+                    *reinterpret_cast<uint4*>(smem + kQOff + h * kSub + swz(r, c)) = v;
                 }
             }
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_Q_FULL]);
 
-            float m_used = -INFINITY, l = 0.f;
+            float m = -INFINITY, l = 0.f;
             for (int j = 0; j < x.n_tiles; ++j) {
                 const uint32_t g = kt + j;
                 if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_S_FULL + (g & 1)],
@@ -402,46 +428,62 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_after();
-                float s[kKeys];
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lane_base + (g & 1) * kKeys + c4 * 32, v);
+                float s[64];
+                {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32(tmem + lane_base + (g & 1) * kKeys + h * 64, v0);
+                    tmem_ld32(tmem + lane_base + (g & 1) * kKeys + h * 64 + 32, v1);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) s[c4 * 32 + i] = __uint_as_float(v[i]);
+                    for (int i = 0; i < 32; ++i) {
+                        s[i] = __uint_as_float(v0[i]);
+                        s[32 + i] = __uint_as_float(v1[i]);
+                    }
                 }
                 tc_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[B_S_EMPTY + (g & 1)]);
 
-                // scale to log2 units and mask keys beyond this row's causal limit
-                const int key0 = j * kKeys;
+                // mask keys beyond this row's causal limit; max on the raw scores
+                const int key0 = j * kKeys + h * 64;
                 float mx = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < kKeys; ++c) {
-                    s[c] = (key0 + c <= limit) ? s[c] * p.scale_log2 : -INFINITY;
+                for (int c = 0; c < 64; ++c) {
+                    s[c] = (key0 + c <= limit) ? s[c] : -INFINITY;
                     mx = fmaxf(mx, s[c]);
                 }
-                const float m_new = fmaxf(m_used, mx);
-                const bool need = m_new > m_used + kRescaleThreshold;  // always on the first tile
-                const bool warp_need = __any_sync(0xffffffffu, need);
+                const float m_new = fmaxf(m, mx * p.scale_log2);
+                const bool need = m_new > m + kRescaleThreshold;  // first visible keys included
                 float alpha = 1.f;
                 if (need) {
-                    alpha = exp2f(m_used - m_new);  // 0 on the first tile (O, l still empty)
-                    m_used = m_new;
+                    alpha = exp2f(m - m_new);
+                    m = m_new;
                     l *= alpha;
                 }
+                // P = 2^(s * scale - m) in bf16, computed before waiting on the previous PV
+                const float neg_m = m == -INFINITY ? 0.f : -m;
+                uint32_t w[32];
+                float rowsum = 0.f;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float p0 = exp2f(fmaf(s[2 * c], p.scale_log2, neg_m));
+                    const float p1 = exp2f(fmaf(s[2 * c + 1], p.scale_log2, neg_m));
+                    rowsum += p0 + p1;
+                    w[c] = pack_bf16(p0, p1);
+                }
+                l += rowsum;
+                const bool warp_need = __any_sync(0xffffffffu, need);
                 if (j > 0) {
-                    // PV of the previous tile must be done: P buffer free, O current
-                    ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE], (g - 1) & 1, p.err));
+                    // the previous PV of this half is done: P half free, O half current
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait(&bars[B_O_DONE + h], (g - 1) & 1, p.err));
                     if (!ok) break;
                     tc_after();
                     if (warp_need) {
 #pragma unroll 1
                         for (int c4 = 0; c4 < 4; ++c4) {
                             uint32_t v[32];
-                            const uint32_t ta = tmem + lane_base + kOCol + c4 * 32;
+                            const uint32_t ta = tmem + lane_base + kOCol + h * 128 + c4 * 32;
                             tmem_ld32(ta, v);
                             tmem_wait_ld();
 #pragma unroll
@@ -452,30 +494,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_wait_st();
                     }
                 }
-                // P = 2^(s - m) in bf16, row r of the K-major swizzled P tile
-                float rowsum = 0.f;
 #pragma unroll
-                for (int c8 = 0; c8 < 16; ++c8) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float p0 = exp2f(s[c8 * 8 + 2 * e] - m_used);
-                        const float p1 = exp2f(s[c8 * 8 + 2 * e + 1] - m_used);
-                        rowsum += p0 + p1;
-                        w[e] = pack_bf16(p0, p1);
-                    }
-                    *reinterpret_cast<uint4*>(smem + kPOff + (c8 >> 3) * kSub + swz(r, c8 & 7)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
-                }
-                l += rowsum;
+                for (int c8 = 0; c8 < 8; ++c8)
+                    *reinterpret_cast<uint4*>(smem + kPOff + h * kSub + swz(r, c8)) =
+                        make_uint4(w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
                 // rows of the last staged block that lie beyond the context were
-                // never written: zero their V so 0 * (anything) cannot become NaN
+                // never written: zero their V so 0 * (anything) cannot become NaN.
+                // The half whose keys hold that block does it before its P V.
                 const int rows_last = x.ctx - (x.nblk - 1) * kBlockTokens;  // valid rows, 1..16+
-                if (j == x.n_tiles - 1 && rows_last < kBlockTokens) {
-                    const int slot = (x.nblk - 1) - j * kBlkPerTile;
+                const int slot = (x.nblk - 1) - j * kBlkPerTile;
+                if (j == x.n_tiles - 1 && rows_last < kBlockTokens && (slot >> 2) == h) {
+                    // the V tile must have landed before its rows are overwritten (its
+                    // stage cannot be refilled before this tile's P V has been issued)
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_V_FULL + g % kStages],
+                                                           (g / kStages) & 1, p.err));
+                    if (!ok) break;
                     const int nz = (kBlockTokens - rows_last) * 2 * 8;  // rows x halves x chunks
                     unsigned char* vs = smem + kKVOff + (g % kStages) * kStageBytes + kKBytes;
-                    for (int i = r; i < nz; i += 128) {
+                    for (int i = r; i < nz; i += kRows) {
                         const int row = rows_last + i / 16, half = (i / 8) & 1, c = i & 7;
                         *reinterpret_cast<uint4*>(vs + half * (kKeys * 128) +
                                                   (slot * kBlockTokens + row) * 128 + c * 16) =
@@ -485,31 +521,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_async_smem();
                 tc_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[B_P_FULL]);
+                if (lane == 0) mbar_arrive(&bars[B_P_FULL + h]);
             }
             if (!ok) break;
-            // ---- epilogue: O / l -> out ----
+            // ---- epilogue: merge the halves, O / l -> out (this thread: dims 64h..64h+63) ----
             const uint32_t glast = kt + x.n_tiles - 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE], glast & 1, p.err));
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE], glast & 1, p.err) &&
+                                             mbar_wait(&bars[B_O_DONE + 1], glast & 1, p.err));
             if (!ok) break;
             tc_after();
-            const float inv = 1.f / l;
+            float2* st_set = stat + (it & 1) * 2 * kRows;
+            st_set[h * kRows + r] = make_float2(m, l);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_STAT]);
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_STAT], it & 1, p.err));
+            if (!ok) break;
+            const float2 o0 = st_set[r], o1 = st_set[kRows + r];
+            const float M = fmaxf(o0.x, o1.x);
+            const float a0 = exp2f(o0.x - M), a1 = exp2f(o1.x - M);
+            const float inv = 1.f / (o0.y * a0 + o1.y * a1);
+            const float w0 = a0 * inv, w1 = a1 * inv;
             uint4* dst = reinterpret_cast<uint4*>(
-                p.out + (size_t(x.q0 + t) * p.num_q_heads + x.kvh * G + g_head) * kDim);
+                p.out + (size_t(x.q0 + t) * p.num_q_heads + x.kvh * G + g_head) * kDim + h * 64);
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_base + kOCol + c4 * 32, v);
+            for (int c2 = 0; c2 < 2; ++c2) {
+                uint32_t v0[32], v1[32];
+                tmem_ld32(tmem + lane_base + kOCol + h * 64 + c2 * 32, v0);
+                tmem_ld32(tmem + lane_base + kOCol + 128 + h * 64 + c2 * 32, v1);
                 tmem_wait_ld();
                 if (row_valid) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        uint32_t w[4];
+                        uint32_t q4[4];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            w[k] = pack_bf16(__uint_as_float(v[e * 8 + 2 * k]) * inv,
-                                             __uint_as_float(v[e * 8 + 2 * k + 1]) * inv);
-                        dst[c4 * 4 + e] = make_uint4(w[0], w[1], w[2], w[3]);
+                        for (int k = 0; k < 4; ++k) {
+                            const int i0 = e * 8 + 2 * k;
+                            q4[k] = pack_bf16(
+                                __uint_as_float(v0[i0]) * w0 + __uint_as_float(v1[i0]) * w1,
+                                __uint_as_float(v0[i0 + 1]) * w0 + __uint_as_float(v1[i0 + 1]) * w1);
+                        }
+                        dst[c2 * 4 + e] = make_uint4(q4[0], q4[1], q4[2], q4[3]);
                     }
                 }
             }
@@ -524,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_before();
     __syncthreads();
     tc_after();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols)
                      : "memory");
