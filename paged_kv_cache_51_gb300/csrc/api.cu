@@ -197,10 +197,14 @@ extern "C" int paged_attention_varlen(void* out, const void* q, const void* k_ca
     a.scale = scale;
     a.stream = static_cast<cudaStream_t>(stream);
     if ((st = launch_plan(a)) != PKV_OK) return st;
+    if (max_query_len > 1) {
+        // prefill chunks first, on the SMs the planner gives them; the decode
+        // kernel may start beside it on the rest (programmatic dependent launch)
+        if ((st = launch_prefill(a)) != PKV_OK) return st;
+        a.pdl = true;
+    }
     if ((st = launch_decode_split(a)) != PKV_OK) return st;
-    if ((st = launch_decode_merge(a)) != PKV_OK) return st;
-    if (max_query_len > 1) return launch_prefill(a);
-    return PKV_OK;
+    return launch_decode_merge(a);
 }
 
 extern "C" int pkv_device_error(int32_t* code_out, int32_t clear) {

@@ -45,6 +45,9 @@ struct PlanParams {
     int32_t max_context_len;
     int32_t table_stride;
     int32_t tokens_per_tile;          // prefill tile height in tokens
+    int32_t num_sms;
+    double kv_bytes_per_token;        // K + V bytes of one token, all KV heads
+    double flops_per_pair;            // QK^T + PV flops of one (query, key) pair, all query heads
     Workspace ws;
     int* err;
 };
@@ -52,10 +55,13 @@ struct PlanParams {
 __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
     __shared__ int warp_d[32], warp_p[32];
     __shared__ int carry_d, carry_p, layout_ok;
+    __shared__ unsigned long long dec_tokens, pre_pairs;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
         carry_d = 0;
         carry_p = 0;
+        dec_tokens = 0;
+        pre_pairs = 0;
         layout_ok = 1;
         if (p.query_start_loc) {
             if (p.query_start_loc[0] != 0 || p.query_start_loc[p.num_seqs] != p.num_query_tokens) {
@@ -81,8 +87,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
                     flag_error(p.err, PKV_DEV_TABLE_TOO_NARROW);
                 } else if (qlen == 1) {
                     nd = (ctx + kSplitTokens - 1) / kSplitTokens;
+                    atomicAdd(&dec_tokens, (unsigned long long)ctx);
                 } else {
                     np = (qlen + p.tokens_per_tile - 1) / p.tokens_per_tile;
+                    // causal (query, key) pairs of the chunk
+                    const unsigned long long q = qlen, c = ctx;
+                    atomicAdd(&pre_pairs, q * (c - q) + q * (q + 1) / 2);
                 }
             }
         }
@@ -133,6 +143,17 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
     if (tid == 0) {
         p.ws.counters[0] = carry_d;
         p.ws.counters[1] = min(carry_p, p.ws.max_prefill_items);
+        // SMs for the prefill chunks: their share of the estimated time, so that
+        // tensor-bound chunks and HBM-bound decode rows finish together
+        int sms_prefill = 0;
+        if (pre_pairs) {
+            const double t_pre = double(pre_pairs) * p.flops_per_pair / kPrefillFlopsPerNs;
+            const double t_dec = double(dec_tokens) * p.kv_bytes_per_token / kDecodeBytesPerNs;
+            sms_prefill = int(ceil(p.num_sms * t_pre / (t_pre + t_dec)));
+            sms_prefill = max(1, min(p.num_sms, sms_prefill));
+        }
+        p.ws.counters[2] = sms_prefill;
+        p.ws.counters[3] = 0;  // decode unit ticket
     }
 }
 
@@ -145,6 +166,10 @@ int launch_plan(const AttnArgs& a) {
     p.max_context_len = a.max_context_len;
     p.table_stride = a.table_stride;
     p.tokens_per_tile = kPrefillRows / (a.desc->num_q_heads / a.desc->num_kv_heads);
+    p.num_sms = num_sms();
+    p.kv_bytes_per_token =
+        2.0 * a.desc->num_kv_heads * a.desc->head_dim * double(elem_bytes(a.desc->dtype));
+    p.flops_per_pair = 4.0 * a.desc->head_dim * a.desc->num_q_heads;
     p.ws = a.ws;
     p.err = a.err;
     plan_kernel<<<1, 1024, 0, a.stream>>>(p);
@@ -164,6 +189,7 @@ struct SplitParams {
     const int32_t* query_start_loc;
     const int2* items;
     const int32_t* n_items;
+    int32_t* ticket;
     float2* part_ml;
     float* part_o;
     int32_t table_stride;
@@ -194,7 +220,8 @@ struct SplitCfg {
     static constexpr size_t kPBufOff = size_t(kStages) * kStageBytes;
     static constexpr size_t kCombOff = kPBufOff + size_t(kWarps) * kPBuf * 4;
     static constexpr size_t kBarOff = align_up_c(kCombOff + size_t(kWarps) * kComb * 4, 16);
-    static constexpr size_t kSmem = kBarOff + 2 * kStages * 8;
+    static constexpr size_t kQueueOff = kBarOff + 2 * kStages * 8;
+    static constexpr size_t kSmem = kQueueOff + sizeof(UnitQueue);
     static_assert(kDPL == 2 || kDPL == 4, "head_dim 64 or 128");
     static_assert(kNV == 16 || kNV == 32, "group size 1, 2, 4 or 8");
 };
@@ -258,6 +285,7 @@ __global__ void __launch_bounds__(SplitCfg<T, D, G>::kThreads)
     float* comb = reinterpret_cast<float*>(smem + C::kCombOff);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
     uint64_t* empty = full + C::kStages;
+    UnitQueue* uq = reinterpret_cast<UnitQueue*>(smem + C::kQueueOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -265,6 +293,7 @@ __global__ void __launch_bounds__(SplitCfg<T, D, G>::kThreads)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
+        uq_init(uq);
         fence_mbar_init();
     }
     __syncthreads();
@@ -278,7 +307,10 @@ __global__ void __launch_bounds__(SplitCfg<T, D, G>::kThreads)
         bool ok = true;
         const unsigned char* kb = static_cast<const unsigned char*>(p.k_cache);
         const unsigned char* vb = static_cast<const unsigned char*>(p.v_cache);
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        int next = uq_first_ticket(p.ticket, lane);
+        for (uint32_t k = 0;; ++k) {
+            const int u = uq_produce(uq, k, next, p.ticket, n_units, lane, p.err, ok);
+            if (u < 0) break;
             const int2 item = p.items[u / Hkv];
             const int kvh = u % Hkv;
             const int ctx = p.context_lens[item.x];
@@ -326,7 +358,9 @@ __global__ void __launch_bounds__(SplitCfg<T, D, G>::kThreads)
     uint32_t it_base = 0;
     bool ok = true;
 
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    for (uint32_t k = 0;; ++k) {
+        const int u = uq_consume(uq, k, C::kWarps * 32, p.err, ok);
+        if (u < 0) break;
         const int2 item = p.items[u / Hkv];
         const int seq = item.x, split = item.y;
         const int kvh = u % Hkv;
@@ -457,6 +491,8 @@ __global__ void __launch_bounds__(SplitCfg<T, D, G>::kThreads)
         }
         consumer_sync(C::kWarps * 32);
     }
+    // a preceding prefill kernel overlapped this grid: finish only after it has
+    if (threadIdx.x == 0) pdl_wait_prerequisites();
 }
 
 // ---------------------------------------------------------------------------
@@ -522,14 +558,14 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(MergeParams p) {
 // ---------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------
-namespace {
-
 int num_sms() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     return n;
 }
+
+namespace {
 
 template <typename T, int D, int G>
 int launch_split_t(const AttnArgs& a) {
@@ -556,6 +592,7 @@ int launch_split_t(const AttnArgs& a) {
     p.query_start_loc = a.query_start_loc;
     p.items = a.ws.items;
     p.n_items = a.ws.counters;
+    p.ticket = a.ws.counters + 3;
     p.part_ml = a.ws.part_ml;
     p.part_o = a.ws.part_o;
     p.table_stride = a.table_stride;
@@ -565,8 +602,17 @@ int launch_split_t(const AttnArgs& a) {
     p.max_splits = a.ws.max_splits;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.err = a.err;
-    kern<<<unsigned(grid), C::kThreads, C::kSmem, a.stream>>>(p);
-    return cuda_status(cudaGetLastError());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.pdl ? 1 : 0;
+    return cuda_status(cudaLaunchKernelEx(&cfg, kern, p));
 }
 
 template <typename T, int D>

@@ -38,6 +38,7 @@ struct MmaParams {
     const int32_t* query_start_loc;
     const int2* items;
     const int32_t* n_items;
+    int32_t* ticket;
     float2* part_ml;
     float* part_o;
     int32_t table_stride;
@@ -61,7 +62,8 @@ struct MmaCfg {
     static constexpr int kComb = G * (D + 2);
     static constexpr int kCombOff = kRingBytes;
     static constexpr int kBarOff = kCombOff + kWarps * kComb * 4;
-    static constexpr int kSmem = kBarOff + 2 * kStages * 8 + 1024;  // + alignment slack
+    static constexpr int kQueueOff = kBarOff + 2 * kStages * 8;
+    static constexpr int kSmem = kQueueOff + int(sizeof(UnitQueue)) + 1024;  // + alignment slack
     static_assert(G == 2 || G == 4 || G == 8, "group size");
 };
 
@@ -119,6 +121,7 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads)
     float* comb = reinterpret_cast<float*>(smem + C::kCombOff);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
     uint64_t* empty = full + C::kStages;
+    UnitQueue* uq = reinterpret_cast<UnitQueue*>(smem + C::kQueueOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -126,6 +129,7 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
+        uq_init(uq);
         fence_mbar_init();
     }
     __syncthreads();
@@ -138,7 +142,10 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads)
         // ---------------- producer ----------------
         uint32_t it = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        int next = uq_first_ticket(p.ticket, lane);
+        for (uint32_t k = 0;; ++k) {
+            const int u = uq_produce(uq, k, next, p.ticket, n_units, lane, p.err, ok);
+            if (u < 0) break;
             const int2 item = p.items[u / Hkv];
             const int kvh = u % Hkv;
             const int ctx = p.context_lens[item.x];
@@ -183,7 +190,9 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads)
     const int gid = lane >> 2, tig = lane & 3;
     uint32_t it_base = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    for (uint32_t k = 0;; ++k) {
+        const int u = uq_consume(uq, k, C::kWarps * 32, p.err, ok);
+        if (u < 0) break;
         const int2 item = p.items[u / Hkv];
         const int seq = item.x, split = item.y;
         const int kvh = u % Hkv;
@@ -329,6 +338,8 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads)
         }
         asm volatile("bar.sync 1, %0;" ::"r"(C::kWarps * 32) : "memory");
     }
+    // a preceding prefill kernel overlapped this grid: finish only after it has
+    if (threadIdx.x == 0) pdl_wait_prerequisites();
 }
 
 int sms() {
@@ -365,6 +376,7 @@ int launch_t(const AttnArgs& a) {
     p.query_start_loc = a.query_start_loc;
     p.items = a.ws.items;
     p.n_items = a.ws.counters;
+    p.ticket = a.ws.counters + 3;
     p.part_ml = a.ws.part_ml;
     p.part_o = a.ws.part_o;
     p.table_stride = a.table_stride;
@@ -374,8 +386,17 @@ int launch_t(const AttnArgs& a) {
     p.max_splits = a.ws.max_splits;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.err = a.err;
-    kern<<<unsigned(grid), C::kThreads, C::kSmem, a.stream>>>(mk, mv, p);
-    return cuda_status(cudaGetLastError());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.pdl ? 1 : 0;
+    return cuda_status(cudaLaunchKernelEx(&cfg, kern, mk, mv, p));
 }
 
 template <int D>

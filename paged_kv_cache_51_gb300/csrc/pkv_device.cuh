@@ -91,6 +91,76 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// ---- dynamic work units -------------------------------------------------------
+// A CTA's producer warp takes work units from a global ticket and hands them to
+// the CTA's consumer warps through a 4-deep queue in shared memory, so CTAs that
+// start late (because other kernels held their SM) simply find less work.
+struct UnitQueue {
+    int32_t unit[4];
+    int32_t current;          // unit the consumer warps are on
+    int32_t pad;
+    uint64_t ready[4];        // producer -> consumers
+    uint64_t empty[4];        // consumers -> producer
+};
+
+__device__ __forceinline__ void uq_init(UnitQueue* q) {
+    for (int i = 0; i < 4; ++i) {
+        mbar_init(&q->ready[i], 1);
+        mbar_init(&q->empty[i], 1);
+    }
+}
+
+// Producer warp (all lanes): the unit of step k, or -1 when the ticket is
+// exhausted or a wait failed; published to the consumers either way.  The
+// ticket for step k + 1 is taken here too and kept in `next` (lane 0), so the
+// atomic's latency hides behind the issue of step k's copies.  Start with
+// next = uq_first_ticket(...).
+__device__ __forceinline__ int uq_first_ticket(int* ticket, int lane) {
+    return lane == 0 ? atomicAdd(ticket, 1) : 0;
+}
+__device__ __forceinline__ int uq_produce(UnitQueue* q, uint32_t k, int& next, int* ticket,
+                                          int n_units, int lane, int* err, bool& ok) {
+    ok = ok && __all_sync(0xffffffffu, mbar_wait(&q->empty[k & 3], ((k >> 2) & 1) ^ 1, err));
+    int u = -1;
+    if (lane == 0) {
+        if (ok && next < n_units) {
+            u = next;
+            next = atomicAdd(ticket, 1);
+        }
+        q->unit[k & 3] = u;
+        mbar_arrive(&q->ready[k & 3]);
+    }
+    return __shfl_sync(0xffffffffu, u, 0);
+}
+
+// Consumer warps (all `nthreads` threads, named barrier 1): the unit of step k.
+// One thread waits for it and publishes it, so every consumer warp sees the same
+// sequence of units (and -1 together).
+__device__ __forceinline__ int uq_consume(UnitQueue* q, uint32_t k, int nthreads, int* err,
+                                          bool& ok) {
+    if (threadIdx.x == 0) {
+        int u = -1;
+        if (ok && mbar_wait(&q->ready[k & 3], (k >> 2) & 1, err)) u = q->unit[k & 3];
+        q->current = u;
+        mbar_arrive(&q->empty[k & 3]);
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+    const int u = *reinterpret_cast<volatile int32_t*>(&q->current);
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+    if (u < 0) ok = false;
+    return u;
+}
+
+// ---- programmatic dependent launch ---------------------------------------------
+// Let the next kernel in the stream start while this grid still runs.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the grids this one depends on have completed (no-op without PDL).
+__device__ __forceinline__ void pdl_wait_prerequisites() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---- element conversion -------------------------------------------------------
 template <typename T>
 struct Elem;

@@ -29,7 +29,8 @@ inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_E
 
 // Workspace carve-up shared by decode and varlen.
 struct Workspace {
-    int32_t* counters;   // [0] decode items, [1] prefill items
+    int32_t* counters;   // [0] decode items, [1] prefill items, [2] SMs for prefill,
+                         // [3] decode unit ticket
     int2* items;         // decode items (seq, split)
     int2* prefill_items; // prefill items (seq, row tile)
     float2* part_ml;     // [num_seqs][num_q_heads][max_splits] (max, sum), log2 domain
@@ -59,7 +60,15 @@ struct AttnArgs {
     Workspace ws;
     cudaStream_t stream;
     int* err;
+    bool pdl;            // decode kernels may start while the preceding prefill kernel runs
 };
+
+// Planning rates for the split of SMs between prefill chunks and decode rows
+// of one mixed batch (what this library's kernels sustain on GB300).
+constexpr double kDecodeBytesPerNs = 6400.0;     // decode streams KV at ~6.4 TB/s
+constexpr double kPrefillFlopsPerNs = 450000.0;  // prefill kernel ~450 TFLOP/s over causal pairs
+
+int num_sms();
 
 // tmap.cpp: tensor map of a bf16 cache viewed as 2-D [num_blocks * Hkv * bs rows][head_dim],
 // box = one block of one head (bs rows) x 64 dims, 128-byte swizzled in shared memory.

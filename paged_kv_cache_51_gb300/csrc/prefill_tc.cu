@@ -202,6 +202,7 @@ struct PrefillParams {
     const int32_t* query_start_loc;
     const int2* items;
     const int32_t* n_items;
+    const int32_t* counters;   // [2]: how many CTAs (one per SM) take prefill units
     int32_t table_stride;
     int32_t num_blocks;
     int32_t num_kv_heads;
@@ -236,6 +237,13 @@ __device__ __forceinline__ Unit unit_of(const PrefillParams& p, int u) {
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, PrefillParams p) {
+    // The planner gives the prefill chunks only as many SMs as their share of
+    // the batch's work; the other CTAs leave at once, and the decode kernel that
+    // follows in the stream may start right away on the SMs they free.
+    const int active = min(p.counters[2], int(gridDim.x));
+    pdl_launch_dependents();
+    if (int(blockIdx.x) >= active) return;
+
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;           // 1 KiB aligned for the swizzle
@@ -293,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ring = base + kKVOff + (is_v ? kKBytes : 0);
         uint32_t kt = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        for (int u = blockIdx.x; u < n_units && ok; u += active) {
             const Unit x = unit_of(p, u);
             const int32_t* bt = p.block_tables + size_t(x.seq) * p.table_stride;
             for (int j = 0; j < x.n_tiles && ok; ++j, ++kt) {
@@ -357,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_commit(&bars[B_V_EMPTY + g % kStages]);
                 return true;
             };
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++it) {
+            for (int u = blockIdx.x; u < n_units && ok; u += active, ++it) {
                 const Unit x = unit_of(p, u);
                 ok = mbar_wait(&bars[B_Q_FULL], it & 1, p.err) && !*abort_flag;
                 if (!ok) break;
@@ -398,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int G = p.group;
         uint32_t kt = 0, it = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
+        for (int u = blockIdx.x; u < n_units; u += active, ++it) {
             const Unit x = unit_of(p, u);
             const int tok = r / G, g_head = r % G;
             const bool row_valid = tok < x.nt;
@@ -619,6 +627,7 @@ int launch_prefill(const AttnArgs& a) {
     p.query_start_loc = a.query_start_loc;
     p.items = a.ws.prefill_items;
     p.n_items = a.ws.counters + 1;
+    p.counters = a.ws.counters;
     p.table_stride = a.table_stride;
     p.num_blocks = d->num_blocks;
     p.num_kv_heads = d->num_kv_heads;
