@@ -55,13 +55,12 @@ struct PlanParams {
 __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
     __shared__ int warp_d[32], warp_p[32];
     __shared__ int carry_d, carry_p, layout_ok;
-    __shared__ unsigned long long dec_tokens, pre_pairs;
+    __shared__ unsigned long long warp_tok[32], warp_pairs[32];
+    unsigned long long my_tok = 0, my_pairs = 0;   // this thread's work estimate
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
         carry_d = 0;
         carry_p = 0;
-        dec_tokens = 0;
-        pre_pairs = 0;
         layout_ok = 1;
         if (p.query_start_loc) {
             if (p.query_start_loc[0] != 0 || p.query_start_loc[p.num_seqs] != p.num_query_tokens) {
@@ -87,12 +86,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
                     flag_error(p.err, PKV_DEV_TABLE_TOO_NARROW);
                 } else if (qlen == 1) {
                     nd = (ctx + kSplitTokens - 1) / kSplitTokens;
-                    atomicAdd(&dec_tokens, (unsigned long long)ctx);
+                    my_tok += (unsigned long long)ctx;
                 } else {
                     np = (qlen + p.tokens_per_tile - 1) / p.tokens_per_tile;
                     // causal (query, key) pairs of the chunk
                     const unsigned long long q = qlen, c = ctx;
-                    atomicAdd(&pre_pairs, q * (c - q) + q * (q + 1) / 2);
+                    my_pairs += q * (c - q) + q * (q + 1) / 2;
                 }
             }
         }
@@ -140,7 +139,23 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
         }
         __syncthreads();
     }
+    // block-wide sums of the work estimates
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+        my_tok += __shfl_xor_sync(kFull, my_tok, off);
+        my_pairs += __shfl_xor_sync(kFull, my_pairs, off);
+    }
+    if (lane == 0) {
+        warp_tok[warp] = my_tok;
+        warp_pairs[warp] = my_pairs;
+    }
+    __syncthreads();
     if (tid == 0) {
+        unsigned long long dec_tokens = 0, pre_pairs = 0;
+        for (int w = 0; w < 32; ++w) {
+            dec_tokens += warp_tok[w];
+            pre_pairs += warp_pairs[w];
+        }
         p.ws.counters[0] = carry_d;
         p.ws.counters[1] = min(carry_p, p.ws.max_prefill_items);
         // SMs for the prefill chunks: their share of the estimated time, so that
