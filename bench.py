@@ -247,6 +247,34 @@ def accounting(w, step):
         "context_tokens": sum(ctx)}
 
 
+def max_over_ranks(ms, dist=None, device=None):
+    """The slowest rank's time: the whole job finishes when its last replica does."""
+    if dist is None:
+        return ms
+    import torch
+
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_workload(config, rank, batch=0, prefill_chunks=False):
+    """Each rank runs its own replica of the workload, drawn with seed = rank.
+    Sequences are independent, so replicas need no exchange on the data path."""
+    import workloads
+
+    if prefill_chunks:
+        return workloads.random_varlen(rank, "bf16", 32, 8, 128, 16,
+                                       [(0, 512), (1024, 512), (3072, 512)], scale=0.5)
+    kw = {"batch": batch} if batch and config in (2, 3) else {}
+    return workloads.make(config, seed=rank, **kw)
+
+
+def job_throughput(bytes_per_rank, world, ms):
+    """Whole-job GB/s: every replica moved `bytes_per_rank` in the slowest rank's time."""
+    return bytes_per_rank * world / (ms * 1e-3) / 1e9
+
+
 def time_steps(step, steps, warmup):
     """Device time of `steps` steps and the mean time of the attention call inside them."""
     import torch
@@ -342,13 +370,7 @@ def run_gpu(args):
 
         dist.init_process_group("nccl")
 
-    if args.prefill_chunks:
-        # the three 512-token chunks of the SplitFuse batch (prefixes 0/1024/3072), no decode rows
-        w = workloads.random_varlen(rank, "bf16", 32, 8, 128, 16,
-                                    [(0, 512), (1024, 512), (3072, 512)], scale=0.5)
-    else:
-        kw = {"batch": args.batch} if args.batch and args.config in (2, 3) else {}
-        w = workloads.make(args.config, seed=rank, **kw)
+    w = replica_workload(args.config, rank, args.batch, args.prefill_chunks)
     dc, step = runner.prepare(w)
     acc = accounting(w, step)
     attn_b = acc["attn_bytes"]
@@ -372,10 +394,7 @@ def run_gpu(args):
     if dist:
         dist.barrier()
     sampler.stop()
-    if dist:
-        t = torch.tensor([ms_per_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
+    ms_per_step = max_over_ranks(ms_per_step, dist, "cuda")
     if pkv.device_error() != 0:
         raise SystemExit("device error during the timed region")
 
@@ -406,7 +425,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / k_e2e
 
-    value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
+    value = job_throughput(step_bytes, world, ms_per_step)
     peak, peak_kind, tc_peak, _ = peaks()
     achieved = attn_b / (attn_ms * 1e-3) / 1e9
     launches_per_step = ((1 if step.pairs.shape[0] else 0) + 1 + 2
