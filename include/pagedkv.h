@@ -146,6 +146,20 @@ PKV_API int pkv_block_ref_count(const pkv_pool* pool, int32_t block, int32_t* ou
 PKV_API int pkv_block_tables(const pkv_pool* pool, const int64_t* seq_ids, int32_t n,
                      int32_t max_blocks, int32_t* tables_out, int32_t* ctx_lens_out);
 
+/* Compose one forward pass of a mixed batch under a token budget [FastGen
+ * §3.2 动态分割融合: split long prompts, fuse short ones, keep every pass the
+ * same size; Ch15 §15.6 两阶段与 Chunked Prefill: sum(prefill chunk tokens) +
+ * decode sequences <= budget, decodes first].  `num_decode` running sequences
+ * each want one token; `prompt_remaining` (host, [num_prompts]) are the
+ * unprocessed prompt tokens of waiting requests in arrival order.
+ * *decode_admitted = min(num_decode, budget); then chunk_out[i] (host,
+ * [num_prompts]) = min(prompt_remaining[i], budget left), in order, so only
+ * the last prompt served is split.  *tokens_used (optional) = tokens placed.
+ * Pure host code. */
+PKV_API int pkv_splitfuse_compose(int32_t token_budget, int32_t num_decode, int32_t num_prompts,
+                                  const int32_t* prompt_remaining, int32_t* chunk_out,
+                                  int32_t* decode_admitted, int32_t* tokens_used);
+
 /* ======================================================================== *
  * Device entry points.
  * ======================================================================== */

@@ -27,10 +27,11 @@ Modules
                second, independent path used only to pin the first)
   sketch       the pages' per-block-normalised sketch (a negative control)
   kv_size      closed-form KV-cache size
+  splitfuse    token-budget composition of one forward pass (decodes + prompt chunks)
 
 Parity: every function here is pinned by ``tests/test_oracle_*.py`` against
 values the pages print, closed forms, brute force on unpaged data, or
 invariants; none is marked "parity unpinned".
 """
 
-from . import attention, block_pool, cache, kv_size, numerics, online, sketch  # noqa: F401
+from . import attention, block_pool, cache, kv_size, numerics, online, sketch, splitfuse  # noqa: F401

@@ -41,7 +41,7 @@ EXPORTS = (
     "pkv_block_ref_count", "pkv_block_tables", "pkv_copy_blocks", "paged_kv_append",
     "pkv_decode_workspace_bytes", "paged_attention_decode", "paged_attention_decode_noalloc",
     "pkv_varlen_workspace_bytes",
-    "paged_attention_varlen", "pkv_device_error", "pkv_status_string",
+    "paged_attention_varlen", "pkv_device_error", "pkv_status_string", "pkv_splitfuse_compose",
 )
 
 
@@ -94,6 +94,7 @@ def lib():
                                                   i32, i32, i32, ctypes.c_float, p, sz, p]),
         "pkv_device_error": (ctypes.c_int, [P(i32), i32]),
         "pkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "pkv_splitfuse_compose": (ctypes.c_int, [i32, i32, i32, p, p, P(i32), P(i32)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -200,6 +201,20 @@ class BlockPool:
         _check(lib().pkv_block_tables(self._h, ids.data_ptr(), n, max_blocks, tables.data_ptr(),
                                       ctx.data_ptr()), "pkv_block_tables")
         return tables, ctx
+
+
+def pkv_splitfuse_compose(token_budget, num_decode, prompt_remaining):
+    """Token-budget composition of one forward pass (C++).
+
+    Returns (decode_admitted, chunks, tokens_used): the first decode_admitted
+    decode sequences take one token each, prompt i takes chunks[i] tokens."""
+    n = len(prompt_remaining)
+    rem = (ctypes.c_int32 * max(n, 1))(*[int(r) for r in prompt_remaining])
+    out = (ctypes.c_int32 * max(n, 1))()
+    dec, used = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().pkv_splitfuse_compose(token_budget, num_decode, n, rem, out, ctypes.byref(dec),
+                                       ctypes.byref(used)), "pkv_splitfuse_compose")
+    return dec.value, list(out)[:n], used.value
 
 
 # ----------------------------------------------------------------------------

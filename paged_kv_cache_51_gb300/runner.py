@@ -97,9 +97,11 @@ class DeviceCache:
             self._apply(op, record=False)
         self.flush()
 
-    def plan_step(self):
-        """Plan the step's pool operations; returns the step's device inputs (not yet applied)."""
-        for op in self.w.step:
+    def plan_step(self, ops=None):
+        """Plan the step's pool operations (the workload's own step, or `ops`); returns
+        the step's device inputs (not yet applied to the cache)."""
+        self.step_slots, self.step_rows, self.step_pairs = [], [], []
+        for op in (self.w.step if ops is None else ops):
             self._apply(op, record=True)
         # the step's copies and appends stay queued: hand them to the caller
         self._slots, self._rows, self._pairs = [], [], []
@@ -112,14 +114,15 @@ class DeviceCache:
             "pairs": torch.tensor(self.step_pairs, dtype=torch.int32).reshape(-1, 2),
         }
 
-    def batch_metadata(self):
+    def batch_metadata(self, batch=None):
         """Block tables [S, W] (padded -1), context lengths [S], query_start_loc [S+1] (host)."""
         w = self.w
-        seqs = [s for s, _ in w.batch]
+        batch = w.batch if batch is None else batch
+        seqs = [s for s, _ in batch]
         width = max(math.ceil(self.pool.seq_len(s) / w.block_size) for s in seqs)
         tables, ctx = self.pool.block_tables(seqs, width)
         qsl = torch.zeros(len(seqs) + 1, dtype=torch.int32)
-        qsl[1:] = torch.cumsum(torch.tensor([q for _, q in w.batch], dtype=torch.int32), 0)
+        qsl[1:] = torch.cumsum(torch.tensor([q for _, q in batch], dtype=torch.int32), 0)
         return tables, ctx, qsl
 
     def q_tensor(self):
@@ -129,24 +132,26 @@ class DeviceCache:
 class Step:
     """Device-resident inputs of one step and the calls that run it."""
 
-    def __init__(self, dc, planned):
+    def __init__(self, dc, planned, batch=None, q=None):
+        """`batch` ([(seq, qlen)]) and `q` (host rows [Tq, Hq, D]) default to the workload's."""
         w = dc.w
+        batch = w.batch if batch is None else batch
         dev = dc.device
         self.dc = dc
         self.slot_mapping = planned["slot_mapping"].to(dev)
         self.k_new = planned["k"].to(dev)
         self.v_new = planned["v"].to(dev)
         self.pairs = planned["pairs"].to(dev)
-        tables, ctx, qsl = dc.batch_metadata()
+        tables, ctx, qsl = dc.batch_metadata(batch)
         self.tables = tables.to(dev)
         self.ctx = ctx.to(dev)
         self.qsl = qsl.to(dev)
         self.max_ctx = int(ctx.max())
-        self.max_qlen = max(q for _, q in w.batch)
+        self.max_qlen = max(q for _, q in batch)
         self.decode_only = self.max_qlen == 1
-        self.q = dc.q_tensor().to(dev)
+        self.q = (dc.q_tensor() if q is None else _torch_rows(q, w.dtype)).to(dev)
         self.out = torch.empty_like(self.q)
-        S = len(w.batch)
+        S = len(batch)
         if self.decode_only:
             nbytes = decode_workspace_bytes(dc.desc, S, self.max_ctx)
         else:

@@ -259,3 +259,46 @@ def random_varlen(seed, dtype, hq, hkv, d, bs, spans, scale=1.0, slack=0.1):
     return Workload(f"varlen-{dtype}", dtype, hq, hkv, d, bs, nb, free_order, setup, step, batch,
                     q, k_rows, v_rows,
                     notes={"context_lens": [p + qn for p, qn in spans]})
+
+
+@dataclass
+class ServingTrace:
+    """Requests for a multi-step run: prompt length, tokens to generate, the step at
+    which each arrives, and value rows indexed by (request, position)."""
+    dtype: str
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    free_order: np.ndarray
+    prompt_len: list
+    gen_len: list
+    arrival: list
+    row_offset: list
+    k_rows: np.ndarray
+    v_rows: np.ndarray
+    q_rows: np.ndarray
+
+
+def serving_trace(seed=0, n_requests=6, prompt_range=(20, 700), gen_range=(1, 6), arrive_every=1,
+                  hq=32, hkv=8, d=128, bs=16, scale=0.5):
+    """A seeded stream of requests (values N(0,1) * scale, bf16)."""
+    rng = np.random.default_rng(seed)
+    prompt = [int(x) for x in rng.integers(prompt_range[0], prompt_range[1], size=n_requests,
+                                           endpoint=True)]
+    gen = [int(x) for x in rng.integers(gen_range[0], gen_range[1], size=n_requests,
+                                        endpoint=True)]
+    arrival = [i * arrive_every for i in range(n_requests)]
+    offs, row = [], 0
+    for p, g in zip(prompt, gen):
+        offs.append(row)
+        row += p + g
+    need = sum(_blocks(p + g, bs) for p, g in zip(prompt, gen))
+    nb = int(np.ceil(need * 1.1)) + 2
+    free_order = rng.permutation(nb).astype(np.int32)
+    k_rows = _values(rng, (row, hkv, d), "bf16", scale)
+    v_rows = _values(rng, (row, hkv, d), "bf16", scale)
+    q_rows = _values(rng, (row, hq, d), "bf16", scale)
+    return ServingTrace("bf16", hq, hkv, d, bs, nb, free_order, prompt, gen, arrival, offs,
+                        k_rows, v_rows, q_rows)
