@@ -72,6 +72,7 @@ extern "C" {
 #define PKV_DEV_BAD_QUERY_LAYOUT 5  /* query_start_loc not non-decreasing from 0 to num_query_tokens */
 #define PKV_DEV_WAIT_TIMEOUT     6  /* a pipeline wait exceeded its limit (internal fault) */
 #define PKV_DEV_TABLE_TOO_NARROW 7  /* context needs more blocks than max_blocks_per_seq */
+#define PKV_DEV_BAD_POSITION     8  /* rotary position outside [0, max_position) */
 
 /* ---- data types -------------------------------------------------------- */
 #define PKV_F32  0
@@ -182,6 +183,27 @@ PKV_API int pkv_copy_blocks(const int32_t* block_pairs, int32_t num_pairs, void*
  * must be distinct.  num_tokens == 0 is a no-op. */
 PKV_API int paged_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int32_t num_tokens,
                     void* k_cache, void* v_cache, const pkv_cache_desc* desc, void* stream);
+
+/* Append with rotary position embedding fused in [Ch15 §15.3 RoPE 与 Flash
+ * Attention 的融合: rotate in registers rather than in a separate pass through
+ * HBM; FastGen §6 (rotary fused with the blocked-KV write)].  Rotate-half form
+ * (the pages defer RoPE's formula; this is the reading taken): for token t at
+ * position p = positions[t] and i < head_dim/2, with c = cos_sin[p][i] and
+ * s = cos_sin[p][head_dim/2 + i],
+ *   x'[i] = x[i] c - x[i + D/2] s,   x'[i + D/2] = x[i] s + x[i + D/2] c,
+ * each product and sum rounded in fp32 on its own (no fused multiply-add),
+ * then rounded to the cache dtype (bf16: nearest-even).  K is rotated and
+ * written with V through slot_mapping as paged_kv_append does; V is copied
+ * unrotated; q (device [T][Hq][D], optional) is rotated into q_out (may alias
+ * q; both NULL to skip).  cos_sin: device fp32 [max_position][head_dim],
+ * 16-byte aligned.  positions: device int32 [T]; a position outside
+ * [0, max_position) sets PKV_DEV_BAD_POSITION and that row is skipped.
+ * head_dim 64 or 128. */
+PKV_API int paged_kv_append_rope(const void* q, void* q_out, const void* k, const void* v,
+                                 const int64_t* slot_mapping, const int32_t* positions,
+                                 const float* cos_sin, int32_t max_position, int32_t num_tokens,
+                                 void* k_cache, void* v_cache, const pkv_cache_desc* desc,
+                                 void* stream);
 
 /* Bytes of workspace paged_attention_decode needs for `num_seqs` sequences
  * whose context lengths are at most `max_context_len` (0 on bad arguments). */

@@ -32,6 +32,7 @@ PKV_BF16 = 1
 DEVICE_ERRORS = {
     0: "ok", 1: "bad block id", 2: "bad context length", 3: "bad slot", 4: "bad copy pair",
     5: "bad query layout", 6: "pipeline wait timeout", 7: "block table too narrow",
+    8: "bad rotary position",
 }
 
 # every symbol the header declares (checked by the tests)
@@ -39,6 +40,7 @@ EXPORTS = (
     "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_num_free", "pkv_pool_can_allocate",
     "pkv_seq_add", "pkv_seq_fork", "pkv_seq_append_slot", "pkv_seq_free", "pkv_seq_len",
     "pkv_block_ref_count", "pkv_block_tables", "pkv_copy_blocks", "paged_kv_append",
+    "paged_kv_append_rope",
     "pkv_decode_workspace_bytes", "paged_attention_decode", "paged_attention_decode_noalloc",
     "pkv_varlen_workspace_bytes",
     "paged_attention_varlen", "pkv_device_error", "pkv_status_string", "pkv_splitfuse_compose",
@@ -84,6 +86,8 @@ def lib():
         "pkv_block_tables": (ctypes.c_int, [p, p, i32, i32, p, p]),
         "pkv_copy_blocks": (ctypes.c_int, [p, i32, p, p, P(CacheDesc), p]),
         "paged_kv_append": (ctypes.c_int, [p, p, p, i32, p, p, P(CacheDesc), p]),
+        "paged_kv_append_rope": (ctypes.c_int, [p, p, p, p, p, p, p, i32, i32, p, p,
+                                                P(CacheDesc), p]),
         "pkv_decode_workspace_bytes": (sz, [P(CacheDesc), i32, i32]),
         "paged_attention_decode": (ctypes.c_int, [p, p, p, p, P(CacheDesc), p, i32, p, i32, i32,
                                                   ctypes.c_float, p, sz, p]),
@@ -267,6 +271,29 @@ def paged_kv_append(k, v, slot_mapping, k_cache, v_cache, desc, stream=None):
     _check(lib().paged_kv_append(_ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache),
                                  _ptr(v_cache), ctypes.byref(desc), _stream(stream)),
            "paged_kv_append")
+
+
+def paged_kv_append_rope(k, v, slot_mapping, positions, cos_sin, k_cache, v_cache, desc,
+                         q=None, q_out=None, stream=None):
+    """Append with rotary embedding fused in: k rotated at `positions` (CUDA int32
+    [T]) using `cos_sin` (CUDA fp32 [max_position, D]); v copied; q (optional,
+    [T, Hq, D]) rotated into q_out (defaults to q, in place)."""
+    T = k.shape[0]
+    dt = _TORCH_DTYPE[desc.dtype]
+    for t, nm in ((k, "k"), (v, "v"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, dt, nm)
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    _need(positions, torch.int32, "positions")
+    _need(cos_sin, torch.float32, "cos_sin")
+    if q is not None:
+        _need(q, dt, "q")
+        q_out = q if q_out is None else q_out
+        _need(q_out, dt, "q_out")
+    _check(lib().paged_kv_append_rope(_ptr(q), _ptr(q_out), _ptr(k), _ptr(v), _ptr(slot_mapping),
+                                      _ptr(positions), _ptr(cos_sin), cos_sin.shape[0], T,
+                                      _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc),
+                                      _stream(stream)), "paged_kv_append_rope")
+    return q_out
 
 
 def decode_workspace_bytes(desc, num_seqs, max_context_len):

@@ -88,6 +88,130 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(CopyParams p) {
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// Rotary position embedding fused with the append ("第 15 章：推理引擎与部署"
+// §15.3 RoPE 与 Flash Attention 的融合: rotate in registers instead of a separate
+// pass through HBM; "DeepSpeed-FastGen 深度解析" §6 linear_blocked_kv_rotary:
+// rotary fused with the blocked-KV write).  Rotate-half form: for i < D/2,
+//   x'[i] = x[i] c - x[i+D/2] s,   x'[i+D/2] = x[i] s + x[i+D/2] c,
+// with (c, s) from the caller's table at the token's position.  Each product
+// and sum is rounded on its own (no fused multiply-add), then the result is
+// rounded to the cache dtype, so the stored bytes are reproducible exactly.
+// One thread handles 8 rotation pairs of one (token, row), where the rows of a
+// token are its Hq query heads, then its Hkv key heads, then its Hkv value
+// heads (values are copied unrotated).
+// ---------------------------------------------------------------------------
+struct RopeParams {
+    const void* q;
+    void* q_out;
+    const void* k;
+    const void* v;
+    const int64_t* slots;
+    const int32_t* positions;
+    const float* cos_sin;     // [max_position][D]: cos of the D/2 angles, then their sin
+    void* k_cache;
+    void* v_cache;
+    int64_t num_tokens;
+    int32_t num_q_rows;       // Hq, or 0 when q is not rotated
+    int32_t num_kv_heads;
+    int32_t block_size;
+    int32_t max_position;
+    int64_t num_slots;
+    int* err;
+};
+
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float (&x)[8]);
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&x)[8]) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float (&x)[8]) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+template <typename T>
+__device__ __forceinline__ void store8(T* p, const float (&x)[8]);
+template <>
+__device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* p, const float (&x)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+template <>
+__device__ __forceinline__ void store8<float>(float* p, const float (&x)[8]) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) append_rope_kernel(RopeParams p) {
+    constexpr int kChunks = D / 16;           // 8-pair chunks per head row
+    const int rows = p.num_q_rows + 2 * p.num_kv_heads;
+    const int64_t total = p.num_tokens * rows * kChunks;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t t = i / (int64_t(rows) * kChunks);
+        const int r = int(i / kChunks % rows);
+        const int c = int(i % kChunks);
+        const bool is_q = r < p.num_q_rows;
+        const bool is_v = r >= p.num_q_rows + p.num_kv_heads;
+        const int h = is_q ? r : (r - p.num_q_rows) % p.num_kv_heads;
+        int64_t dst_row = 0;
+        if (!is_q) {
+            const int64_t slot = __ldg(p.slots + t);
+            if (slot < 0) continue;                                    // padding token
+            if (slot >= p.num_slots) {
+                flag_error(p.err, PKV_DEV_BAD_SLOT);
+                continue;
+            }
+            const int64_t blk = slot / p.block_size;
+            dst_row = (blk * p.num_kv_heads + h) * p.block_size + (slot - blk * p.block_size);
+        }
+        const T* src = is_q ? static_cast<const T*>(p.q) + (t * p.num_q_rows + h) * D
+                            : static_cast<const T*>(is_v ? p.v : p.k) + (t * p.num_kv_heads + h) * D;
+        float x1[8], x2[8];
+        load8<T>(src + 8 * c, x1);
+        load8<T>(src + D / 2 + 8 * c, x2);
+        if (!is_v) {
+            const int pos = __ldg(p.positions + t);
+            if (pos < 0 || pos >= p.max_position) {
+                flag_error(p.err, PKV_DEV_BAD_POSITION);
+                continue;
+            }
+            const float* cs = p.cos_sin + int64_t(pos) * D;
+            float co[8], si[8];
+            load8<float>(cs + 8 * c, co);
+            load8<float>(cs + D / 2 + 8 * c, si);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float a = __fmul_rn(x1[j], co[j]), b = __fmul_rn(x2[j], si[j]);
+                const float e = __fmul_rn(x1[j], si[j]), f = __fmul_rn(x2[j], co[j]);
+                x1[j] = __fsub_rn(a, b);
+                x2[j] = __fadd_rn(e, f);
+            }
+        }
+        T* dst = is_q ? static_cast<T*>(p.q_out) + (t * p.num_q_rows + h) * D
+                      : static_cast<T*>(is_v ? p.v_cache : p.k_cache) + dst_row * D;
+        store8<T>(dst + 8 * c, x1);
+        store8<T>(dst + D / 2 + 8 * c, x2);
+    }
+}
+
 namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -161,5 +285,57 @@ extern "C" int pkv_copy_blocks(const int32_t* block_pairs, int32_t num_pairs, vo
     p.err = err;
     const unsigned gx = unsigned(std::min<int64_t>((p.vec_per_block + 255) / 256, 64));
     copy_blocks_kernel<<<dim3(gx, unsigned(num_pairs)), 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    return cuda_status(cudaGetLastError());
+}
+
+extern "C" int paged_kv_append_rope(const void* q, void* q_out, const void* k, const void* v,
+                                    const int64_t* slot_mapping, const int32_t* positions,
+                                    const float* cos_sin, int32_t max_position,
+                                    int32_t num_tokens, void* k_cache, void* v_cache,
+                                    const pkv_cache_desc* desc, void* stream) {
+    int st = check_desc(desc, false);
+    if (st != PKV_OK) return st;
+    if (num_tokens < 0 || max_position < 1) return PKV_ERR_INVALID;
+    if (num_tokens == 0) return PKV_OK;
+    if (desc->head_dim != 64 && desc->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (!k || !v || !slot_mapping || !positions || !cos_sin || !k_cache || !v_cache ||
+        (q && !q_out) || (!q && q_out))
+        return PKV_ERR_INVALID;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        !aligned16(cos_sin) || (q && (!aligned16(q) || !aligned16(q_out))) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) ||
+        (reinterpret_cast<uintptr_t>(positions) & 3u))
+        return PKV_ERR_INVALID;
+    int* err = device_error_ptr(&st);
+    if (st != PKV_OK) return st;
+    RopeParams p;
+    p.q = q;
+    p.q_out = q_out;
+    p.k = k;
+    p.v = v;
+    p.slots = slot_mapping;
+    p.positions = positions;
+    p.cos_sin = cos_sin;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.num_tokens = num_tokens;
+    p.num_q_rows = q ? desc->num_q_heads : 0;
+    p.num_kv_heads = desc->num_kv_heads;
+    p.block_size = desc->block_size;
+    p.max_position = max_position;
+    p.num_slots = int64_t(desc->num_blocks) * desc->block_size;
+    p.err = err;
+    const int64_t total = int64_t(num_tokens) * (p.num_q_rows + 2 * p.num_kv_heads) *
+                          (desc->head_dim / 16);
+    const int64_t blocks = std::min<int64_t>((total + 255) / 256, int64_t(std::max(sm_count(), 1)) * 8);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool bf = desc->dtype == PKV_BF16;
+    if (desc->head_dim == 128) {
+        if (bf) append_rope_kernel<__nv_bfloat16, 128><<<unsigned(blocks), 256, 0, s>>>(p);
+        else append_rope_kernel<float, 128><<<unsigned(blocks), 256, 0, s>>>(p);
+    } else {
+        if (bf) append_rope_kernel<__nv_bfloat16, 64><<<unsigned(blocks), 256, 0, s>>>(p);
+        else append_rope_kernel<float, 64><<<unsigned(blocks), 256, 0, s>>>(p);
+    }
     return cuda_status(cudaGetLastError());
 }

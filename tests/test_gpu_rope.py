@@ -1,0 +1,107 @@
+"""GPU parity for the rotary-embedding append: rotated q and cache bytes exact, then
+decode over the rotated values within tolerance."""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import workloads  # noqa: E402
+from oracle import attention, cache, rope  # noqa: E402
+from oracle.run import OracleState  # noqa: E402
+from tests.gpu_parity import TOL, cache_bytes_equal, out_f64  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+def _torch_rows(rows, dtype):
+    from paged_kv_cache_51_gb300.runner import _torch_rows as f
+
+    return f(rows, dtype)
+
+
+@pytest.mark.parametrize("dtype,hq,hkv,d", [("bf16", 32, 8, 128), ("bf16", 16, 16, 64),
+                                            ("f32", 8, 2, 128), ("f32", 8, 8, 64)])
+def test_append_rope_bit_exact_then_decode(lib, dtype, hq, hkv, d):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_51_gb300 import paged_attention_decode, paged_kv_append_rope, runner
+
+    lib.device_error(clear=True)
+    scale = 2.0 if dtype == "f32" else 1.0
+    w = workloads.random_decode(31, dtype, hq, hkv, d, 16, [5, 200, 1031, 2999], scale=scale)
+    max_pos = 4096
+    tab = rope.rope_table(max_pos, d)
+    # history on both sides (plain appends), then the step's tokens through the rotary append
+    dc = runner.DeviceCache(w)
+    dc.run_setup()
+    planned = dc.plan_step()
+    ost = OracleState(w)
+    ost.run_setup()
+    # oracle: its own pool gives the step's slots and positions
+    o_slots = []
+    for kind, seq, n, row in w.step:
+        if kind == "add":
+            o_slots += ost.pool.add_sequence(seq, n)[1]
+        else:
+            for _ in range(n):
+                o_slots.append(ost.pool.append_slot(seq)[0])
+    slots = np.array(o_slots, dtype=np.int64)
+    assert np.array_equal(slots, planned["slot_mapping"].numpy())
+    rows = np.concatenate([np.arange(row, row + n) for _, _, n, row in w.step])
+    positions = np.array([ost.pool.context_len(s) - 1 for s, _ in w.batch], dtype=np.int32)
+    q_ref = rope.append_rope(ost.k_cache, ost.v_cache, w.q, w.k_rows[rows], w.v_rows[rows],
+                             slots, positions, tab, w.block_size, w.dtype, cache.append)
+    # device
+    dev = "cuda"
+    q = _torch_rows(w.q, dtype).to(dev)
+    k_new = planned["k"].to(dev)
+    v_new = planned["v"].to(dev)
+    pos_d = torch.tensor([dc.pool.seq_len(s) - 1 for s, _ in w.batch], dtype=torch.int32,
+                         device=dev)
+    tab_d = torch.from_numpy(tab).to(dev)
+    q_out = torch.empty_like(q)
+    paged_kv_append_rope(k_new, v_new, planned["slot_mapping"].to(dev), pos_d, tab_d, dc.k_cache,
+                         dc.v_cache, dc.desc, q=q, q_out=q_out)
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0
+    got_q = q_out.cpu()
+    got_q = got_q.numpy() if dtype == "f32" else got_q.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got_q.view(np.uint8), np.ascontiguousarray(q_ref).view(np.uint8))
+    assert cache_bytes_equal(dc.k_cache, ost.k_cache)
+    assert cache_bytes_equal(dc.v_cache, ost.v_cache)
+    # in place rotation gives the same bytes
+    q2 = q.clone()
+    paged_kv_append_rope(k_new, v_new, planned["slot_mapping"].to(dev), pos_d, tab_d, dc.k_cache,
+                         dc.v_cache, dc.desc, q=q2)
+    torch.cuda.synchronize()
+    assert torch.equal(q2, q_out)
+    # decode over the rotated cache and query
+    tables, ctx, _ = dc.batch_metadata()
+    out = torch.empty_like(q)
+    paged_attention_decode(out, q_out, dc.k_cache, dc.v_cache, dc.desc, tables.to(dev),
+                           ctx.to(dev), int(ctx.max()))
+    torch.cuda.synchronize()
+    bt, octx, _ = ost.batch_metadata()
+    ref = attention.decode(q_ref, ost.k_cache, ost.v_cache, bt, octx, w.block_size, w.dtype)
+    d_ = np.abs(out_f64(out) - ref)
+    tmax, tmean = TOL[dtype]
+    assert float(d_.max()) <= tmax * (4 if dtype == "f32" else 1) and float(d_.mean()) <= tmean
+
+
+def test_bad_rotary_position_is_flagged(lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_51_gb300 import cache_desc, paged_kv_append_rope
+
+    kc = torch.zeros((4, 2, 16, 64), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    desc = cache_desc(kc, 2)
+    k = torch.ones((1, 2, 64), dtype=torch.bfloat16, device="cuda")
+    tab = torch.from_numpy(rope.rope_table(8, 64)).cuda()
+    pos = torch.tensor([8], dtype=torch.int32, device="cuda")       # table has 0..7
+    slots = torch.tensor([3], dtype=torch.int64, device="cuda")
+    lib.device_error(clear=True)
+    paged_kv_append_rope(k, k, slots, pos, tab, kc, vc, desc)
+    assert lib.device_error() == 8                                  # PKV_DEV_BAD_POSITION
+    assert torch.count_nonzero(kc) == 0                             # K row skipped
