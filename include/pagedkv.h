@@ -77,9 +77,11 @@ extern "C" {
 /* ---- data types -------------------------------------------------------- */
 #define PKV_F32  0
 #define PKV_BF16 1
+#define PKV_INT8 2   /* 8-bit codes + fp32 scales in the cache; q, k, v, out bf16 */
 
 typedef struct pkv_cache_desc {
-    int32_t dtype;        /* PKV_F32 or PKV_BF16: cache, q, k, v and out share it */
+    int32_t dtype;        /* PKV_F32 or PKV_BF16: cache, q, k, v and out share it;
+                             PKV_INT8: only the *_int8 entry points take it */
     int32_t num_blocks;   /* physical blocks in each of the K and V pools */
     int32_t block_size;   /* tokens per block (the kernels implement 16) */
     int32_t num_kv_heads;
@@ -284,6 +286,39 @@ PKV_API int paged_attention_varlen(void* out, const void* q, const void* k_cache
                            int32_t num_query_tokens, int32_t max_query_len,
                            int32_t max_context_len, float scale, void* workspace,
                            size_t workspace_bytes, void* stream);
+
+/* 8-bit KV cache [Deploy §2.5 LMDeploy, 2. TurboMind 推理引擎解析 (the KV cache
+ * kept in 8 bits, halving the bytes decode reads)].  The pages give no format;
+ * the one implemented is symmetric int8 with one fp32 scale per (token, kv head):
+ *   amax = max_d |x[d]|,  scale = amax / 127,
+ *   code[d] = clamp(rint(x[d] / scale), -127, 127)     (code = 0 when amax = 0)
+ * with both divisions rounded once in fp32 (ties to even), so the stored codes
+ * and scales are reproducible bit for bit.  A value reads back as code * scale.
+ * Pools (desc->dtype = PKV_INT8; block_size, heads and head_dim as above):
+ *   k_codes, v_codes:   device int8 [num_blocks][num_kv_heads][block_size][head_dim]
+ *   k_scales, v_scales: device fp32 [num_blocks][num_kv_heads][block_size]
+ * all 16-byte aligned.  head_dim 64 or 128.
+ *
+ * Append: k, v device bf16 [num_tokens][num_kv_heads][head_dim], quantised and
+ * written through slot_mapping as paged_kv_append writes (negative slot skips;
+ * slot >= num_blocks * block_size sets PKV_DEV_BAD_SLOT and is skipped). */
+PKV_API int paged_kv_append_int8(const void* k, const void* v, const int64_t* slot_mapping,
+                                 int32_t num_tokens, void* k_codes, void* v_codes,
+                                 float* k_scales, float* v_scales, const pkv_cache_desc* desc,
+                                 void* stream);
+
+/* Decode attention over the 8-bit cache: exactly the attention of
+ * paged_attention_decode over the dequantised keys and values (code * scale),
+ * computed with the same splits and merge.  q, out: device bf16
+ * [num_seqs][num_q_heads][head_dim].  workspace: >= pkv_decode_workspace_bytes
+ * of the same desc.  Other arguments and errors as for paged_attention_decode. */
+PKV_API int paged_attention_decode_int8(void* out, const void* q, const void* k_codes,
+                                        const void* v_codes, const float* k_scales,
+                                        const float* v_scales, const pkv_cache_desc* desc,
+                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t* context_lens, int32_t num_seqs,
+                                        int32_t max_context_len, float scale, void* workspace,
+                                        size_t workspace_bytes, void* stream);
 
 /* Read the current device's error word into *code_out (PKV_DEV_* code of the
  * first fault recorded since the last clear) and, if `clear` is non-zero,

@@ -28,10 +28,13 @@ Modules
   sketch       the pages' per-block-normalised sketch (a negative control)
   kv_size      closed-form KV-cache size
   splitfuse    token-budget composition of one forward pass (decodes + prompt chunks)
+  rope         rotate-half rotary embedding fused into the append (fp32, bf16 rounding)
+  quant        8-bit KV cache: per-(token, head) symmetric int8 codes and decode over them
 
 Parity: every function here is pinned by ``tests/test_oracle_*.py`` against
 values the pages print, closed forms, brute force on unpaged data, or
 invariants; none is marked "parity unpinned".
 """
 
-from . import attention, block_pool, cache, kv_size, numerics, online, sketch, splitfuse  # noqa: F401
+from . import (attention, block_pool, cache, kv_size, numerics, online, quant, rope,  # noqa: F401
+               sketch, splitfuse)

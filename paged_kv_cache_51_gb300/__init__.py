@@ -28,6 +28,7 @@ PKV_ERR_HOST = -7
 
 PKV_F32 = 0
 PKV_BF16 = 1
+PKV_INT8 = 2
 
 DEVICE_ERRORS = {
     0: "ok", 1: "bad block id", 2: "bad context length", 3: "bad slot", 4: "bad copy pair",
@@ -44,6 +45,7 @@ EXPORTS = (
     "pkv_decode_workspace_bytes", "paged_attention_decode", "paged_attention_decode_noalloc",
     "pkv_varlen_workspace_bytes",
     "paged_attention_varlen", "pkv_device_error", "pkv_status_string", "pkv_splitfuse_compose",
+    "paged_kv_append_int8", "paged_attention_decode_int8",
 )
 
 
@@ -99,6 +101,9 @@ def lib():
         "pkv_device_error": (ctypes.c_int, [P(i32), i32]),
         "pkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "pkv_splitfuse_compose": (ctypes.c_int, [i32, i32, i32, p, p, P(i32), P(i32)]),
+        "paged_kv_append_int8": (ctypes.c_int, [p, p, p, i32, p, p, p, p, P(CacheDesc), p]),
+        "paged_attention_decode_int8": (ctypes.c_int, [p, p, p, p, p, p, P(CacheDesc), p, i32, p,
+                                                       i32, i32, ctypes.c_float, p, sz, p]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -380,6 +385,70 @@ def paged_attention_varlen(out, q, k_cache, v_cache, desc, block_tables, query_s
                                         _ptr(context_lens), S, Tq, max_query_len, max_context_len,
                                         scale, _ptr(ws), ws.numel(), _stream(stream)),
            "paged_attention_varlen")
+    return out
+
+
+class Int8Cache:
+    """The four pools of an 8-bit KV cache: codes int8 [NB, Hkv, bs, D] and
+    scales fp32 [NB, Hkv, bs], for K and for V (see paged_kv_append_int8 in
+    include/pagedkv.h for the format)."""
+
+    def __init__(self, num_blocks, num_kv_heads, block_size, head_dim, num_q_heads,
+                 device="cuda"):
+        shape = (num_blocks, num_kv_heads, block_size, head_dim)
+        self.k_codes = torch.zeros(shape, dtype=torch.int8, device=device)
+        self.v_codes = torch.zeros(shape, dtype=torch.int8, device=device)
+        self.k_scales = torch.zeros(shape[:3], dtype=torch.float32, device=device)
+        self.v_scales = torch.zeros(shape[:3], dtype=torch.float32, device=device)
+        self.desc = CacheDesc(PKV_INT8, num_blocks, block_size, num_kv_heads, num_q_heads,
+                              head_dim)
+
+    def tensors(self):
+        return self.k_codes, self.v_codes, self.k_scales, self.v_scales
+
+
+def _need_int8_cache(c):
+    for t, dt, nm in ((c.k_codes, torch.int8, "k_codes"), (c.v_codes, torch.int8, "v_codes"),
+                      (c.k_scales, torch.float32, "k_scales"),
+                      (c.v_scales, torch.float32, "v_scales")):
+        _need(t, dt, nm)
+
+
+def paged_kv_append_int8(k, v, slot_mapping, cache, stream=None):
+    """Quantise k, v (CUDA bf16 [T, Hkv, D]) into the 8-bit cache through
+    slot_mapping (CUDA int64 [T])."""
+    _need(k, torch.bfloat16, "k")
+    _need(v, torch.bfloat16, "v")
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    _need_int8_cache(cache)
+    _check(lib().paged_kv_append_int8(_ptr(k), _ptr(v), _ptr(slot_mapping), k.shape[0],
+                                      _ptr(cache.k_codes), _ptr(cache.v_codes),
+                                      _ptr(cache.k_scales), _ptr(cache.v_scales),
+                                      ctypes.byref(cache.desc), _stream(stream)),
+           "paged_kv_append_int8")
+
+
+def paged_attention_decode_int8(out, q, cache, block_tables, context_lens, max_context_len,
+                                scale=None, ws=None, stream=None):
+    """Decode attention over the 8-bit cache; out, q: CUDA bf16 [S, Hq, D]."""
+    S = q.shape[0]
+    _need(out, torch.bfloat16, "out")
+    _need(q, torch.bfloat16, "q")
+    _need_int8_cache(cache)
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    desc = cache.desc
+    if scale is None:
+        scale = 1.0 / math.sqrt(desc.head_dim)
+    if ws is None:
+        ws = workspace(decode_workspace_bytes(desc, S, max_context_len), q.device)
+    _check(lib().paged_attention_decode_int8(_ptr(out), _ptr(q), _ptr(cache.k_codes),
+                                             _ptr(cache.v_codes), _ptr(cache.k_scales),
+                                             _ptr(cache.v_scales), ctypes.byref(desc),
+                                             _ptr(block_tables), block_tables.shape[1],
+                                             _ptr(context_lens), S, max_context_len, scale,
+                                             _ptr(ws), ws.numel(), _stream(stream)),
+           "paged_attention_decode_int8")
     return out
 
 

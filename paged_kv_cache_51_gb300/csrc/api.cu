@@ -105,8 +105,11 @@ int check_attention_common(void* out, const void* q, const void* k_cache, const 
 
 extern "C" size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs,
                                              int32_t max_context_len) {
-    if (check_desc(desc, false) != PKV_OK || num_seqs < 0 || max_context_len < 1) return 0;
-    return workspace_layout(desc, num_seqs, max_context_len, 0, nullptr, nullptr);
+    if (!desc) return 0;
+    pkv_cache_desc d = *desc;
+    if (d.dtype == PKV_INT8) d.dtype = PKV_BF16;  // the partials do not depend on the cache type
+    if (check_desc(&d, false) != PKV_OK || num_seqs < 0 || max_context_len < 1) return 0;
+    return workspace_layout(&d, num_seqs, max_context_len, 0, nullptr, nullptr);
 }
 
 extern "C" size_t pkv_varlen_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs,

@@ -27,6 +27,7 @@
 #include <cfloat>
 #include <cuda_runtime.h>
 
+#include "decode_common.cuh"
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -240,55 +241,6 @@ struct SplitCfg {
     static_assert(kDPL == 2 || kDPL == 4, "head_dim 64 or 128");
     static_assert(kNV == 16 || kNV == 32, "group size 1, 2, 4 or 8");
 };
-
-// Reduce-scatter across the warp: every lane holds NV partial sums; afterwards
-// lane l holds the full sum of value l (NV = 32) or of value l >> 1 (NV = 16).
-template <int NV>
-__device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane) {
-#pragma unroll
-    for (int step = 0; (NV >> step) > 1; ++step) {
-        const int n = NV >> step;
-        const int off = 16 >> step;
-        const bool upper = (lane & off) != 0;
-#pragma unroll
-        for (int i = 0; i < n / 2; ++i) {
-            const float send = upper ? v[i] : v[i + n / 2];
-            const float keep = upper ? v[i + n / 2] : v[i];
-            v[i] = keep + __shfl_xor_sync(kFull, send, off);
-        }
-    }
-    float r = v[0];
-    if (NV == 16) r += __shfl_xor_sync(kFull, r, 1);
-    return r;
-}
-
-// max / sum over the lanes that hold the same query head
-template <int G, int TC>
-__device__ __forceinline__ float group_max(float x) {
-    if (G == 1) {
-#pragma unroll
-        for (int off = 2; off < 32; off <<= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, off));
-    } else {
-#pragma unroll
-        for (int off = 1; off < TC; off <<= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, off));
-    }
-    return x;
-}
-template <int G, int TC>
-__device__ __forceinline__ float group_sum(float x) {
-    if (G == 1) {
-#pragma unroll
-        for (int off = 2; off < 32; off <<= 1) x += __shfl_xor_sync(kFull, x, off);
-    } else {
-#pragma unroll
-        for (int off = 1; off < TC; off <<= 1) x += __shfl_xor_sync(kFull, x, off);
-    }
-    return x;
-}
-
-__device__ __forceinline__ void consumer_sync(int nthreads) {
-    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
 
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(SplitCfg<T, D, G>::kThreads)

@@ -170,3 +170,38 @@ def test_device_calls_reject_bad_arguments_before_launch(lib):
     # zero-sized work is a no-op
     assert L.paged_kv_append(None, None, None, 0, None, None, ref(desc), None) == 0
     assert L.pkv_copy_blocks(None, 0, None, None, ref(desc), None) == 0
+
+
+def test_int8_entry_points_validate_on_the_host(lib):
+    L = lib.lib()
+    ref = ctypes.byref
+    i8 = lib.CacheDesc(lib.PKV_INT8, 100, 16, 8, 32, 128)
+    bf = lib.CacheDesc(lib.PKV_BF16, 100, 16, 8, 32, 128)
+    fake = ctypes.c_void_p(1 << 20)
+    # the split partials do not depend on the cache type
+    assert lib.decode_workspace_bytes(i8, 64, 4096) == lib.decode_workspace_bytes(bf, 64, 4096)
+    # the 8-bit calls take only PKV_INT8, the others never take it
+    assert L.paged_kv_append_int8(fake, fake, fake, 4, fake, fake, fake, fake, ref(bf),
+                                  None) == lib.PKV_ERR_UNSUPPORTED
+    assert L.paged_attention_decode_int8(fake, fake, fake, fake, fake, fake, ref(bf), fake, 4,
+                                         fake, 1, 16, 0.1, fake, 1 << 20,
+                                         None) == lib.PKV_ERR_UNSUPPORTED
+    assert L.paged_kv_append(fake, fake, fake, 4, fake, fake, ref(i8), None) == \
+        lib.PKV_ERR_UNSUPPORTED
+    assert L.paged_attention_decode(fake, fake, fake, fake, ref(i8), fake, 4, fake, 1, 16, 0.1,
+                                    fake, 1 << 20, None) == lib.PKV_ERR_UNSUPPORTED
+    # null pointers, misaligned scales, head_dim, workspace, empty work
+    assert L.paged_kv_append_int8(None, fake, fake, 4, fake, fake, fake, fake, ref(i8),
+                                  None) == lib.PKV_ERR_INVALID
+    assert L.paged_kv_append_int8(fake, fake, fake, 4, fake, fake, ctypes.c_void_p((1 << 20) + 4),
+                                  fake, ref(i8), None) == lib.PKV_ERR_INVALID
+    d96 = lib.CacheDesc(lib.PKV_INT8, 100, 16, 8, 32, 96)
+    assert L.paged_kv_append_int8(fake, fake, fake, 4, fake, fake, fake, fake, ref(d96),
+                                  None) == lib.PKV_ERR_UNSUPPORTED
+    assert L.paged_attention_decode_int8(fake, fake, fake, fake, fake, fake, ref(i8), fake, 4,
+                                         fake, 64, 4096, 0.1, fake, 256,
+                                         None) == lib.PKV_ERR_WORKSPACE
+    assert L.paged_attention_decode_int8(fake, fake, fake, fake, fake, fake, ref(i8), fake, 4,
+                                         fake, 1, 16, float("nan"), fake, 1 << 20,
+                                         None) == lib.PKV_ERR_INVALID
+    assert L.paged_kv_append_int8(None, None, None, 0, None, None, None, None, ref(i8), None) == 0

@@ -1,0 +1,125 @@
+"""GPU parity for the 8-bit KV cache: codes and scales bit-exact against the
+oracle's quantiser, decode within the bf16 tolerance of exact attention over
+the dequantised cache."""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import workloads  # noqa: E402
+from oracle import quant  # noqa: E402
+from oracle.run import execute  # noqa: E402
+from tests.gpu_parity import TOL, out_f64  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+def _bf16_tensor(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+
+def _pool_rows(c):
+    """[NB, Hkv, bs, D] -> rows [NB * bs, Hkv, D] (row index = slot)."""
+    nb, hkv, bs, d = c.shape
+    return np.ascontiguousarray(np.swapaxes(c, 1, 2).reshape(nb * bs, hkv, d))
+
+
+def _fill(lib, w, ost, slot_perm_seed):
+    """Quantise the oracle's final bf16 cache (every slot, in shuffled order) into a
+    device 8-bit cache; returns it with the oracle's codes and scales."""
+    ic = lib.Int8Cache(w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim, w.num_q_heads)
+    k_rows = _pool_rows(ost.k_cache)
+    v_rows = _pool_rows(ost.v_cache)
+    n = k_rows.shape[0]
+    order = np.random.default_rng(slot_perm_seed).permutation(n)
+    slots = order.astype(np.int64)
+    slots[::7] = -1                                             # padding rows are skipped
+    keep = slots >= 0
+    lib.paged_kv_append_int8(_bf16_tensor(k_rows[order]).cuda(), _bf16_tensor(v_rows[order]).cuda(),
+                             torch.from_numpy(slots).cuda(), ic)
+    # the skipped slots take a second pass, in their own order
+    rest = order[~keep]
+    lib.paged_kv_append_int8(_bf16_tensor(k_rows[rest]).cuda(), _bf16_tensor(v_rows[rest]).cuda(),
+                             torch.from_numpy(rest.astype(np.int64)).cuda(), ic)
+    shape = ost.k_cache.shape
+    kq = np.zeros(shape, np.int8)
+    vq = np.zeros(shape, np.int8)
+    ks = np.zeros(shape[:3], np.float32)
+    vs = np.zeros(shape[:3], np.float32)
+    quant.append_int8(kq, ks, vq, vs, k_rows, v_rows, np.arange(n), w.block_size, "bf16")
+    return ic, (kq, ks, vq, vs)
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(32, 32, 128), (32, 8, 128), (16, 8, 64), (64, 8, 128),
+                                      (8, 8, 64)])
+def test_int8_append_bit_exact_and_decode(lib, hq, hkv, d):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    lib.device_error(clear=True)
+    w = workloads.random_decode(41 + hq + d, "bf16", hq, hkv, d, 16, [1, 5, 16, 17, 200, 513,
+                                                                     1031, 2999], scale=2.0)
+    ost, _ = execute(w, with_attention=False)
+    ic, (kq, ks, vq, vs) = _fill(lib, w, ost, hq * 7 + d)
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0
+    assert np.array_equal(ic.k_codes.cpu().numpy(), kq)
+    assert np.array_equal(ic.v_codes.cpu().numpy(), vq)
+    assert np.array_equal(ic.k_scales.cpu().numpy().view(np.uint32), ks.view(np.uint32))
+    assert np.array_equal(ic.v_scales.cpu().numpy().view(np.uint32), vs.view(np.uint32))
+    bt, ctx, _ = ost.batch_metadata()
+    q = _bf16_tensor(w.q).cuda()
+    out = torch.empty_like(q)
+    lib.paged_attention_decode_int8(out, q, ic, torch.from_numpy(bt).cuda(),
+                                    torch.from_numpy(ctx).cuda(), int(ctx.max()))
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0
+    ref = quant.decode_int8(w.q, kq, ks, vq, vs, bt, ctx, w.block_size, "bf16")
+    diff = np.abs(out_f64(out) - ref)
+    tmax, tmean = TOL["bf16"]
+    assert float(diff.max()) <= tmax and float(diff.mean()) <= tmean
+
+
+def test_int8_extremes_and_zero_rows(lib):
+    """All-zero rows (scale 0), a row of one spike, bf16 subnormals and the
+    largest bf16 values quantise exactly as the oracle does."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    hkv, d = 2, 128
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((12, hkv, d)).astype(np.float32)
+    x[0] = 0.0
+    x[1] = 0.0
+    x[1, :, 5] = -3.0
+    x[2] *= 1e-39                                               # subnormal range
+    x[3] *= 1e37                                                # near the top of the range
+    x[4, 0, :] = 1.0                                            # constant row
+    bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    ic = lib.Int8Cache(2, hkv, 16, d, hkv)
+    slots = np.arange(12, dtype=np.int64) + 3
+    lib.device_error(clear=True)
+    lib.paged_kv_append_int8(_bf16_tensor(bits).cuda(), _bf16_tensor(bits[::-1]).cuda(),
+                             torch.from_numpy(slots).cuda(), ic)
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0
+    kq = np.zeros((2, hkv, 16, d), np.int8)
+    vq = np.zeros_like(kq)
+    ks = np.zeros((2, hkv, 16), np.float32)
+    vs = np.zeros_like(ks)
+    quant.append_int8(kq, ks, vq, vs, bits, np.ascontiguousarray(bits[::-1]), slots, 16, "bf16")
+    assert np.array_equal(ic.k_codes.cpu().numpy(), kq)
+    assert np.array_equal(ic.v_codes.cpu().numpy(), vq)
+    assert np.array_equal(ic.k_scales.cpu().numpy().view(np.uint32), ks.view(np.uint32))
+    assert np.array_equal(ic.v_scales.cpu().numpy().view(np.uint32), vs.view(np.uint32))
+    assert ks[0, 0, 3] == 0 and np.all(kq[0, :, 3] == 0)
+
+
+def test_int8_bad_slot_is_flagged(lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ic = lib.Int8Cache(2, 2, 16, 64, 2)
+    k = torch.ones((2, 2, 64), dtype=torch.bfloat16, device="cuda")
+    lib.device_error(clear=True)
+    lib.paged_kv_append_int8(k, k, torch.tensor([1, 32], dtype=torch.int64, device="cuda"), ic)
+    assert lib.device_error() == 3                                  # PKV_DEV_BAD_SLOT
+    assert int(torch.count_nonzero(ic.k_codes)) == 2 * 64           # slot 1 written, 32 skipped
