@@ -64,15 +64,25 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def ncu_traffic(kernel_src):
+DECODE_SOURCES = ("decode.cu", "decode_common.cuh", "pkv_device.cuh")
+INT8_SOURCES = ("kv_int8.cu", "decode_common.cuh", "pkv_device.cuh")
+
+
+def source_hash(sources):
+    """sha256 over the kernel's source files (csrc/), in the order given."""
+    h = hashlib.sha256()
+    for name in sources:
+        with open(os.path.join(ROOT, "paged_kv_cache_51_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(profile, sources):
     """DRAM bytes per launch recorded from an ncu capture, if the kernel is unchanged since."""
-    prof = os.path.join(ROOT, "profiles", "decode_attention_llama2_7b.md")
-    src = os.path.join(ROOT, "paged_kv_cache_51_gb300", "csrc", kernel_src)
     try:
-        with open(src, "rb") as f:
-            h = hashlib.sha256(f.read()).hexdigest()
+        h = source_hash(sources)
         vals = {}
-        with open(prof) as f:
+        with open(os.path.join(ROOT, "profiles", profile)) as f:
             for line in f:
                 if ":" in line and line.strip().startswith("- "):
                     k, v = line.strip()[2:].split(":", 1)
@@ -350,6 +360,76 @@ def mixed_batch_summary(steps, warmup):
     }
 
 
+def int8_decode_summary(w, dc, step, steps, warmup, bf16_attn_ms, full_size):
+    """The same decode batch over an 8-bit copy of the cache: every slot of the
+    bf16 pools quantised by the int8 append, then the int8 attention call timed
+    alone (inputs larger than L2)."""
+    import torch
+
+    import paged_kv_cache_51_gb300 as pkv
+
+    nb, hkv, bs, d = dc.k_cache.shape
+    ic = pkv.Int8Cache(nb, hkv, bs, d, w.num_q_heads)
+
+    def rows(c):
+        return c.transpose(1, 2).reshape(nb * bs, hkv, d).contiguous()
+
+    slots = torch.arange(nb * bs, dtype=torch.int64, device="cuda")
+    pkv.paged_kv_append_int8(rows(dc.k_cache), rows(dc.v_cache), slots, ic)
+    S = step.q.shape[0]
+    out = torch.empty_like(step.q)
+    ws = pkv.workspace(pkv.decode_workspace_bytes(ic.desc, S, step.max_ctx))
+    stream = torch.cuda.current_stream()
+
+    def call():
+        pkv.paged_attention_decode_int8(out, step.q, ic, step.tables, step.ctx, step.max_ctx,
+                                        ws=ws)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evs:
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    if pkv.device_error() != 0:
+        raise SystemExit("device error in the int8 decode")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    # the step's own tokens through the quantising append
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(steps):
+        pkv.paged_kv_append_int8(step.k_new, step.v_new, step.slot_mapping, ic)
+    a1.record(stream)
+    torch.cuda.synchronize()
+    app_ms = a0.elapsed_time(a1) / steps
+    ctx = [int(c) for c in step.ctx.cpu().tolist()]
+    kv = sum(ctx) * hkv * 2 * (d + 4)
+    qo = S * w.num_q_heads * d * 2 * 2
+    tables = sum(math.ceil(c / bs) for c in ctx) * 4 + 4 * S
+    nbytes = kv + qo + tables
+    bw, kind, _, _ = peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    diff = float((out.float() - step.out.float()).abs().max())
+    del ic, ws
+    torch.cuda.empty_cache()
+    return {
+        "kernel": "paged_attention_decode_int8 (planner + int8 split + merge)",
+        "ms_per_launch": ms, "bytes_per_launch": nbytes, "achieved_gbs": gbs,
+        "frac": gbs / bw, "peak": bw, "peak_kind": f"{kind} hbm_gbs (burst copy)",
+        "speedup_vs_bf16_attention": bf16_attn_ms / ms,
+        "context_tokens_per_s": sum(ctx) / (ms * 1e-3),
+        "append_ms_per_step": app_ms,
+        "max_abs_diff_vs_bf16_cache": diff,
+        "traffic": ncu_traffic("decode_int8_llama2_7b.md", INT8_SOURCES) if full_size else None,
+        "note": "same sequences, contexts and q as the headline; bytes = codes + fp32 scales "
+                "of every attended key + q/out + tables",
+    }
+
+
 def run_gpu(args):
     import torch
 
@@ -432,6 +512,11 @@ def run_gpu(args):
                          + (1 if math.ceil(step.max_ctx / 512) > 1 else 0)
                          + (1 if step.max_qlen > 1 else 0))
     clocks = sampler.summary(t_wall0, t_wall1)
+    int8 = None
+    if world == 1 and step.decode_only and w.dtype == "bf16" and not args.no_int8:
+        step.run()   # step.out holds the bf16 result for the comparison
+        int8 = int8_decode_summary(w, dc, step, min(args.steps, 200), args.warmup, attn_ms,
+                                   args.config == 2 and not args.batch)
     del dc, step
     torch.cuda.empty_cache()
     if rank != 0:
@@ -460,13 +545,14 @@ def run_gpu(args):
         "tokens_per_s": acc["query_tokens"] * world / (ms_per_step * 1e-3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
-                     "traffic": ncu_traffic("decode.cu") if args.config == 2 and not args.batch
-                     else None,
+                     "traffic": ncu_traffic("decode_attention_llama2_7b.md", DECODE_SOURCES)
+                     if args.config == 2 and not args.batch else None,
                      "kernel": "paged attention call (planner + split + merge"
                                + (" + tcgen05 prefill)" if acc["prefill_flops"] else ")"),
                      "bytes_per_launch": attn_b, "ms_per_launch": attn_ms,
                      "peak_kind": f"{peak_kind} hbm_gbs (burst copy)"},
         "mixed_batch": mixed,
+        "int8_kv_decode": int8,
         "cpu_baseline": cpu,
         "e2e": {"value": step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
@@ -499,6 +585,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-mixed", action="store_true",
                     help="skip the mixed-batch (SplitFuse) sub-measurement")
+    ap.add_argument("--no-int8", action="store_true",
+                    help="skip the 8-bit KV cache decode sub-measurement")
     ap.add_argument("--cpu-worker", action="store_true")
     ap.add_argument("--cpu-seqs", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -294,10 +294,17 @@ PKV_API int paged_attention_varlen(void* out, const void* q, const void* k_cache
  *   code[d] = clamp(rint(x[d] / scale), -127, 127)     (code = 0 when amax = 0)
  * with both divisions rounded once in fp32 (ties to even), so the stored codes
  * and scales are reproducible bit for bit.  A value reads back as code * scale.
- * Pools (desc->dtype = PKV_INT8; block_size, heads and head_dim as above):
- *   k_codes, v_codes:   device int8 [num_blocks][num_kv_heads][block_size][head_dim]
- *   k_scales, v_scales: device fp32 [num_blocks][num_kv_heads][block_size]
- * all 16-byte aligned.  head_dim 64 or 128.
+ * Pools (desc->dtype = PKV_INT8; block_size 16; head_dim 64 or 128):
+ *   k_codes, v_codes:   device int8, one tile of 16 * head_dim bytes per
+ *                       (block, kv head), tiles ordered [num_blocks][num_kv_heads]
+ *   k_scales, v_scales: device fp32 [num_blocks][num_kv_heads][16]
+ * all 16-byte aligned.  Inside a tile, the code of token row r (slot % 16)
+ * and dimension d is stored at
+ *   K: r * head_dim + 16 * ((d / 16) ^ sw(r)) + d % 16,
+ *      sw(r) = r & 7 (head_dim 128) or (r >> 1) & 3 (head_dim 64)
+ *   V: d * 16 + r
+ * (layouts the decode kernel reads without shared-memory bank conflicts).
+ * Whole tiles can be moved as bytes: the layout depends only on r.
  *
  * Append: k, v device bf16 [num_tokens][num_kv_heads][head_dim], quantised and
  * written through slot_mapping as paged_kv_append writes (negative slot skips;

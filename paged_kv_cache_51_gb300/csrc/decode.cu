@@ -239,6 +239,9 @@ struct SplitCfg {
     static constexpr size_t kQueueOff = kBarOff + 2 * kStages * 8;
     static constexpr size_t kSmem = kQueueOff + sizeof(UnitQueue);
     static_assert(kDPL == 2 || kDPL == 4, "head_dim 64 or 128");
+    // a consumer warp waits on a stage by parity: its previous use must be the
+    // same warp's own tile (tiles of a unit go to warps round-robin)
+    static_assert(kStages % kWarps == 0, "stage ring must be a multiple of the consumer warps");
     static_assert(kNV == 16 || kNV == 32, "group size 1, 2, 4 or 8");
 };
 

@@ -65,6 +65,9 @@ struct MmaCfg {
     static constexpr int kQueueOff = kBarOff + 2 * kStages * 8;
     static constexpr int kSmem = kQueueOff + int(sizeof(UnitQueue)) + 1024;  // + alignment slack
     static_assert(G == 2 || G == 4 || G == 8, "group size");
+    // a consumer warp waits on a stage by parity: its previous use must be the
+    // same warp's own tile (tiles of a unit go to warps round-robin)
+    static_assert(kStages % kWarps == 0, "stage ring must be a multiple of the consumer warps");
 };
 
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y,

@@ -5,14 +5,30 @@
 // symmetric int8 with one fp32 scale per (token, KV head),
 //   amax = max_d |x[d]|,  scale = amax / 127,  code = clamp(rint(x / scale), -127, 127)
 // (code = 0, scale = 0 for an all-zero row), each division rounded once in
-// fp32, so the stored codes are reproducible exactly.  Pools: codes
-// [NB][Hkv][bs][D] int8 and scales [NB][Hkv][bs] fp32, for K and for V.
+// fp32, so the stored codes are reproducible exactly.
 //
-// Decode reads a (block, head) tile as 16·D bytes of codes plus 64 bytes of
-// scales (two bulk copies each for K and V).  The score of key t is
-// scale_k[t] · (q · code_k[t]), and the V scale is folded into p, so the
-// dequantisation costs one multiply per key.  Everything else (work units,
-// online softmax, split merge) is the bf16 decode path's.
+// Tile layout.  One (block, KV head) tile holds 16 tokens.  K codes are
+// row-major [token][D] with the 16-byte chunks of row r XOR-swizzled
+// (chunk c stored at c ^ sw(r), sw(r) = r & 7 for D = 128 and (r >> 1) & 3 for
+// D = 64); V codes are dim-major [D][token].  Scales are [token] fp32.  Both
+// code layouts let a warp load its tensor-core fragments as 32-bit words with
+// no shared-memory bank conflicts.
+//
+// Decode runs both products on tensor cores (mma.sync m16n8k16, f16 in, fp32
+// accumulate), which keeps the kernel on the HBM roofline for every group size:
+//   * codes become f16 exactly: flipping the sign bit gives the byte c + 128, a
+//     byte permute places two such bytes in the mantissas of 1024 (f16 0x64xx),
+//     and one packed subtraction of 1152 leaves c;
+//   * q (bf16) is exact in f16 after a power-of-two shift chosen per work unit
+//     (largest |q| in [2^14, 2^15)); the shift is undone on the fp32 scores;
+//   * S = K q^T (tokens x heads) is scaled per token by the K scale;
+//   * the V scale is folded into P, P' = p * v_scale * 2^(127 - e_v), where e_v
+//     is the running largest V-scale exponent of the unit, so P' < 2 fits f16;
+//     when e_v grows the accumulator is rescaled with the softmax alpha;
+//   * O^T = V^T P' (dims x heads) accumulates in the mma's fp32 registers.
+// Work units, the online softmax, the warp combine and the split merge are
+// the bf16 decode path's.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -24,6 +40,12 @@
 
 namespace pkv {
 namespace {
+
+// 16-byte chunk swizzle of the K tile row r
+template <int D>
+__host__ __device__ constexpr int k_swizzle(int r) {
+    return D == 128 ? (r & 7) : ((r >> 1) & 3);
+}
 
 // ---------------------------------------------------------------------------
 // Append: one warp per (token, KV head) row; K and V rows of a token handled
@@ -80,27 +102,40 @@ __global__ void __launch_bounds__(256) append_int8_kernel(AppendI8Params p) {
 #pragma unroll
         for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullWarp, amax, off));
         const float scale = __fdiv_rn(amax, 127.f);
-        uint32_t packed = 0;
+        int32_t code[DPL];
 #pragma unroll
         for (int i = 0; i < DPL; ++i) {
             float c = scale > 0.f ? rintf(__fdiv_rn(x[i], scale)) : 0.f;
-            c = fminf(fmaxf(c, -127.f), 127.f);
-            packed |= (uint32_t(int32_t(c)) & 0xffu) << (8 * i);
+            code[i] = int32_t(fminf(fmaxf(c, -127.f), 127.f));
         }
         const int64_t blk = slot / p.block_size;
-        const int64_t row = (blk * p.num_kv_heads + h) * p.block_size + (slot - blk * p.block_size);
-        int8_t* dst = (is_v ? p.v_codes : p.k_codes) + row * D + lane * DPL;
-        if constexpr (DPL == 4) {
-            *reinterpret_cast<uint32_t*>(dst) = packed;
+        const int rr = int(slot - blk * p.block_size);           // token row within the tile
+        const int64_t tile = blk * p.num_kv_heads + h;
+        if (!is_v) {
+            // row-major, 16-byte chunk (lane * DPL) / 16 swizzled by the row
+            const int d0 = lane * DPL;
+            int8_t* dst = p.k_codes + tile * (kBlockTokens * D) + rr * D +
+                          (((d0 >> 4) ^ k_swizzle<D>(rr)) << 4) + (d0 & 15);
+            uint32_t packed = 0;
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) packed |= (uint32_t(code[i]) & 0xffu) << (8 * i);
+            if constexpr (DPL == 4) {
+                *reinterpret_cast<uint32_t*>(dst) = packed;
+            } else {
+                *reinterpret_cast<uint16_t*>(dst) = uint16_t(packed);
+            }
         } else {
-            *reinterpret_cast<uint16_t*>(dst) = uint16_t(packed);
+            // dim-major: byte (d, rr) at d * 16 + rr
+            int8_t* dst = p.v_codes + tile * (kBlockTokens * D) + rr;
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) dst[(lane * DPL + i) * kBlockTokens] = int8_t(code[i]);
         }
-        if (lane == 0) (is_v ? p.v_scales : p.k_scales)[row] = scale;
+        if (lane == 0) (is_v ? p.v_scales : p.k_scales)[tile * kBlockTokens + rr] = scale;
     }
 }
 
 // ---------------------------------------------------------------------------
-// Decode split kernel (CUDA cores, any group size 1/2/4/8).
+// Decode split kernel (tensor cores, group size 1, 2, 4 or 8).
 // ---------------------------------------------------------------------------
 struct SplitI8Params {
     const __nv_bfloat16* q;
@@ -129,45 +164,71 @@ template <int D, int G>
 struct I8Cfg {
     static constexpr int kWarps = 4;
     static constexpr int kThreads = (kWarps + 1) * 32;
-    static constexpr int kDPL = D / 32;
+    static constexpr int kKB = D / 16;                       // 16-dim blocks
     static constexpr int kTileBytes = kBlockTokens * D;      // codes of one (block, head)
     static constexpr int kScaleBytes = kBlockTokens * 4;     // their scales
     // stage: [K codes][V codes][K scales][V scales]
     static constexpr int kStageBytes = 2 * kTileBytes + 2 * kScaleBytes;
-    static constexpr int kStages = 12;
-    static constexpr int kTC = G == 1 ? 16 : 32 / G;
-    static constexpr int kNV = kTC * G;
-    static constexpr int kNC = kBlockTokens / kTC;
-    static constexpr int kPBuf = G * kBlockTokens + G;
+    static constexpr int kStages = 8;
+    static constexpr int kPB = 8 * kBlockTokens * 2;         // P' per warp: f16 [8 heads][16 tokens]
     static constexpr int kComb = G * (D + 2);
+    static constexpr int kQBytes = G * D * 2;                // q of one unit (bf16)
+    static constexpr int kQSlots = 2;                        // units whose q is in flight
     static constexpr int kPBufOff = kStages * kStageBytes;
-    static constexpr int kCombOff = kPBufOff + kWarps * kPBuf * 4;
-    static constexpr int kBarOff = (kCombOff + kWarps * kComb * 4 + 15) / 16 * 16;
-    static constexpr int kQueueOff = kBarOff + 2 * kStages * 8;
+    static constexpr int kCombOff = kPBufOff + kWarps * kPB;
+    static constexpr int kQOff = (kCombOff + kWarps * kComb * 4 + 15) / 16 * 16;
+    static constexpr int kMetaOff = kQOff + kQSlots * kQBytes;
+    static constexpr int kBarOff = kMetaOff + kQSlots * 16;
+    // full[kStages], empty[kStages], q_full[kQSlots], q_empty[kQSlots]
+    static constexpr int kQueueOff = kBarOff + (2 * kStages + 2 * kQSlots) * 8;
     static constexpr int kSmem = kQueueOff + int(sizeof(UnitQueue));
+    static_assert(kStageBytes % 16 == 0 && kTileBytes % 16 == 0, "bulk copy alignment");
+    // Consumer warp w takes tiles w, w + kWarps, ... of a unit and waits on a
+    // stage by parity alone.  With kStages a multiple of kWarps the previous use
+    // of that stage is the same warp's own (finished) tile; otherwise it can be
+    // another warp's tile whose copy has not landed, the parity matches the
+    // wrong phase and the wait passes early.
+    static_assert(kStages % kWarps == 0, "stage ring must be a multiple of the consumer warps");
 };
 
-template <int DPL>
-__device__ __forceinline__ void load_codes(const int8_t* p, float (&out)[DPL]) {
-    if constexpr (DPL == 4) {
-        const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) out[i] = float(int8_t(u >> (8 * i)));
-    } else {
-        const uint16_t u = *reinterpret_cast<const uint16_t*>(p);
-        out[0] = float(int8_t(u));
-        out[1] = float(int8_t(u >> 8));
-    }
+// four int8 codes -> two f16x2 registers, exactly (lo: bytes 0, 1; hi: bytes 2, 3)
+__device__ __forceinline__ void codes_to_f16x2(uint32_t u, uint32_t& lo, uint32_t& hi) {
+    const uint32_t x = u ^ 0x80808080u;                  // byte c + 128
+    const uint32_t a = __byte_perm(x, 0x64646464u, 0x4140u);   // f16 1024 + byte (two lanes)
+    const uint32_t b = __byte_perm(x, 0x64646464u, 0x4342u);
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));   // - 1152
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
 }
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 2^k for an exponent k in [-126, 127]
+__device__ __forceinline__ float exp2i(int k) { return __uint_as_float(uint32_t(127 + k) << 23); }
 
 template <int D, int G>
 __global__ void __launch_bounds__(I8Cfg<D, G>::kThreads) decode_split_int8_kernel(SplitI8Params p) {
     using C = I8Cfg<D, G>;
+    constexpr int KB = C::kKB;
     extern __shared__ __align__(128) unsigned char smem[];
-    float* pbuf_all = reinterpret_cast<float*>(smem + C::kPBufOff);
     float* comb = reinterpret_cast<float*>(smem + C::kCombOff);
+    unsigned char* qbuf = smem + C::kQOff;
+    int4* meta = reinterpret_cast<int4*>(smem + C::kMetaOff);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
     uint64_t* empty = full + C::kStages;
+    uint64_t* q_full = empty + C::kStages;
+    uint64_t* q_empty = q_full + C::kQSlots;
     UnitQueue* uq = reinterpret_cast<UnitQueue*>(smem + C::kQueueOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -175,6 +236,10 @@ __global__ void __launch_bounds__(I8Cfg<D, G>::kThreads) decode_split_int8_kerne
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < C::kQSlots; ++s) {
+            mbar_init(&q_full[s], 1);
+            mbar_init(&q_empty[s], C::kWarps);
         }
         uq_init(uq);
         fence_mbar_init();
@@ -197,6 +262,18 @@ __global__ void __launch_bounds__(I8Cfg<D, G>::kThreads) decode_split_int8_kerne
             const int ctx = p.context_lens[item.x];
             const int b0 = item.y * kSplitBlocks;
             const int nb = min(kSplitBlocks, (ctx + kBlockTokens - 1) / kBlockTokens - b0);
+            // the unit's description and q, so the consumers start without global loads
+            const int qs = k % C::kQSlots;
+            ok = __all_sync(kFullWarp,
+                            mbar_wait(&q_empty[qs], ((k / C::kQSlots) & 1) ^ 1, p.err));
+            if (!ok) break;
+            if (lane == 0) {
+                meta[qs] = make_int4(item.x, item.y, ctx, kvh);
+                mbar_arrive_expect_tx(&q_full[qs], C::kQBytes);
+                bulk_g2s(qbuf + qs * C::kQBytes, p.q + (size_t(item.x) * Hq + kvh * G) * D,
+                         C::kQBytes, &q_full[qs]);
+            }
+            __syncwarp();
             int my_blk = 0;
             if (lane < nb) my_blk = p.block_tables[size_t(item.x) * p.table_stride + b0 + lane];
             for (int j = 0; j < nb; ++j, ++it) {
@@ -230,40 +307,65 @@ __global__ void __launch_bounds__(I8Cfg<D, G>::kThreads) decode_split_int8_kerne
                 mbar_wait(&full[last % C::kStages], (last / C::kStages) & 1, p.err);
             }
         }
-        return;
+        return;   // q copies: each one completes before its unit's consumers (which wait on it) finish
     }
 
     // ---------------- consumer warps ----------------
-    constexpr int DPL = C::kDPL, TC = C::kTC, NV = C::kNV, NC = C::kNC;
-    const int my_head = G == 1 ? 0 : lane / TC;
-    const int my_tok = G == 1 ? (lane >> 1) : lane % TC;
-    float* pbuf = pbuf_all + warp * C::kPBuf;
+    // mma fragment coordinates: lane = 4 g + t
+    const int g = lane >> 2, t = lane & 3;
+    uint16_t* pb = reinterpret_cast<uint16_t*>(smem + C::kPBufOff + warp * C::kPB);
+    const int ksw = k_swizzle<D>(g);                  // rows g and g + 8 share it
     uint32_t it_base = 0;
     bool ok = true;
     for (uint32_t k = 0;; ++k) {
         const int u = uq_consume(uq, k, C::kWarps * 32, p.err, ok);
         if (u < 0) break;
-        const int2 item = p.items[u / Hkv];
-        const int seq = item.x, split = item.y;
-        const int kvh = u % Hkv;
-        const int ctx = p.context_lens[seq];
+        const int qs = k % C::kQSlots;
+        if (ok) ok = __all_sync(kFullWarp, mbar_wait(&q_full[qs], (k / C::kQSlots) & 1, p.err));
+        const int4 mt = meta[qs];
+        const int seq = mt.x, split = mt.y, ctx = mt.z, kvh = mt.w;
         const int b0 = split * kSplitBlocks;
-        const int nb = min(kSplitBlocks, (ctx + kBlockTokens - 1) / kBlockTokens - b0);
+        const int nb = ok ? min(kSplitBlocks, (ctx + kBlockTokens - 1) / kBlockTokens - b0) : 0;
 
-        float qr[G][DPL];
+        // q as the B operand of S = K q^T: head g, dims 16 kb + 4 t .. + 3 (the
+        // k index of the product is permuted the same way on the K side)
+        const __nv_bfloat16* qsm = reinterpret_cast<const __nv_bfloat16*>(qbuf + qs * C::kQBytes);
+        float qv[KB][4];
+        float amax = 0.f;
 #pragma unroll
-        for (int j = 0; j < G; ++j) {
-            float t[DPL];
-            Elem<__nv_bfloat16>::template load<DPL>(p.q + (size_t(seq) * Hq + kvh * G + j) * D + lane * DPL, t);
+        for (int kb = 0; kb < KB; ++kb) {
+            uint2 w = make_uint2(0u, 0u);
+            if (g < G) w = *reinterpret_cast<const uint2*>(qsm + g * D + 16 * kb + 4 * t);
+            qv[kb][0] = __uint_as_float(w.x << 16);
+            qv[kb][1] = __uint_as_float(w.x & 0xffff0000u);
+            qv[kb][2] = __uint_as_float(w.y << 16);
+            qv[kb][3] = __uint_as_float(w.y & 0xffff0000u);
 #pragma unroll
-            for (int d = 0; d < DPL; ++d) qr[j][d] = t[d] * p.scale_log2;
+            for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(qv[kb][i]));
         }
-        float m = -INFINITY, l = 0.f;
-        float o[G][DPL];
 #pragma unroll
-        for (int j = 0; j < G; ++j)
+        for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullWarp, amax, off));
+        // shift e: amax * 2^-e in [2^14, 2^15), exact in f16
+        const int e = max(int(__float_as_uint(amax) >> 23) - 141, -100);
+        const float down = exp2i(-e);
+        const float qf = exp2i(e) * p.scale_log2;
+        uint32_t qb[KB][2];
 #pragma unroll
-            for (int d = 0; d < DPL; ++d) o[j][d] = 0.f;
+        for (int kb = 0; kb < KB; ++kb) {
+            qb[kb][0] = pack_f16x2(qv[kb][0] * down, qv[kb][1] * down);
+            qb[kb][1] = pack_f16x2(qv[kb][2] * down, qv[kb][3] * down);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_empty[qs]);   // this warp is done with the slot
+
+        // running state: heads 2t and 2t + 1 (m, per-lane partial l), O^T fragments
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        int ev = 0;                                   // largest V-scale exponent seen (biased)
+        float o[KB][4];
+#pragma unroll
+        for (int mb = 0; mb < KB; ++mb)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[mb][i] = 0.f;
 
         for (int jb = warp; jb < nb; jb += C::kWarps) {
             const uint32_t it = it_base + jb;
@@ -271,84 +373,122 @@ __global__ void __launch_bounds__(I8Cfg<D, G>::kThreads) decode_split_int8_kerne
             if (ok) ok = __all_sync(kFullWarp, mbar_wait(&full[st], (it / C::kStages) & 1, p.err));
             if (!ok) continue;
             const unsigned char* sb = smem + size_t(st) * C::kStageBytes;
-            const int8_t* kt = reinterpret_cast<const int8_t*>(sb);
-            const int8_t* vt = kt + C::kTileBytes;
+            const unsigned char* kt = sb;
+            const unsigned char* vt = sb + C::kTileBytes;
             const float* ksc = reinterpret_cast<const float*>(sb + 2 * C::kTileBytes);
             const float* vsc = ksc + kBlockTokens;
             const int nvalid = min(kBlockTokens, ctx - (b0 + jb) * kBlockTokens);
 
-            float s[NC];
+            // S = K q^T: rows tokens g, g + 8; columns heads 2t, 2t + 1
+            float sacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < NC; ++c) {
-                float part[NV];
-#pragma unroll
-                for (int tt = 0; tt < TC; ++tt) {
-                    float kf[DPL];
-                    load_codes<DPL>(kt + (c * TC + tt) * D + lane * DPL, kf);
-#pragma unroll
-                    for (int j = 0; j < G; ++j) {
-                        float acc = qr[j][0] * kf[0];
-#pragma unroll
-                        for (int d = 1; d < DPL; ++d) acc = fmaf(qr[j][d], kf[d], acc);
-                        part[j * TC + tt] = acc;
-                    }
-                }
-                const int tok = c * TC + my_tok;
-                s[c] = reduce_scatter<NV>(part, lane) * ksc[tok];
-                if (tok >= nvalid) s[c] = -INFINITY;
+            for (int kb = 0; kb < KB; ++kb) {
+                const int off = ((kb ^ ksw) << 4) + 4 * t;
+                const uint32_t u0 = *reinterpret_cast<const uint32_t*>(kt + g * D + off);
+                const uint32_t u1 = *reinterpret_cast<const uint32_t*>(kt + (g + 8) * D + off);
+                uint32_t a0, a1, a2, a3;
+                codes_to_f16x2(u0, a0, a2);
+                codes_to_f16x2(u1, a1, a3);
+                mma_f16(sacc, a0, a1, a2, a3, qb[kb][0], qb[kb][1]);
             }
-            float mx = s[0];
+            const bool val0 = g < nvalid, val1 = g + 8 < nvalid;
+            const float kq0 = ksc[g] * qf, kq1 = ksc[g + 8] * qf;
+            const float s0 = val0 ? sacc[0] * kq0 : -INFINITY;
+            const float s1 = val0 ? sacc[1] * kq0 : -INFINITY;
+            const float s2 = val1 ? sacc[2] * kq1 : -INFINITY;
+            const float s3 = val1 ? sacc[3] * kq1 : -INFINITY;
+            float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
 #pragma unroll
-            for (int c = 1; c < NC; ++c) mx = fmaxf(mx, s[c]);
-            mx = group_max<G, TC>(mx);
-            const float m_new = fmaxf(m, mx);
-            const float alpha = exp2f(m - m_new);
-            float psum = 0.f;
-#pragma unroll
-            for (int c = 0; c < NC; ++c) {
-                const float pc = exp2f(s[c] - m_new);
-                psum += pc;
-                const int tok = c * TC + my_tok;
-                pbuf[my_head * kBlockTokens + tok] = pc * vsc[tok];   // V scale folded into p
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(kFullWarp, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(kFullWarp, mx1, off));
             }
-            psum = group_sum<G, TC>(psum);
-            l = l * alpha + psum;
-            m = m_new;
-            if (my_tok == 0) pbuf[G * kBlockTokens + my_head] = alpha;
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+            m0 = mn0;
+            m1 = mn1;
+            const float p0 = exp2f(s0 - mn0), p1 = exp2f(s1 - mn1);
+            const float p2 = exp2f(s2 - mn0), p3 = exp2f(s3 - mn1);
+            l0 = l0 * al0 + (p0 + p2);
+            l1 = l1 * al1 + (p1 + p3);
+
+            // V scales of the valid tokens; the running exponent keeps P' < 2
+            const float vs0 = val0 ? vsc[g] : 0.f, vs1 = val1 ? vsc[g + 8] : 0.f;
+            float vm = fmaxf(vs0, vs1);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) vm = fmaxf(vm, __shfl_xor_sync(kFullWarp, vm, off));
+            const int ev_new = max(ev, min(int(__float_as_uint(vm) >> 23), 253));
+            const float shift = exp2i(max(ev - ev_new, -126));
+            ev = ev_new;
+            const float fv = exp2i(127 - ev);
+            const float2 ao = make_float2(al0 * shift, al1 * shift);
+
+            // P' (f16) through shared memory into the B-operand layout [head][token]
+            pb[(2 * t) * kBlockTokens + g] = __half_as_ushort(__float2half_rn(p0 * vs0 * fv));
+            pb[(2 * t + 1) * kBlockTokens + g] = __half_as_ushort(__float2half_rn(p1 * vs0 * fv));
+            pb[(2 * t) * kBlockTokens + g + 8] = __half_as_ushort(__float2half_rn(p2 * vs1 * fv));
+            pb[(2 * t + 1) * kBlockTokens + g + 8] = __half_as_ushort(__float2half_rn(p3 * vs1 * fv));
             __syncwarp();
+            // head g, tokens 4t .. 4t + 3 (the PV product's k index, permuted as on the V side)
+            const uint2 bp = *reinterpret_cast<const uint2*>(pb + g * kBlockTokens + 4 * t);
+
+            // O^T = diag-scaled O^T + V^T P': rows dims 16 mb + g, + 8; columns heads 2t, 2t + 1
 #pragma unroll
-            for (int j = 0; j < G; ++j) {
-                const float a = pbuf[G * kBlockTokens + j];
-#pragma unroll
-                for (int d = 0; d < DPL; ++d) o[j][d] *= a;
-            }
-            for (int t = 0; t < nvalid; ++t) {
-                float vf[DPL];
-                load_codes<DPL>(vt + t * D + lane * DPL, vf);
-#pragma unroll
-                for (int j = 0; j < G; ++j) {
-                    const float pj = pbuf[j * kBlockTokens + t];
-#pragma unroll
-                    for (int d = 0; d < DPL; ++d) o[j][d] = fmaf(pj, vf[d], o[j][d]);
-                }
+            for (int mb = 0; mb < KB; ++mb) {
+                const float2 lo = __fmul2_rn(make_float2(o[mb][0], o[mb][1]), ao);
+                const float2 hi = __fmul2_rn(make_float2(o[mb][2], o[mb][3]), ao);
+                o[mb][0] = lo.x;
+                o[mb][1] = lo.y;
+                o[mb][2] = hi.x;
+                o[mb][3] = hi.y;
+                const uint32_t u0 =
+                    *reinterpret_cast<const uint32_t*>(vt + (16 * mb + g) * kBlockTokens + 4 * t);
+                const uint32_t u1 = *reinterpret_cast<const uint32_t*>(
+                    vt + (16 * mb + g + 8) * kBlockTokens + 4 * t);
+                uint32_t a0, a1, a2, a3;
+                codes_to_f16x2(u0, a0, a2);
+                codes_to_f16x2(u1, a1, a3);
+                mma_f16(o[mb], a0, a1, a2, a3, bp.x, bp.y);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
         }
         it_base += nb;
 
+        // ---- combine the consumer warps' states ----
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(kFullWarp, l0, off);
+            l1 += __shfl_xor_sync(kFullWarp, l1, off);
+        }
+        const float inv_fv = ev > 0 ? __uint_as_float(uint32_t(ev) << 23) : 0.f;   // 2^(ev - 127)
         float* rec = comb + warp * C::kComb;
+        const int h0 = 2 * t, h1 = 2 * t + 1;
 #pragma unroll
-        for (int j = 0; j < G; ++j)
-#pragma unroll
-            for (int d = 0; d < DPL; ++d) rec[j * D + lane * DPL + d] = o[j][d];
-        if (my_tok == 0) {
-            rec[G * D + my_head] = m;
-            rec[G * D + G + my_head] = l;
+        for (int mb = 0; mb < KB; ++mb) {
+            if (h0 < G) {
+                rec[h0 * D + 16 * mb + g] = o[mb][0] * inv_fv;
+                rec[h0 * D + 16 * mb + g + 8] = o[mb][2] * inv_fv;
+            }
+            if (h1 < G) {
+                rec[h1 * D + 16 * mb + g] = o[mb][1] * inv_fv;
+                rec[h1 * D + 16 * mb + g + 8] = o[mb][3] * inv_fv;
+            }
+        }
+        if (g == 0) {
+            if (h0 < G) {
+                rec[G * D + h0] = m0;
+                rec[G * D + G + h0] = l0;
+            }
+            if (h1 < G) {
+                rec[G * D + h1] = m1;
+                rec[G * D + G + h1] = l1;
+            }
         }
         consumer_sync(C::kWarps * 32);
         const int nsplit = (ctx + kSplitTokens - 1) / kSplitTokens;
-        for (int idx = threadIdx.x; idx < G * D; idx += C::kWarps * 32) {
+        // (a failed wait leaves the unit's description unknown: write nothing)
+        for (int idx = threadIdx.x; ok && idx < G * D; idx += C::kWarps * 32) {
             const int j = idx / D, d = idx % D;
             float M = -INFINITY;
 #pragma unroll
@@ -445,6 +585,7 @@ extern "C" int paged_kv_append_int8(const void* k, const void* v, const int64_t*
     int st = check_desc(&bd, false);
     if (st != PKV_OK) return st;
     if (desc->head_dim != 64 && desc->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (desc->block_size != kBlockTokens) return PKV_ERR_UNSUPPORTED;   // the tile layout is 16 rows
     if (num_tokens < 0) return PKV_ERR_INVALID;
     if (num_tokens == 0) return PKV_OK;
     if (!k || !v || !slot_mapping || !k_codes || !v_codes || !k_scales || !v_scales)

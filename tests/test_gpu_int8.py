@@ -19,6 +19,23 @@ def _bf16_tensor(bits):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
 
 
+def _logical_codes(k_phys, v_phys):
+    """Device tile layout -> logical [NB, Hkv, 16, D] (the layout the header
+    defines: K rows with 16-byte chunks XOR-swizzled by the row, V dim-major)."""
+    k = k_phys.cpu().numpy()
+    v = v_phys.cpu().numpy()
+    nb, hkv, bs, d = k.shape
+    r = np.arange(bs)
+    sw = (r & 7) if d == 128 else ((r >> 1) & 3)
+    chunks = k.reshape(nb, hkv, bs, d // 16, 16)
+    kl = np.empty_like(chunks)
+    for row in range(bs):
+        for c in range(d // 16):
+            kl[:, :, row, c] = chunks[:, :, row, c ^ sw[row]]
+    vl = np.ascontiguousarray(np.swapaxes(v.reshape(nb, hkv, d, bs), 2, 3))
+    return kl.reshape(nb, hkv, bs, d), vl
+
+
 def _pool_rows(c):
     """[NB, Hkv, bs, D] -> rows [NB * bs, Hkv, D] (row index = slot)."""
     nb, hkv, bs, d = c.shape
@@ -63,8 +80,9 @@ def test_int8_append_bit_exact_and_decode(lib, hq, hkv, d):
     ic, (kq, ks, vq, vs) = _fill(lib, w, ost, hq * 7 + d)
     torch.cuda.synchronize()
     assert lib.device_error() == 0
-    assert np.array_equal(ic.k_codes.cpu().numpy(), kq)
-    assert np.array_equal(ic.v_codes.cpu().numpy(), vq)
+    kl, vl = _logical_codes(ic.k_codes, ic.v_codes)
+    assert np.array_equal(kl, kq)
+    assert np.array_equal(vl, vq)
     assert np.array_equal(ic.k_scales.cpu().numpy().view(np.uint32), ks.view(np.uint32))
     assert np.array_equal(ic.v_scales.cpu().numpy().view(np.uint32), vs.view(np.uint32))
     bt, ctx, _ = ost.batch_metadata()
@@ -107,8 +125,9 @@ def test_int8_extremes_and_zero_rows(lib):
     ks = np.zeros((2, hkv, 16), np.float32)
     vs = np.zeros_like(ks)
     quant.append_int8(kq, ks, vq, vs, bits, np.ascontiguousarray(bits[::-1]), slots, 16, "bf16")
-    assert np.array_equal(ic.k_codes.cpu().numpy(), kq)
-    assert np.array_equal(ic.v_codes.cpu().numpy(), vq)
+    kl, vl = _logical_codes(ic.k_codes, ic.v_codes)
+    assert np.array_equal(kl, kq)
+    assert np.array_equal(vl, vq)
     assert np.array_equal(ic.k_scales.cpu().numpy().view(np.uint32), ks.view(np.uint32))
     assert np.array_equal(ic.v_scales.cpu().numpy().view(np.uint32), vs.view(np.uint32))
     assert ks[0, 0, 3] == 0 and np.all(kq[0, :, 3] == 0)
