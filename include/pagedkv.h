@@ -109,7 +109,53 @@ typedef struct pkv_pool pkv_pool;
 PKV_API int pkv_pool_create(int32_t num_blocks, int32_t block_size, int32_t watermark_blocks,
                     const int32_t* free_order, pkv_pool** out);
 PKV_API int pkv_pool_destroy(pkv_pool* pool);
+
+/* Pool variants [Deploy §2.1 BlockSpaceManager(sliding_window, enable_caching);
+ * the pages refuse the two together, and so does this call with
+ * PKV_ERR_UNSUPPORTED].
+ *
+ * PKV_POOL_PREFIX_CACHING [Deploy §2.1 CachedBlockAllocator, LRUEvictor]:
+ *   - Full blocks are shared by a hash of the whole token prefix.  The hash
+ *     of logical block j is FNV-1a 64 over the previous block's hash (0 for
+ *     block 0; 8 bytes little-endian) followed by the block's token ids
+ *     (4 bytes little-endian each).  A block holding that hash, in use or
+ *     parked, is reused (reference count + 1); the partial last block of a
+ *     prompt is never shared.
+ *   - A hashed block whose last reference goes away is parked in the evictor,
+ *     not freed.
+ *   - New blocks come from the free list, else from the evictor: least
+ *     recently accessed first, then the one whose hash covers the most tokens,
+ *     then the one parked first.
+ *   - Access times come from pkv_pool_set_clock.
+ *   - Sequences are added with pkv_seq_add_tokens and grown with
+ *     pkv_seq_append_token; the count-only calls return PKV_ERR_UNSUPPORTED.
+ *   - When a token fills its block, the block's hash is looked up: if it is
+ *     found, the sequence switches to that block (the filled block is freed
+ *     and any copy pair of that call is cancelled); otherwise the block is
+ *     registered under the hash.
+ *   - Free counts and admission include parked blocks.
+ *
+ * sliding_window > 0 (a multiple of block_size; W_b = window / block_size)
+ * [Deploy §2.1 block_sliding_window]:
+ *   - A table is a ring of W_b blocks: logical block j >= W_b reuses entry
+ *     j % W_b.  Admission counts min(blocks, W_b).
+ *   - A prompt token whose slot a later token of the same prompt takes gets
+ *     slot -1 (skip it when appending).
+ *   - A shared ring block is copied before it is written.
+ *   - pkv_block_tables exports the ring entries of the last W_b logical
+ *     blocks in logical order, with context min(len, window): exactly the
+ *     last `window` tokens, for decode.
+ * flags = 0 and sliding_window = 0 is pkv_pool_create. */
+#define PKV_POOL_PREFIX_CACHING 1
+PKV_API int pkv_pool_create_ex(int32_t num_blocks, int32_t block_size, int32_t watermark_blocks,
+                               const int32_t* free_order, int32_t flags, int32_t sliding_window,
+                               pkv_pool** out);
+/* Free blocks, parked (evictable) blocks included. */
 PKV_API int pkv_pool_num_free(const pkv_pool* pool, int32_t* out);
+/* Parked blocks of a prefix-caching pool (0 otherwise). */
+PKV_API int pkv_pool_num_evictable(const pkv_pool* pool, int32_t* out);
+/* The access clock stamped on blocks handed out or parked from now on. */
+PKV_API int pkv_pool_set_clock(pkv_pool* pool, int64_t now);
 
 /* Admission of a new sequence of `num_tokens` tokens [Deploy §2.1 can_allocate]:
  * PKV_ERR_NEVER if num_blocks - need < watermark, PKV_OK if
@@ -122,6 +168,15 @@ PKV_API int pkv_pool_can_allocate(const pkv_pool* pool, int32_t num_tokens);
  * slot block * block_size + row of every token in order.  On any error the
  * pool is unchanged. */
 PKV_API int pkv_seq_add(pkv_pool* pool, int64_t seq_id, int32_t num_tokens, int64_t* slots_out);
+
+/* Add a sequence from its token ids (host, [num_tokens]).  Prefix caching:
+ * full blocks are shared as described at pkv_pool_create_ex and
+ * *num_cached_tokens_out (optional) = block_size * the number of leading
+ * blocks that were found, whose K/V the caller need not write again.  Other
+ * pools: as pkv_seq_add, with *num_cached_tokens_out = 0. */
+PKV_API int pkv_seq_add_tokens(pkv_pool* pool, int64_t seq_id, const int32_t* token_ids,
+                               int32_t num_tokens, int64_t* slots_out,
+                               int32_t* num_cached_tokens_out);
 
 /* New sequence `child` shares every block of `parent` (reference count + 1 each). */
 PKV_API int pkv_seq_fork(pkv_pool* pool, int64_t parent, int64_t child);
@@ -136,12 +191,22 @@ PKV_API int pkv_seq_fork(pkv_pool* pool, int64_t parent, int64_t child);
 PKV_API int pkv_seq_append_slot(pkv_pool* pool, int64_t seq_id, int64_t* slot_out,
                         int32_t* cow_src, int32_t* cow_dst);
 
+/* pkv_seq_append_slot for a token whose id is known; a prefix-caching pool
+ * needs it to hash the block the token fills (see pkv_pool_create_ex). */
+PKV_API int pkv_seq_append_token(pkv_pool* pool, int64_t seq_id, int32_t token_id,
+                                 int64_t* slot_out, int32_t* cow_src, int32_t* cow_dst);
+
 /* Drop one reference on each block of the sequence (table order); blocks that
- * reach zero return to the free list. */
+ * reach zero return to the free list (hashed blocks of a prefix-caching pool:
+ * to the evictor). */
 PKV_API int pkv_seq_free(pkv_pool* pool, int64_t seq_id);
 
 PKV_API int pkv_seq_len(const pkv_pool* pool, int64_t seq_id, int32_t* len_out);
 PKV_API int pkv_block_ref_count(const pkv_pool* pool, int32_t block, int32_t* out);
+/* The hash a prefix-caching pool has registered for `block`: *hashed_out = 1
+ * and *hash_out = the hash, or 0 and 0. */
+PKV_API int pkv_block_hash(const pkv_pool* pool, int32_t block, uint64_t* hash_out,
+                           int32_t* hashed_out);
 
 /* Export block tables and context lengths of `n` sequences (host buffers):
  * tables_out [n][max_blocks] padded with -1, ctx_lens_out [n] (optional).
@@ -313,6 +378,15 @@ PKV_API int paged_kv_append_int8(const void* k, const void* v, const int64_t* sl
                                  int32_t num_tokens, void* k_codes, void* v_codes,
                                  float* k_scales, float* v_scales, const pkv_cache_desc* desc,
                                  void* stream);
+
+/* Copy-on-write for an 8-bit cache: for each (src, dst) pair, the codes and
+ * scales of block src (every kv head) are copied to block dst, as
+ * pkv_copy_blocks does for the other caches.  block_pairs: device int32
+ * [num_pairs][2]; an id outside [0, num_blocks) sets PKV_DEV_BAD_COPY_PAIR and
+ * that pair is skipped. */
+PKV_API int pkv_copy_blocks_int8(const int32_t* block_pairs, int32_t num_pairs, void* k_codes,
+                                 void* v_codes, float* k_scales, float* v_scales,
+                                 const pkv_cache_desc* desc, void* stream);
 
 /* Decode attention over the 8-bit cache: exactly the attention of
  * paged_attention_decode over the dequantised keys and values (code * scale),

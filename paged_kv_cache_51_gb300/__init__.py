@@ -45,8 +45,12 @@ EXPORTS = (
     "pkv_decode_workspace_bytes", "paged_attention_decode", "paged_attention_decode_noalloc",
     "pkv_varlen_workspace_bytes",
     "paged_attention_varlen", "pkv_device_error", "pkv_status_string", "pkv_splitfuse_compose",
-    "paged_kv_append_int8", "paged_attention_decode_int8",
+    "paged_kv_append_int8", "paged_attention_decode_int8", "pkv_copy_blocks_int8",
+    "pkv_pool_create_ex", "pkv_pool_num_evictable", "pkv_pool_set_clock", "pkv_seq_add_tokens",
+    "pkv_seq_append_token", "pkv_block_hash",
 )
+
+PKV_POOL_PREFIX_CACHING = 1
 
 
 class PagedKVError(RuntimeError):
@@ -76,6 +80,12 @@ def lib():
     P = ctypes.POINTER
     sig = {
         "pkv_pool_create": (ctypes.c_int, [i32, i32, i32, p, P(p)]),
+        "pkv_pool_create_ex": (ctypes.c_int, [i32, i32, i32, p, i32, i32, P(p)]),
+        "pkv_pool_num_evictable": (ctypes.c_int, [p, P(i32)]),
+        "pkv_pool_set_clock": (ctypes.c_int, [p, i64]),
+        "pkv_seq_add_tokens": (ctypes.c_int, [p, i64, p, i32, p, P(i32)]),
+        "pkv_seq_append_token": (ctypes.c_int, [p, i64, i32, P(i64), P(i32), P(i32)]),
+        "pkv_block_hash": (ctypes.c_int, [p, i32, P(ctypes.c_uint64), P(i32)]),
         "pkv_pool_destroy": (ctypes.c_int, [p]),
         "pkv_pool_num_free": (ctypes.c_int, [p, P(i32)]),
         "pkv_pool_can_allocate": (ctypes.c_int, [p, i32]),
@@ -102,6 +112,7 @@ def lib():
         "pkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "pkv_splitfuse_compose": (ctypes.c_int, [i32, i32, i32, p, p, P(i32), P(i32)]),
         "paged_kv_append_int8": (ctypes.c_int, [p, p, p, i32, p, p, p, p, P(CacheDesc), p]),
+        "pkv_copy_blocks_int8": (ctypes.c_int, [p, i32, p, p, p, p, P(CacheDesc), p]),
         "paged_attention_decode_int8": (ctypes.c_int, [p, p, p, p, p, p, P(CacheDesc), p, i32, p,
                                                        i32, i32, ctypes.c_float, p, sz, p]),
     }
@@ -131,15 +142,20 @@ def _check(status, what):
 class BlockPool:
     """Host block pool (C++): ref-counted blocks, block tables, copy-on-write."""
 
-    def __init__(self, num_blocks, block_size, watermark_blocks=0, free_order=None):
+    def __init__(self, num_blocks, block_size, watermark_blocks=0, free_order=None,
+                 prefix_caching=False, sliding_window=0):
         self._h = ctypes.c_void_p()
         arr = None
         if free_order is not None:
             arr = (ctypes.c_int32 * num_blocks)(*[int(b) for b in free_order])
-        _check(lib().pkv_pool_create(num_blocks, block_size, watermark_blocks, arr,
-                                     ctypes.byref(self._h)), "pkv_pool_create")
+        flags = PKV_POOL_PREFIX_CACHING if prefix_caching else 0
+        _check(lib().pkv_pool_create_ex(num_blocks, block_size, watermark_blocks, arr, flags,
+                                        sliding_window, ctypes.byref(self._h)),
+               "pkv_pool_create_ex")
         self.num_blocks = num_blocks
         self.block_size = block_size
+        self.prefix_caching = prefix_caching
+        self.sliding_window = sliding_window
 
     def close(self):
         if self._h:
@@ -171,6 +187,37 @@ class BlockPool:
         slots = (ctypes.c_int64 * max(num_tokens, 1))()
         st = lib().pkv_seq_add(self._h, seq_id, num_tokens, slots)
         return st, (list(slots)[:num_tokens] if st == PKV_OK else None)
+
+    def add_tokens(self, seq_id, token_ids):
+        """Returns (status, slots or None, num_cached_tokens)."""
+        n = len(token_ids)
+        toks = (ctypes.c_int32 * max(n, 1))(*[int(t) for t in token_ids])
+        slots = (ctypes.c_int64 * max(n, 1))()
+        cached = ctypes.c_int32()
+        st = lib().pkv_seq_add_tokens(self._h, seq_id, toks, n, slots, ctypes.byref(cached))
+        return st, (list(slots)[:n] if st == PKV_OK else None), cached.value
+
+    def append_token(self, seq_id, token_id):
+        """Returns (status, slot, cow) with cow = (src, dst) or None."""
+        slot, src, dst = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+        st = lib().pkv_seq_append_token(self._h, seq_id, int(token_id), ctypes.byref(slot),
+                                        ctypes.byref(src), ctypes.byref(dst))
+        return st, slot.value, ((src.value, dst.value) if st == PKV_OK and src.value >= 0 else None)
+
+    def set_clock(self, now):
+        _check(lib().pkv_pool_set_clock(self._h, int(now)), "pkv_pool_set_clock")
+
+    def num_evictable(self):
+        out = ctypes.c_int32()
+        _check(lib().pkv_pool_num_evictable(self._h, ctypes.byref(out)), "pkv_pool_num_evictable")
+        return out.value
+
+    def block_hash(self, block):
+        """The registered hash of a block, or None."""
+        h, reg = ctypes.c_uint64(), ctypes.c_int32()
+        _check(lib().pkv_block_hash(self._h, block, ctypes.byref(h), ctypes.byref(reg)),
+               "pkv_block_hash")
+        return h.value if reg.value else None
 
     def fork(self, parent, child):
         _check(lib().pkv_seq_fork(self._h, parent, child), "pkv_seq_fork")
@@ -426,6 +473,19 @@ def paged_kv_append_int8(k, v, slot_mapping, cache, stream=None):
                                       _ptr(cache.k_scales), _ptr(cache.v_scales),
                                       ctypes.byref(cache.desc), _stream(stream)),
            "paged_kv_append_int8")
+
+
+def pkv_copy_blocks_int8(block_pairs, cache, stream=None):
+    """Copy-on-write for the 8-bit cache; block_pairs: CUDA int32 [n, 2] (src, dst)."""
+    n = block_pairs.shape[0] if block_pairs is not None else 0
+    if n == 0:
+        return
+    _need(block_pairs, torch.int32, "block_pairs")
+    _need_int8_cache(cache)
+    _check(lib().pkv_copy_blocks_int8(_ptr(block_pairs), n, _ptr(cache.k_codes),
+                                      _ptr(cache.v_codes), _ptr(cache.k_scales),
+                                      _ptr(cache.v_scales), ctypes.byref(cache.desc),
+                                      _stream(stream)), "pkv_copy_blocks_int8")
 
 
 def paged_attention_decode_int8(out, q, cache, block_tables, context_lens, max_context_len,

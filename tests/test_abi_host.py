@@ -205,3 +205,9 @@ def test_int8_entry_points_validate_on_the_host(lib):
                                          fake, 1, 16, float("nan"), fake, 1 << 20,
                                          None) == lib.PKV_ERR_INVALID
     assert L.paged_kv_append_int8(None, None, None, 0, None, None, None, None, ref(i8), None) == 0
+    # copy-on-write for the 8-bit cache takes only PKV_INT8
+    assert L.pkv_copy_blocks_int8(fake, 2, fake, fake, fake, fake, ref(bf), None) == \
+        lib.PKV_ERR_UNSUPPORTED
+    assert L.pkv_copy_blocks_int8(None, 2, fake, fake, fake, fake, ref(i8), None) == \
+        lib.PKV_ERR_INVALID
+    assert L.pkv_copy_blocks_int8(None, 0, None, None, None, None, ref(i8), None) == 0

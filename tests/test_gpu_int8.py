@@ -142,3 +142,35 @@ def test_int8_bad_slot_is_flagged(lib):
     lib.paged_kv_append_int8(k, k, torch.tensor([1, 32], dtype=torch.int64, device="cuda"), ic)
     assert lib.device_error() == 3                                  # PKV_DEV_BAD_SLOT
     assert int(torch.count_nonzero(ic.k_codes)) == 2 * 64           # slot 1 written, 32 skipped
+
+
+def test_int8_copy_on_write_moves_codes_and_scales(lib):
+    """Block copies through pkv_copy_blocks_int8 equal the oracle's whole-block copy."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from oracle import cache as ocache
+
+    hkv, d, nb = 4, 128, 12
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((nb * 16, hkv, d)).astype(np.float32)
+    bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    ic = lib.Int8Cache(nb, hkv, 16, d, hkv * 2)
+    slots = np.arange(nb * 16, dtype=np.int64)
+    lib.paged_kv_append_int8(_bf16_tensor(bits).cuda(), _bf16_tensor(bits[::-1].copy()).cuda(),
+                             torch.from_numpy(slots).cuda(), ic)
+    kq = np.zeros((nb, hkv, 16, d), np.int8)
+    vq = np.zeros_like(kq)
+    ks = np.zeros((nb, hkv, 16), np.float32)
+    vs = np.zeros_like(ks)
+    quant.append_int8(kq, ks, vq, vs, bits, bits[::-1].copy(), slots, 16, "bf16")
+    pairs = [(3, 7), (0, 11), (5, 2)]
+    ocache.copy_blocks(kq, vq, pairs)
+    ocache.copy_blocks(ks[..., None], vs[..., None], pairs)
+    lib.device_error(clear=True)
+    lib.pkv_copy_blocks_int8(torch.tensor(pairs, dtype=torch.int32, device="cuda"), ic)
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0
+    kl, vl = _logical_codes(ic.k_codes, ic.v_codes)
+    assert np.array_equal(kl, kq) and np.array_equal(vl, vq)
+    assert np.array_equal(ic.k_scales.cpu().numpy(), ks)
+    assert np.array_equal(ic.v_scales.cpu().numpy(), vs)

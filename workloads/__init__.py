@@ -302,3 +302,23 @@ def serving_trace(seed=0, n_requests=6, prompt_range=(20, 700), gen_range=(1, 6)
     q_rows = _values(rng, (row, hq, d), "bf16", scale)
     return ServingTrace("bf16", hq, hkv, d, bs, nb, free_order, prompt, gen, arrival, offs,
                         k_rows, v_rows, q_rows)
+
+
+class TokenValues:
+    """K/V rows that depend only on (token id, position), as a model's K/V depend
+    on the token prefix: row(t, p) = bf16(E[t] + P[p]) with E, P seeded normal
+    tables.  Sequences that share a token prefix get bit-identical rows there,
+    which is what lets cached blocks be shared."""
+
+    def __init__(self, seed, vocab, max_pos, hkv, d, scale=0.5):
+        rng = np.random.default_rng(seed)
+        self.ek = rng.standard_normal((vocab, hkv, d), dtype=np.float32) * np.float32(scale)
+        self.ev = rng.standard_normal((vocab, hkv, d), dtype=np.float32) * np.float32(scale)
+        self.pk = rng.standard_normal((max_pos, hkv, d), dtype=np.float32) * np.float32(scale)
+        self.pv = rng.standard_normal((max_pos, hkv, d), dtype=np.float32) * np.float32(scale)
+
+    def rows(self, token_ids, positions):
+        """(k, v) bf16 bit patterns [len, hkv, d] for the given tokens at the given positions."""
+        t = np.asarray(token_ids, dtype=np.int64)
+        p = np.asarray(positions, dtype=np.int64)
+        return _bf16_bits(self.ek[t] + self.pk[p]), _bf16_bits(self.ev[t] + self.pv[p])
