@@ -61,8 +61,13 @@ struct MmaCfg {
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kComb = G * (D + 2);
     static constexpr int kCombOff = kRingBytes;
-    static constexpr int kBarOff = kCombOff + kWarps * kComb * 4;
-    static constexpr int kQueueOff = kBarOff + 2 * kStages * 8;
+    static constexpr int kQBytes = G * D * 2;               // q of one unit (bf16)
+    static constexpr int kQSlots = 2;                       // units whose q is in flight
+    static constexpr int kQOff = kCombOff + kWarps * kComb * 4;
+    static constexpr int kMetaOff = kQOff + kQSlots * kQBytes;
+    static constexpr int kBarOff = kMetaOff + kQSlots * 32;
+    // full[kStages], empty[kStages], q_full[kQSlots], q_empty[kQSlots]
+    static constexpr int kQueueOff = kBarOff + (2 * kStages + 2 * kQSlots) * 8;
     static constexpr int kSmem = kQueueOff + int(sizeof(UnitQueue)) + 1024;  // + alignment slack
     static_assert(G == 2 || G == 4 || G == 8, "group size");
     // a consumer warp waits on a stage by parity: its previous use must be the
@@ -122,8 +127,12 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads)
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char* smem = smem_raw + (base - raw);
     float* comb = reinterpret_cast<float*>(smem + C::kCombOff);
+    unsigned char* qbuf = smem + C::kQOff;
+    int4* meta = reinterpret_cast<int4*>(smem + C::kMetaOff);   // [slot][2]
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
     uint64_t* empty = full + C::kStages;
+    uint64_t* q_full = empty + C::kStages;
+    uint64_t* q_empty = q_full + C::kQSlots;
     UnitQueue* uq = reinterpret_cast<UnitQueue*>(smem + C::kQueueOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -131,6 +140,10 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads)
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < C::kQSlots; ++s) {
+            mbar_init(&q_full[s], 1);
+            mbar_init(&q_empty[s], C::kWarps);
         }
         uq_init(uq);
         fence_mbar_init();
@@ -156,6 +169,19 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads)
             const int nb = min(kSplitBlocks, (ctx + kBlockTokens - 1) / kBlockTokens - b0);
             int my_blk = 0;
             if (lane < nb) my_blk = p.block_tables[size_t(item.x) * p.table_stride + b0 + lane];
+            // the unit's description and q, so the consumers start without global loads
+            const int qs = k % C::kQSlots;
+            ok = __all_sync(kFullMask, mbar_wait(&q_empty[qs], ((k / C::kQSlots) & 1) ^ 1, p.err));
+            if (!ok) break;
+            if (lane == 0) {
+                const int qrow = p.query_start_loc ? p.query_start_loc[item.x] : item.x;
+                meta[2 * qs] = make_int4(item.x, item.y, ctx, kvh);
+                meta[2 * qs + 1] = make_int4(qrow, 0, 0, 0);
+                mbar_arrive_expect_tx(&q_full[qs], C::kQBytes);
+                bulk_g2s(qbuf + qs * C::kQBytes, p.q + (size_t(qrow) * Hq + kvh * G) * D, C::kQBytes,
+                         &q_full[qs]);
+            }
+            __syncwarp();
             for (int j = 0; j < nb; ++j, ++it) {
                 const int blk = __shfl_sync(kFullMask, my_blk, j);
                 const int st = it % C::kStages;
@@ -196,25 +222,27 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads)
     for (uint32_t k = 0;; ++k) {
         const int u = uq_consume(uq, k, C::kWarps * 32, p.err, ok);
         if (u < 0) break;
-        const int2 item = p.items[u / Hkv];
-        const int seq = item.x, split = item.y;
-        const int kvh = u % Hkv;
-        const int ctx = p.context_lens[seq];
+        const int qs = k % C::kQSlots;
+        if (ok) ok = __all_sync(kFullMask, mbar_wait(&q_full[qs], (k / C::kQSlots) & 1, p.err));
+        const int4 mt = meta[2 * qs];
+        const int seq = mt.x, split = mt.y, ctx = mt.z, kvh = mt.w;
+        const int qrow = meta[2 * qs + 1].x;
         const int b0 = split * kSplitBlocks;
-        const int nb = min(kSplitBlocks, (ctx + kBlockTokens - 1) / kBlockTokens - b0);
-        const int qrow = p.query_start_loc ? p.query_start_loc[seq] : seq;
+        const int nb = ok ? min(kSplitBlocks, (ctx + kBlockTokens - 1) / kBlockTokens - b0) : 0;
 
         // q fragments (A operand): row gid = query head gid of the group, rows >= G zero
         uint32_t qa0[D / 16], qa2[D / 16];
         {
-            const uint32_t* qh = reinterpret_cast<const uint32_t*>(
-                p.q + (size_t(qrow) * Hq + kvh * G + (gid < G ? gid : 0)) * D);
+            const uint32_t* qh = reinterpret_cast<const uint32_t*>(qbuf + qs * C::kQBytes) +
+                                 (gid < G ? gid : 0) * (D / 2);
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
-                qa0[ks] = gid < G ? __ldg(qh + ks * 8 + tig) : 0u;
-                qa2[ks] = gid < G ? __ldg(qh + ks * 8 + 4 + tig) : 0u;
+                qa0[ks] = gid < G ? qh[ks * 8 + tig] : 0u;
+                qa2[ks] = gid < G ? qh[ks * 8 + 4 + tig] : 0u;
             }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_empty[qs]);   // this warp is done with the slot
         float o[D / 8][4];
 #pragma unroll
         for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -317,7 +345,8 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads)
         }
         asm volatile("bar.sync 1, %0;" ::"r"(C::kWarps * 32) : "memory");
         const int nsplit = (ctx + kSplitTokens - 1) / kSplitTokens;
-        for (int idx = threadIdx.x; idx < G * D; idx += C::kWarps * 32) {
+        // (a failed wait leaves the unit's description unknown: write nothing)
+        for (int idx = threadIdx.x; ok && idx < G * D; idx += C::kWarps * 32) {
             const int j = idx / D, d = idx % D;
             float M = -INFINITY;
 #pragma unroll

@@ -26,10 +26,12 @@
 //              own O accumulator in TMEM (O = O_0 + O_1 after rescaling, like a
 //              split over keys), so the two never exchange data inside the
 //              loop.  A thread reads its 64 scores from TMEM, masks, computes P
-//              (bf16) while the previous P V product is still running, writes
-//              P to shared memory, and rescales its O half only when its
-//              running max grows by more than 2^8.  The epilogue merges the
-//              halves.
+//              (bf16) and writes it back into TMEM over its own scores; the
+//              P V product reads P from there.  S is double-buffered, so P is
+//              too: the softmax of the next key tile runs while the previous
+//              P V product is still executing.  O is rescaled only when the
+//              running max grows by more than 2^8 (the one case that waits for
+//              the previous P V).  The epilogue merges the halves.
 //   warp 8     TMA producer for K: blocks of each key tile into a 2-stage K ring;
 //              a K stage is released as soon as its Q K^T product is done
 //   warp 9     TMA producer for V: a 2-stage V ring released by the P V product
@@ -55,8 +57,7 @@ constexpr int kBlkPerTile = kKeys / kBlockTokens;  // 8 cache blocks
 constexpr int kStages = 2;
 constexpr int kSub = kRows * 128;            // one 64-column half of a 128-row operand (16 KiB)
 constexpr int kQOff = 0;                     // Q: 2 halves (dims 0-63, 64-127)
-constexpr int kPOff = 2 * kSub;              // P: 2 halves (keys 0-63, 64-127)
-constexpr int kKVOff = 4 * kSub;             // stages
+constexpr int kKVOff = 2 * kSub;             // stages
 constexpr int kKBytes = 2 * kKeys * 128;     // K of one stage (2 halves of 128 key rows x 128 B)
 constexpr int kStageBytes = 2 * kKBytes;     // K stage s at s * kStageBytes, V stage s after it
 constexpr int kStatOff = kKVOff + kStages * kStageBytes;  // (m, l) per half and row, 2 sets
@@ -67,7 +68,7 @@ constexpr int kKProducerWarp = 8;
 constexpr int kVProducerWarp = 9;
 constexpr int kMmaWarp = 10;
 constexpr int kThreads = 352;
-constexpr uint32_t kTmemCols = 512;          // S double buffer (2 x 128) + O halves (2 x 128)
+constexpr uint32_t kTmemCols = 512;          // S/P double buffer (2 x 128) + O halves (2 x 128)
 constexpr uint32_t kOCol = 256;              // O half h at kOCol + 128 h
 constexpr float kRescaleThreshold = 8.0f;    // log2 units: rescale O only when max grows > 2^8
 constexpr int kBoxBytes = kBlockTokens * 128;  // one TMA box: 16 rows x 64 bf16
@@ -79,10 +80,9 @@ enum {
     B_V_FULL = B_K_EMPTY + kStages,
     B_V_EMPTY = B_V_FULL + kStages,
     B_S_FULL = B_V_EMPTY + kStages,
-    B_S_EMPTY = B_S_FULL + 2,
-    B_P_FULL = B_S_EMPTY + 2,       // per key half
-    B_O_DONE = B_P_FULL + 2,        // per key half
-    B_Q_FULL = B_O_DONE + 2,
+    B_P_FULL = B_S_FULL + 2,        // [key half][S/P buffer]
+    B_O_DONE = B_P_FULL + 4,        // [key half][S/P buffer]: that buffer's P V has completed
+    B_Q_FULL = B_O_DONE + 4,
     B_O_EMPTY,
     B_STAT,                         // both halves' (m, l) of the current unit are published
     B_DRAIN,
@@ -128,6 +128,16 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, ui
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// A operand from tensor memory (rows in lanes, K packed two bf16 per column)
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -266,9 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars[B_V_FULL + s], 1);
             mbar_init(&bars[B_V_EMPTY + s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars[B_S_FULL + s], 1);
-            mbar_init(&bars[B_S_EMPTY + s], kSoftWarps);
+        for (int s = 0; s < 2; ++s) mbar_init(&bars[B_S_FULL + s], 1);
+        for (int s = 0; s < 4; ++s) {
             mbar_init(&bars[B_P_FULL + s], kSoftWarps / 2);
             mbar_init(&bars[B_O_DONE + s], 1);
         }
@@ -344,23 +353,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t kt = 0, it = 0;
             bool ok = true;
-            const uint32_t q_addr = base + kQOff, p_addr = base + kPOff;
-            // O_h += P_h V_h over the 64 keys of half h, for both halves
+            const uint32_t q_addr = base + kQOff;
+            // O_h += P_h V_h over the 64 keys of half h, for both halves; P_h is
+            // bf16 in TMEM over the first 32 columns of its scores
             auto pv = [&](uint32_t g, int j) -> bool {
                 const uint32_t vs = base + kKVOff + (g % kStages) * kStageBytes + kKBytes;
+                const uint32_t b = g & 1;
                 if (!mbar_wait(&bars[B_V_FULL + g % kStages], (g / kStages) & 1, p.err)) return false;
                 for (int h = 0; h < 2; ++h) {
-                    if (!mbar_wait(&bars[B_P_FULL + h], g & 1, p.err)) return false;
+                    if (!mbar_wait(&bars[B_P_FULL + 2 * h + b], (g >> 1) & 1, p.err)) return false;
                     if (j == 0 && h == 0 && !mbar_wait(&bars[B_O_EMPTY], (it & 1) ^ 1, p.err))
                         return false;
                     tc_after();
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t a = sdesc(p_addr + h * kSub + kk * 32, 16, 1024);
-                        const uint64_t b = sdesc(vs + (h * 4 + kk) * 16 * 128, kKeys * 128, 1024);
-                        umma(tmem + kOCol + h * 128, a, b, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                        const uint32_t a = tmem + b * kKeys + h * 64 + kk * 8;
+                        const uint64_t bd = sdesc(vs + (h * 4 + kk) * 16 * 128, kKeys * 128, 1024);
+                        umma_ts(tmem + kOCol + h * 128, a, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
                     }
-                    umma_commit(&bars[B_O_DONE + h]);
+                    umma_commit(&bars[B_O_DONE + 2 * h + b]);
                 }
                 umma_commit(&bars[B_V_EMPTY + g % kStages]);
                 return true;
@@ -372,8 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_after();
                 for (int j = 0; j < x.n_tiles && ok; ++j) {
                     const uint32_t g = kt + j;
+                    // S/P buffer g & 1 last held P(g - 2), whose P V was issued before
+                    // this product: tensor-core instructions run in issue order
                     ok = mbar_wait(&bars[B_K_FULL + g % kStages], (g / kStages) & 1, p.err) &&
-                         mbar_wait(&bars[B_S_EMPTY + (g & 1)], ((g >> 1) & 1) ^ 1, p.err) &&
                          !*abort_flag;
                     if (!ok) break;
                     tc_after();
@@ -448,10 +460,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         s[32 + i] = __uint_as_float(v1[i]);
                     }
                 }
-                tc_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[B_S_EMPTY + (g & 1)]);
-
                 // mask keys beyond this row's causal limit; max on the raw scores
                 const int key0 = j * kKeys + h * 64;
                 float mx = -INFINITY;
@@ -481,31 +489,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 l += rowsum;
                 const bool warp_need = __any_sync(0xffffffffu, need);
-                if (j > 0) {
-                    // the previous PV of this half is done: P half free, O half current
-                    ok = __all_sync(0xffffffffu,
-                                    mbar_wait(&bars[B_O_DONE + h], (g - 1) & 1, p.err));
+                if (j > 0 && warp_need) {
+                    // rescale O_h: wait for the previous P V of this half (buffer
+                    // (g - 1) & 1; that buffer's older products have completed,
+                    // since S(g) is full and was issued after them)
+                    const uint32_t gp = g - 1;
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE + 2 * h + (gp & 1)],
+                                                           (gp >> 1) & 1, p.err));
                     if (!ok) break;
                     tc_after();
-                    if (warp_need) {
 #pragma unroll 1
-                        for (int c4 = 0; c4 < 4; ++c4) {
-                            uint32_t v[32];
-                            const uint32_t ta = tmem + lane_base + kOCol + h * 128 + c4 * 32;
-                            tmem_ld32(ta, v);
-                            tmem_wait_ld();
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        uint32_t v[32];
+                        const uint32_t ta = tmem + lane_base + kOCol + h * 128 + c4 * 32;
+                        tmem_ld32(ta, v);
+                        tmem_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-                            tmem_st32(ta, v);
-                        }
-                        tmem_wait_st();
+                        for (int i = 0; i < 32; ++i)
+                            v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                        tmem_st32(ta, v);
                     }
                 }
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8)
-                    *reinterpret_cast<uint4*>(smem + kPOff + h * kSub + swz(r, c8)) =
-                        make_uint4(w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
+                // P (bf16 pairs) over the first 32 columns of this half's scores
+                tmem_st32(tmem + lane_base + (g & 1) * kKeys + h * 64, w);
                 // rows of the last staged block that lie beyond the context were
                 // never written: zero their V so 0 * (anything) cannot become NaN.
                 // The half whose keys hold that block does it before its P V.
@@ -527,15 +533,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 fence_async_smem();
+                tmem_wait_st();
                 tc_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[B_P_FULL + h]);
+                if (lane == 0) mbar_arrive(&bars[B_P_FULL + 2 * h + (g & 1)]);
             }
             if (!ok) break;
             // ---- epilogue: merge the halves, O / l -> out (this thread: dims 64h..64h+63) ----
             const uint32_t glast = kt + x.n_tiles - 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE], glast & 1, p.err) &&
-                                             mbar_wait(&bars[B_O_DONE + 1], glast & 1, p.err));
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&bars[B_O_DONE + (glast & 1)], (glast >> 1) & 1, p.err) &&
+                                mbar_wait(&bars[B_O_DONE + 2 + (glast & 1)], (glast >> 1) & 1,
+                                          p.err));
             if (!ok) break;
             tc_after();
             float2* st_set = stat + (it & 1) * 2 * kRows;
