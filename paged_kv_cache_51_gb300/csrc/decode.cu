@@ -53,6 +53,9 @@ struct PlanParams {
     int* err;
 };
 
+constexpr int kSortItems = 2048;    // prefill items reordered longest first (at most)
+constexpr int kSortBuckets = 256;   // key-tile counts (larger counts share the last bucket)
+
 __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
     __shared__ int warp_d[32], warp_p[32];
     __shared__ int carry_d, carry_p, layout_ok;
@@ -170,7 +173,55 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
         }
         p.ws.counters[2] = sms_prefill;
         p.ws.counters[3] = 0;  // decode unit ticket
+        p.ws.counters[4] = 0;  // prefill unit ticket
     }
+    // Longest first: prefill units are taken from a ticket in item order, so the
+    // items are reordered by descending key-tile count (a counting sort; items
+    // with equal counts in any order).  Large lists keep their order.
+    __syncthreads();
+    const int n_pre = min(carry_p, p.ws.max_prefill_items);
+    if (n_pre < 2 || n_pre > kSortItems) return;
+    __shared__ int2 s_item[kSortItems];
+    __shared__ int s_bucket[kSortItems];
+    __shared__ int hist[kSortBuckets], cursor[kSortBuckets];
+    for (int i = tid; i < kSortBuckets; i += 1024) hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < n_pre; i += 1024) {
+        const int2 it = p.ws.prefill_items[i];
+        const int q0 = p.query_start_loc[it.x], qlen = p.query_start_loc[it.x + 1] - q0;
+        const int t0 = it.y * p.tokens_per_tile;
+        const int nt = min(p.tokens_per_tile, qlen - t0);
+        const int n_keys = p.context_lens[it.x] - qlen + t0 + nt;
+        const int tiles = (n_keys + kPrefillKeys - 1) / kPrefillKeys;
+        const int b = kSortBuckets - 1 - min(tiles, kSortBuckets - 1);   // descending
+        s_item[i] = it;
+        s_bucket[i] = b;
+        atomicAdd(&hist[b], 1);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // exclusive scan of the histogram, kSortBuckets / 32 buckets per lane
+        constexpr int kPer = kSortBuckets / 32;
+        int run = 0;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) run += hist[lane * kPer + i];
+        int incl = run;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(kFull, incl, off);
+            if (lane >= off) incl += y;
+        }
+        int acc = incl - run;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int h = hist[lane * kPer + i];
+            cursor[lane * kPer + i] = acc;
+            acc += h;
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < n_pre; i += 1024)
+        p.ws.prefill_items[atomicAdd(&cursor[s_bucket[i]], 1)] = s_item[i];
 }
 
 int launch_plan(const AttnArgs& a) {

@@ -11,6 +11,7 @@ namespace pkv {
 
 constexpr int kSplitTokens = 512;       // context span of one decode split
 constexpr int kPrefillRows = 128;       // query rows (tokens x group heads) per prefill tile
+constexpr int kPrefillKeys = 128;       // keys per prefill key tile
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline int ceil_div(int64_t a, int64_t b) { return int((a + b - 1) / b); }
@@ -30,7 +31,7 @@ inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_E
 // Workspace carve-up shared by decode and varlen.
 struct Workspace {
     int32_t* counters;   // [0] decode items, [1] prefill items, [2] SMs for prefill,
-                         // [3] decode unit ticket
+                         // [3] decode unit ticket, [4] prefill unit ticket
     int2* items;         // decode items (seq, split)
     int2* prefill_items; // prefill items (seq, row tile)
     float2* part_ml;     // [num_seqs][num_q_heads][max_splits] (max, sum), log2 domain
@@ -73,6 +74,9 @@ int num_sms();
 // tmap.cpp: tensor map of a bf16 cache viewed as 2-D [num_blocks * Hkv * bs rows][head_dim],
 // box = one block of one head (bs rows) x 64 dims, 128-byte swizzled in shared memory.
 bool make_cache_tensor_map(struct CUtensorMap_st* map, const void* cache, const pkv_cache_desc* d);
+// tmap.cpp: queries [tokens][Hq][128] bf16; box = one 64-dim half of a 128-row prefill Q tile
+bool make_query_tensor_map(struct CUtensorMap_st* map, const void* q, int32_t num_tokens,
+                           int32_t num_q_heads, int32_t group);
 
 // decode_mma.cu: tensor-core split kernel for bf16 GQA groups of 2, 4 or 8
 bool decode_mma_eligible(const pkv_cache_desc* d);

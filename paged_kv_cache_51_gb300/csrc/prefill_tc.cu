@@ -32,10 +32,15 @@
 //              P V product is still executing.  O is rescaled only when the
 //              running max grows by more than 2^8 (the one case that waits for
 //              the previous P V).  The epilogue merges the halves.
-//   warp 8     TMA producer for K: blocks of each key tile into a 2-stage K ring;
-//              a K stage is released as soon as its Q K^T product is done
+//   warp 8     takes work units from a ticket (the planner orders them longest
+//              first) and publishes them to the other roles; TMA producer for
+//              the unit's Q tile and for K: blocks of each key tile into a
+//              3-stage K ring; a K stage is released as soon as its Q K^T
+//              product is done
 //   warp 9     TMA producer for V: a 2-stage V ring released by the P V product
-//   warp 10    TMEM owner and MMA issuer (one thread issues tcgen05.mma)
+//   warp 10    TMEM owner and MMA issuer (one thread issues tcgen05.mma); the
+//              P V of a key tile is issued after the next tile's Q K^T, so the
+//              tensor pipe has work while the softmax runs
 // Every wait is bounded; on a timeout the kernel records an error, stops
 // issuing work, drains its copies and MMAs and frees TMEM before it returns.
 #include <cuda.h>
@@ -54,15 +59,21 @@ constexpr int kRows = 128;                   // query rows per tile
 constexpr int kDim = 128;                    // head dim
 constexpr int kKeys = 128;                   // keys per key tile
 constexpr int kBlkPerTile = kKeys / kBlockTokens;  // 8 cache blocks
-constexpr int kStages = 2;
+// Ring depths.  A key tile's TMA copies take about a microsecond to land, about
+// one tile period: K runs 3 deep, V (needed one tile later) 2 deep, Q single
+// (the next unit's Q loads once the current unit's last Q K^T is done).
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
+constexpr int kQBufs = 1;
 constexpr int kSub = kRows * 128;            // one 64-column half of a 128-row operand (16 KiB)
-constexpr int kQOff = 0;                     // Q: 2 halves (dims 0-63, 64-127)
-constexpr int kKVOff = 2 * kSub;             // stages
-constexpr int kKBytes = 2 * kKeys * 128;     // K of one stage (2 halves of 128 key rows x 128 B)
-constexpr int kStageBytes = 2 * kKBytes;     // K stage s at s * kStageBytes, V stage s after it
-constexpr int kStatOff = kKVOff + kStages * kStageBytes;  // (m, l) per half and row, 2 sets
+constexpr int kQBytes = 2 * kSub;            // one Q tile: 2 halves (dims 0-63, 64-127)
+constexpr int kKBytes = 2 * kKeys * 128;     // one K or V tile (2 halves of 128 key rows x 128 B)
+constexpr int kQOff = 0;
+constexpr int kKOff = kQOff + kQBufs * kQBytes;
+constexpr int kVOff = kKOff + kKStages * kKBytes;
+constexpr int kStatOff = kVOff + kVStages * kKBytes;  // (m, l) per half and row, 2 sets
 constexpr int kBarOff = kStatOff + 2 * 2 * kRows * 8;
-constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + 1 KiB alignment slack
+constexpr int kSmemBytes = kBarOff + 1024 + 1024;  // barriers, unit ring + 1 KiB alignment slack
 constexpr int kSoftWarps = 8;
 constexpr int kKProducerWarp = 8;
 constexpr int kVProducerWarp = 9;
@@ -76,14 +87,17 @@ constexpr int kBoxBytes = kBlockTokens * 128;  // one TMA box: 16 rows x 64 bf16
 // barrier indices
 enum {
     B_K_FULL = 0,
-    B_K_EMPTY = B_K_FULL + kStages,
-    B_V_FULL = B_K_EMPTY + kStages,
-    B_V_EMPTY = B_V_FULL + kStages,
-    B_S_FULL = B_V_EMPTY + kStages,
+    B_K_EMPTY = B_K_FULL + kKStages,
+    B_V_FULL = B_K_EMPTY + kKStages,
+    B_V_EMPTY = B_V_FULL + kVStages,
+    B_S_FULL = B_V_EMPTY + kVStages,
     B_P_FULL = B_S_FULL + 2,        // [key half][S/P buffer]
     B_O_DONE = B_P_FULL + 4,        // [key half][S/P buffer]: that buffer's P V has completed
-    B_Q_FULL = B_O_DONE + 4,
-    B_O_EMPTY,
+    B_Q_FULL = B_O_DONE + 4,        // [Q buffer]
+    B_Q_EMPTY = B_Q_FULL + kQBufs,  // [Q buffer]: the unit's last Q K^T has completed
+    B_U_READY = B_Q_EMPTY + kQBufs, // [unit slot]
+    B_U_EMPTY = B_U_READY + 4,      // [unit slot]
+    B_O_EMPTY = B_U_EMPTY + 4,
     B_STAT,                         // both halves' (m, l) of the current unit are published
     B_DRAIN,
     B_COUNT
@@ -199,13 +213,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// byte offset of 16-byte chunk `c` (0..7) of row `r` in a 128-byte-swizzled half
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-    return uint32_t(r) * 128u + uint32_t((c ^ (r & 7)) << 4);
-}
-
 struct PrefillParams {
-    const __nv_bfloat16* q;
     __nv_bfloat16* out;
     const int32_t* block_tables;
     const int32_t* context_lens;
@@ -213,6 +221,7 @@ struct PrefillParams {
     const int2* items;
     const int32_t* n_items;
     const int32_t* counters;   // [2]: how many CTAs (one per SM) take prefill units
+    int32_t* ticket;           // next prefill unit (reset by the planner)
     int32_t table_stride;
     int32_t num_blocks;
     int32_t num_kv_heads;
@@ -244,9 +253,70 @@ __device__ __forceinline__ Unit unit_of(const PrefillParams& p, int u) {
     return x;
 }
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Block ids of a unit's key tiles, fetched 4 tiles (32 blocks, one per lane) at
+// a time and one group ahead, so a producer never waits on the block table.
+struct BlockIds {
+    const int32_t* bt;
+    int nblk, cur, next;
+    __device__ __forceinline__ int load(int group, int lane) const {
+        const int i = group * 32 + lane;
+        return i < nblk ? bt[i] : -1;
+    }
+    __device__ __forceinline__ void start(const int32_t* table, int n, int lane) {
+        bt = table;
+        nblk = n;
+        cur = load(0, lane);
+        next = load(1, lane);
+    }
+    // block id of block i (0..7) of key tile j for lanes i < 8; call for j = 0, 1, 2, ...
+    __device__ __forceinline__ int tile(int j, int lane) {
+        if (j > 0 && (j & 3) == 0) {
+            cur = next;
+            next = load((j >> 2) + 1, lane);
+        }
+        return __shfl_sync(0xffffffffu, cur, ((j & 3) << 3) + (lane & 7));
+    }
+};
+
+// Unit ring: the K producer takes units from the ticket (the planner ordered
+// the items longest first) and publishes them; the V producer, the MMA issuer
+// and the 8 softmax warps read each one and release its slot.
+constexpr int kUnitSlots = 4;
+constexpr int kUnitReaders = 1 + 1 + kSoftWarps;
+
+// A published unit: its id (-1: no more work) and geometry, computed once by
+// the K producer so the other roles start a unit without global loads.
+struct UnitSlot {
+    int u;
+    Unit x;
+};
+
+__device__ __forceinline__ int unit_read(uint64_t* bars, const UnitSlot* ring, uint32_t k,
+                                         int* err, bool& ok, Unit& x) {
+    const int slot = k % kUnitSlots;
+    int u = -1;
+    if (ok && mbar_wait(&bars[B_U_READY + slot], (k / kUnitSlots) & 1, err)) {
+        u = ring[slot].u;
+        x = ring[slot].x;
+    } else {
+        ok = false;
+    }
+    return u;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                   const __grid_constant__ CUtensorMap tmap_v, PrefillParams p) {
+                   const __grid_constant__ CUtensorMap tmap_v,
+                   const __grid_constant__ CUtensorMap tmap_q, PrefillParams p) {
     // The planner gives the prefill chunks only as many SMs as their share of
     // the batch's work; the other CTAs leave at once, and the decode kernel that
     // follows in the stream may start right away on the SMs they free.
@@ -261,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + B_COUNT * 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + B_COUNT * 8 + 4);
+    UnitSlot* unit_ring = reinterpret_cast<UnitSlot*>(smem + kBarOff + B_COUNT * 8 + 16);
     float2* stat = reinterpret_cast<float2*>(smem + kStatOff);  // [set][half][row]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -270,18 +341,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = threadIdx.x; i < kStatOff / 16; i += kThreads)
         reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kKStages; ++s) {
             mbar_init(&bars[B_K_FULL + s], 1);
             mbar_init(&bars[B_K_EMPTY + s], 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
             mbar_init(&bars[B_V_FULL + s], 1);
             mbar_init(&bars[B_V_EMPTY + s], 1);
+        }
+        for (int s = 0; s < kQBufs; ++s) {
+            mbar_init(&bars[B_Q_FULL + s], 1);
+            mbar_init(&bars[B_Q_EMPTY + s], 1);
         }
         for (int s = 0; s < 2; ++s) mbar_init(&bars[B_S_FULL + s], 1);
         for (int s = 0; s < 4; ++s) {
             mbar_init(&bars[B_P_FULL + s], kSoftWarps / 2);
             mbar_init(&bars[B_O_DONE + s], 1);
         }
-        mbar_init(&bars[B_Q_FULL], kSoftWarps);
+        for (int s = 0; s < kUnitSlots; ++s) {
+            mbar_init(&bars[B_U_READY + s], 1);
+            mbar_init(&bars[B_U_EMPTY + s], kUnitReaders);
+        }
         mbar_init(&bars[B_O_EMPTY], kSoftWarps);
         mbar_init(&bars[B_STAT], kSoftWarps);
         mbar_init(&bars[B_DRAIN], 1);
@@ -301,68 +381,136 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kKProducerWarp || warp == kVProducerWarp) {
-        // ------------------- TMA producers (K ring, V ring) -------------------
-        const bool is_v = warp == kVProducerWarp;
-        const CUtensorMap* map = is_v ? &tmap_v : &tmap_k;
-        uint64_t* full = bars + (is_v ? B_V_FULL : B_K_FULL);
-        uint64_t* empty = bars + (is_v ? B_V_EMPTY : B_K_EMPTY);
-        const uint32_t ring = base + kKVOff + (is_v ? kKBytes : 0);
+    if (warp == kKProducerWarp) {
+        // ------- unit tickets, Q tiles and the K ring (one warp) -------
         uint32_t kt = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units && ok; u += active) {
-            const Unit x = unit_of(p, u);
-            const int32_t* bt = p.block_tables + size_t(x.seq) * p.table_stride;
+        int next = lane == 0 ? atomicAdd(p.ticket, 1) : 0;
+        for (uint32_t k = 0;; ++k) {
+            const int slot = k % kUnitSlots;
+            ok = ok && __all_sync(0xffffffffu, mbar_wait(&bars[B_U_EMPTY + slot],
+                                                         ((k / kUnitSlots) & 1) ^ 1, p.err));
+            int u = -1;
+            if (lane == 0 && ok && !*abort_flag && next < n_units) {
+                u = next;
+                next = atomicAdd(p.ticket, 1);
+            }
+            u = __shfl_sync(0xffffffffu, u, 0);
+            Unit x = {};
+            if (u >= 0) x = unit_of(p, u);
+            if (lane == 0) {
+                unit_ring[slot].u = u;
+                unit_ring[slot].x = x;
+                mbar_arrive(&bars[B_U_READY + slot]);
+            }
+            if (u < 0) break;
+            // Q tile of the unit (two 64-dim halves)
+            const int qb = k % kQBufs;
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&bars[B_Q_EMPTY + qb], ((k / kQBufs) & 1) ^ 1, p.err));
+            if (!ok) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars[B_Q_FULL + qb], 2 * kSub);
+                const uint32_t qd = base + kQOff + qb * kQBytes;
+                tma_load_3d(qd, &tmap_q, 0, x.kvh * p.group, x.q0 + x.t0, &bars[B_Q_FULL + qb]);
+                tma_load_3d(qd + kSub, &tmap_q, 64, x.kvh * p.group, x.q0 + x.t0,
+                            &bars[B_Q_FULL + qb]);
+            }
+            __syncwarp();
+            BlockIds ids;
+            ids.start(p.block_tables + size_t(x.seq) * p.table_stride, x.nblk, lane);
             for (int j = 0; j < x.n_tiles && ok; ++j, ++kt) {
-                const int st = kt % kStages;
-                // read the tile's block ids first: the load overlaps the wait for a free stage
+                const int st = kt % kKStages;
                 const int nb = min(kBlkPerTile, x.nblk - j * kBlkPerTile);
-                int blk = -1;
-                if (lane < nb) blk = bt[j * kBlkPerTile + lane];
+                const int blk = ids.tile(j, lane);
                 ok = __all_sync(0xffffffffu,
-                                mbar_wait(&empty[st], ((kt / kStages) & 1) ^ 1, p.err));
+                                mbar_wait(&bars[B_K_EMPTY + st], ((kt / kKStages) & 1) ^ 1, p.err));
                 if (!ok || *abort_flag) {
                     ok = false;
                     break;
                 }
                 const bool good = lane < nb && blk >= 0 && blk < p.num_blocks;
-                if (lane < nb && !good && !is_v) flag_error(p.err, PKV_DEV_BAD_BLOCK_ID);
+                if (lane < nb && !good) flag_error(p.err, PKV_DEV_BAD_BLOCK_ID);
                 const unsigned mask = __ballot_sync(0xffffffffu, good);
-                if (lane == 0) mbar_arrive_expect_tx(&full[st], uint32_t(__popc(mask)) * 2u * kBoxBytes);
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&bars[B_K_FULL + st], uint32_t(__popc(mask)) * 2u * kBoxBytes);
                 __syncwarp();
                 if (good) {
-                    // each lane issues its own block's two 64-dim boxes
-                    const uint32_t dst = ring + st * kStageBytes + uint32_t(lane) * kBoxBytes;
+                    const uint32_t dst = base + kKOff + st * kKBytes + uint32_t(lane) * kBoxBytes;
                     const int row = (blk * p.num_kv_heads + x.kvh) * kBlockTokens;
-                    tma_load_2d(dst, map, 0, row, &full[st]);
-                    tma_load_2d(dst + kKeys * 128, map, 64, row, &full[st]);
+                    tma_load_2d(dst, &tmap_k, 0, row, &bars[B_K_FULL + st]);
+                    tma_load_2d(dst + kKeys * 128, &tmap_k, 64, row, &bars[B_K_FULL + st]);
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+        }
+        if (!ok) *abort_flag = 1;
+        // never leave with copies in flight: wait for the last fill of each stage
+        if (lane == 0) {
+            for (int k = 0; k < kKStages && uint32_t(k) < kt; ++k) {
+                const uint32_t last = kt - 1 - k;
+                mbar_wait(&bars[B_K_FULL + last % kKStages], (last / kKStages) & 1, p.err);
+            }
+        }
+    } else if (warp == kVProducerWarp) {
+        // ------------------------------ V ring ------------------------------
+        uint32_t kt = 0;
+        bool ok = true;
+        for (uint32_t k = 0;; ++k) {
+            Unit x;
+            const int u = unit_read(bars, unit_ring, k, p.err, ok, x);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_U_EMPTY + k % kUnitSlots]);
+            if (u < 0 || !ok) break;
+            BlockIds ids;
+            ids.start(p.block_tables + size_t(x.seq) * p.table_stride, x.nblk, lane);
+            for (int j = 0; j < x.n_tiles && ok; ++j, ++kt) {
+                const int st = kt % kVStages;
+                const int nb = min(kBlkPerTile, x.nblk - j * kBlkPerTile);
+                const int blk = ids.tile(j, lane);
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&bars[B_V_EMPTY + st], ((kt / kVStages) & 1) ^ 1, p.err));
+                if (!ok || *abort_flag) {
+                    ok = false;
+                    break;
+                }
+                const bool good = lane < nb && blk >= 0 && blk < p.num_blocks;
+                const unsigned mask = __ballot_sync(0xffffffffu, good);
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&bars[B_V_FULL + st], uint32_t(__popc(mask)) * 2u * kBoxBytes);
+                __syncwarp();
+                if (good) {
+                    const uint32_t dst = base + kVOff + st * kKBytes + uint32_t(lane) * kBoxBytes;
+                    const int row = (blk * p.num_kv_heads + x.kvh) * kBlockTokens;
+                    tma_load_2d(dst, &tmap_v, 0, row, &bars[B_V_FULL + st]);
+                    tma_load_2d(dst + kKeys * 128, &tmap_v, 64, row, &bars[B_V_FULL + st]);
                 }
                 __syncwarp();
             }
         }
         if (!ok) *abort_flag = 1;
-        // never leave with copies in flight: wait for the last fill of each stage
         if (lane == 0) {
-            for (int k = 0; k < kStages && uint32_t(k) < kt; ++k) {
+            for (int k = 0; k < kVStages && uint32_t(k) < kt; ++k) {
                 const uint32_t last = kt - 1 - k;
-                mbar_wait(&full[last % kStages], (last / kStages) & 1, p.err);
+                mbar_wait(&bars[B_V_FULL + last % kVStages], (last / kVStages) & 1, p.err);
             }
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
-            uint32_t kt = 0, it = 0;
+            uint32_t kt = 0;
             bool ok = true;
-            const uint32_t q_addr = base + kQOff;
             // O_h += P_h V_h over the 64 keys of half h, for both halves; P_h is
-            // bf16 in TMEM over the first 32 columns of its scores
-            auto pv = [&](uint32_t g, int j) -> bool {
-                const uint32_t vs = base + kKVOff + (g % kStages) * kStageBytes + kKBytes;
+            // bf16 in TMEM over the first 32 columns of its scores.  The first
+            // product of unit k waits until unit k - 1's epilogue has read O.
+            auto pv = [&](uint32_t g, int j, uint32_t k) -> bool {
+                const uint32_t vs = base + kVOff + (g % kVStages) * kKBytes;
                 const uint32_t b = g & 1;
-                if (!mbar_wait(&bars[B_V_FULL + g % kStages], (g / kStages) & 1, p.err)) return false;
+                if (!mbar_wait(&bars[B_V_FULL + g % kVStages], (g / kVStages) & 1, p.err)) return false;
                 for (int h = 0; h < 2; ++h) {
                     if (!mbar_wait(&bars[B_P_FULL + 2 * h + b], (g >> 1) & 1, p.err)) return false;
-                    if (j == 0 && h == 0 && !mbar_wait(&bars[B_O_EMPTY], (it & 1) ^ 1, p.err))
+                    if (j == 0 && h == 0 && !mbar_wait(&bars[B_O_EMPTY], (k & 1) ^ 1, p.err))
                         return false;
                     tc_after();
 #pragma unroll
@@ -373,23 +521,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     umma_commit(&bars[B_O_DONE + 2 * h + b]);
                 }
-                umma_commit(&bars[B_V_EMPTY + g % kStages]);
+                umma_commit(&bars[B_V_EMPTY + g % kVStages]);
                 return true;
             };
-            for (int u = blockIdx.x; u < n_units && ok; u += active, ++it) {
-                const Unit x = unit_of(p, u);
-                ok = mbar_wait(&bars[B_Q_FULL], it & 1, p.err) && !*abort_flag;
+            // the P V of the previous key tile is issued after the next Q K^T, so the
+            // tensor pipe has work while the softmax runs (across units as well)
+            bool pending = false;
+            uint32_t pend_g = 0, pend_k = 0;
+            int pend_j = 0;
+            for (uint32_t k = 0;; ++k) {
+                Unit x;
+                const int u = unit_read(bars, unit_ring, k, p.err, ok, x);
+                mbar_arrive(&bars[B_U_EMPTY + k % kUnitSlots]);
+                if (u < 0 || !ok || *abort_flag) break;
+                const uint32_t qb = k % kQBufs;
+                ok = mbar_wait(&bars[B_Q_FULL + qb], (k / kQBufs) & 1, p.err) && !*abort_flag;
                 if (!ok) break;
                 tc_after();
+                const uint32_t q_addr = base + kQOff + qb * kQBytes;
                 for (int j = 0; j < x.n_tiles && ok; ++j) {
                     const uint32_t g = kt + j;
                     // S/P buffer g & 1 last held P(g - 2), whose P V was issued before
                     // this product: tensor-core instructions run in issue order
-                    ok = mbar_wait(&bars[B_K_FULL + g % kStages], (g / kStages) & 1, p.err) &&
+                    ok = mbar_wait(&bars[B_K_FULL + g % kKStages], (g / kKStages) & 1, p.err) &&
                          !*abort_flag;
                     if (!ok) break;
                     tc_after();
-                    const uint32_t ks = base + kKVOff + (g % kStages) * kStageBytes;
+                    const uint32_t ks = base + kKOff + (g % kKStages) * kKBytes;
 #pragma unroll
                     for (int kk = 0; kk < kDim / 16; ++kk) {
                         const uint64_t a = sdesc(q_addr + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
@@ -398,10 +556,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         umma(tmem + (g & 1) * kKeys, a, b, kIdescQK, kk > 0 ? 1u : 0u);
                     }
                     umma_commit(&bars[B_S_FULL + (g & 1)]);
-                    umma_commit(&bars[B_K_EMPTY + g % kStages]);
-                    if (j > 0) ok = pv(g - 1, j - 1) && !*abort_flag;
+                    umma_commit(&bars[B_K_EMPTY + g % kKStages]);
+                    if (j == x.n_tiles - 1) umma_commit(&bars[B_Q_EMPTY + qb]);
+                    if (pending) ok = pv(pend_g, pend_j, pend_k) && !*abort_flag;
+                    pending = true;
+                    pend_g = g;
+                    pend_j = j;
+                    pend_k = k;
                 }
-                if (ok) ok = pv(kt + x.n_tiles - 1, x.n_tiles - 1);
+                // the unit's last P V now: its epilogue waits for it, and the next
+                // unit's first Q K^T would wait for that unit's Q tile anyway
+                if (ok && pending) ok = pv(pend_g, pend_j, pend_k) && !*abort_flag;
+                pending = false;
                 kt += x.n_tiles;
             }
             if (!ok) *abort_flag = 1;
@@ -416,27 +582,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = warp >> 2;                          // key half of each 128-key tile
         const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
         const int G = p.group;
-        uint32_t kt = 0, it = 0;
+        uint32_t kt = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units; u += active, ++it) {
-            const Unit x = unit_of(p, u);
+        for (uint32_t k = 0;; ++k) {
+            Unit x;
+            const int u = unit_read(bars, unit_ring, k, p.err, ok, x);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_U_EMPTY + k % kUnitSlots]);
+            if (u < 0 || !ok) break;
             const int tok = r / G, g_head = r % G;
             const bool row_valid = tok < x.nt;
             const int t = x.t0 + tok;
             const int limit = row_valid ? x.ctx - x.qlen + t : x.ctx - 1;  // last visible key
-            // ---- Q row, dims 64h..64h+63 -> Q half h (swizzled K-major) ----
-            {
-                const uint4* src = reinterpret_cast<const uint4*>(
-                    p.q + (size_t(x.q0 + t) * p.num_q_heads + x.kvh * G + g_head) * kDim + h * 64);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 v = row_valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4*>(smem + kQOff + h * kSub + swz(r, c)) = v;
-                }
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_Q_FULL]);
 
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < x.n_tiles; ++j) {
@@ -460,14 +617,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         s[32 + i] = __uint_as_float(v1[i]);
                     }
                 }
+
                 // mask keys beyond this row's causal limit; max on the raw scores
                 const int key0 = j * kKeys + h * 64;
-                float mx = -INFINITY;
+                if (key0 + 63 > limit) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    s[c] = (key0 + c <= limit) ? s[c] : -INFINITY;
-                    mx = fmaxf(mx, s[c]);
+                    for (int c = 0; c < 64; ++c) s[c] = (key0 + c <= limit) ? s[c] : -INFINITY;
                 }
+                // eight independent partial maxima instead of one 64-long chain
+                float mx8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+                for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
                 const float m_new = fmaxf(m, mx * p.scale_log2);
                 const bool need = m_new > m + kRescaleThreshold;  // first visible keys included
                 float alpha = 1.f;
@@ -476,18 +640,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m = m_new;
                     l *= alpha;
                 }
-                // P = 2^(s * scale - m) in bf16, computed before waiting on the previous PV
+                // P = 2^(s * scale - m) in bf16
                 const float neg_m = m == -INFINITY ? 0.f : -m;
                 uint32_t w[32];
-                float rowsum = 0.f;
+                float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
                     const float p0 = exp2f(fmaf(s[2 * c], p.scale_log2, neg_m));
                     const float p1 = exp2f(fmaf(s[2 * c + 1], p.scale_log2, neg_m));
-                    rowsum += p0 + p1;
+                    sum8[c & 7] += p0 + p1;
                     w[c] = pack_bf16(p0, p1);
                 }
-                l += rowsum;
+                l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                     ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
                 const bool warp_need = __any_sync(0xffffffffu, need);
                 if (j > 0 && warp_need) {
                     // rescale O_h: wait for the previous P V of this half (buffer
@@ -517,14 +682,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // The half whose keys hold that block does it before its P V.
                 const int rows_last = x.ctx - (x.nblk - 1) * kBlockTokens;  // valid rows, 1..16+
                 const int slot = (x.nblk - 1) - j * kBlkPerTile;
-                if (j == x.n_tiles - 1 && rows_last < kBlockTokens && (slot >> 2) == h) {
+                const bool zero_v = j == x.n_tiles - 1 && rows_last < kBlockTokens && (slot >> 2) == h;
+                if (zero_v) {
                     // the V tile must have landed before its rows are overwritten (its
                     // stage cannot be refilled before this tile's P V has been issued)
-                    ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_V_FULL + g % kStages],
-                                                           (g / kStages) & 1, p.err));
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_V_FULL + g % kVStages],
+                                                           (g / kVStages) & 1, p.err));
                     if (!ok) break;
                     const int nz = (kBlockTokens - rows_last) * 2 * 8;  // rows x halves x chunks
-                    unsigned char* vs = smem + kKVOff + (g % kStages) * kStageBytes + kKBytes;
+                    unsigned char* vs = smem + kVOff + (g % kVStages) * kKBytes;
                     for (int i = r; i < nz; i += kRows) {
                         const int row = rows_last + i / 16, half = (i / 8) & 1, c = i & 7;
                         *reinterpret_cast<uint4*>(vs + half * (kKeys * 128) +
@@ -532,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             make_uint4(0, 0, 0, 0);
                     }
                 }
-                fence_async_smem();
+                if (zero_v) fence_async_smem();   // the zeroed V rows, before the P V reads them
                 tmem_wait_st();
                 tc_before();
                 __syncwarp();
@@ -547,11 +713,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           p.err));
             if (!ok) break;
             tc_after();
-            float2* st_set = stat + (it & 1) * 2 * kRows;
+            float2* st_set = stat + (k & 1) * 2 * kRows;
             st_set[h * kRows + r] = make_float2(m, l);
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_STAT]);
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_STAT], it & 1, p.err));
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_STAT], k & 1, p.err));
             if (!ok) break;
             const float2 o0 = st_set[r], o1 = st_set[kRows + r];
             const float M = fmaxf(o0.x, o1.x);
@@ -571,9 +737,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 4; ++e) {
                         uint32_t q4[4];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int i0 = e * 8 + 2 * k;
-                            q4[k] = pack_bf16(
+                        for (int kq = 0; kq < 4; ++kq) {
+                            const int i0 = e * 8 + 2 * kq;
+                            q4[kq] = pack_bf16(
                                 __uint_as_float(v0[i0]) * w0 + __uint_as_float(v1[i0]) * w1,
                                 __uint_as_float(v0[i0 + 1]) * w0 + __uint_as_float(v1[i0 + 1]) * w1);
                         }
@@ -625,11 +791,12 @@ int prefill_item_bound(int32_t num_seqs, int32_t num_query_tokens, int32_t group
 int launch_prefill(const AttnArgs& a) {
     const pkv_cache_desc* d = a.desc;
     if (!prefill_supported(d)) return PKV_ERR_UNSUPPORTED;
-    CUtensorMap mk, mv;
-    if (!make_cache_tensor_map(&mk, a.k_cache, d) || !make_cache_tensor_map(&mv, a.v_cache, d))
+    const int group = d->num_q_heads / d->num_kv_heads;
+    CUtensorMap mk, mv, mq;
+    if (!make_cache_tensor_map(&mk, a.k_cache, d) || !make_cache_tensor_map(&mv, a.v_cache, d) ||
+        !make_query_tensor_map(&mq, a.q, a.num_query_tokens, d->num_q_heads, group))
         return PKV_ERR_CUDA;
     PrefillParams p;
-    p.q = static_cast<const __nv_bfloat16*>(a.q);
     p.out = static_cast<__nv_bfloat16*>(a.out);
     p.block_tables = a.block_tables;
     p.context_lens = a.context_lens;
@@ -637,11 +804,12 @@ int launch_prefill(const AttnArgs& a) {
     p.items = a.ws.prefill_items;
     p.n_items = a.ws.counters + 1;
     p.counters = a.ws.counters;
+    p.ticket = a.ws.counters + 4;
     p.table_stride = a.table_stride;
     p.num_blocks = d->num_blocks;
     p.num_kv_heads = d->num_kv_heads;
     p.num_q_heads = d->num_q_heads;
-    p.group = d->num_q_heads / d->num_kv_heads;
+    p.group = group;
     p.tokens_per_tile = kPrefillRows / p.group;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.err = a.err;
@@ -651,7 +819,7 @@ int launch_prefill(const AttnArgs& a) {
     const int64_t bound = int64_t(a.ws.max_prefill_items) * d->num_kv_heads;
     const int64_t grid = std::min<int64_t>(sm_count(), bound);
     if (grid < 1) return PKV_OK;
-    prefill_kernel<<<unsigned(grid), kThreads, kSmemBytes, a.stream>>>(mk, mv, p);
+    prefill_kernel<<<unsigned(grid), kThreads, kSmemBytes, a.stream>>>(mk, mv, mq, p);
     return cuda_status(cudaGetLastError());
 }
 

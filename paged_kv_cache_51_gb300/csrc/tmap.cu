@@ -45,4 +45,23 @@ bool make_cache_tensor_map(CUtensorMap* m, const void* cache, const pkv_cache_de
            CUDA_SUCCESS;
 }
 
+// Queries [num_tokens][num_q_heads][128] (bf16) as a 3-D tensor (dims, heads,
+// tokens).  A box is 64 dims x G heads x 128 / G tokens: the 128 rows
+// (token, head of the group) of one 64-dim half of a prefill Q tile, 128 B
+// each, landing 128-byte swizzled like the cache tiles.  Tokens past the end
+// read as zero.
+bool make_query_tensor_map(CUtensorMap* m, const void* q, int32_t num_tokens, int32_t num_q_heads,
+                           int32_t group) {
+    auto fn = encode_fn();
+    if (!fn || num_tokens < 1 || group < 1 || kPrefillRows % group) return false;
+    const cuuint64_t gdim[3] = {128, cuuint64_t(num_q_heads), cuuint64_t(num_tokens)};
+    const cuuint64_t gstride[2] = {128 * 2, cuuint64_t(num_q_heads) * 128 * 2};
+    const cuuint32_t box[3] = {64, cuuint32_t(group), cuuint32_t(kPrefillRows / group)};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), gdim, gstride, box,
+              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 }  // namespace pkv
