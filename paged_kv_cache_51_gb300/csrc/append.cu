@@ -215,12 +215,6 @@ __global__ void __launch_bounds__(256) append_rope_kernel(RopeParams p) {
 namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return n;
-}
 }  // namespace
 
 }  // namespace pkv
@@ -255,7 +249,7 @@ extern "C" int paged_kv_append(const void* k, const void* v, const int64_t* slot
     p.num_slots = int64_t(desc->num_blocks) * desc->block_size;
     p.err = err;
     const int64_t total = int64_t(num_tokens) * desc->num_kv_heads * p.vec_per_row;
-    const int64_t cap = int64_t(std::max(sm_count(), 1)) * 8;
+    const int64_t cap = int64_t(std::max(num_sms(), 1)) * 8;
     const int64_t blocks = std::min<int64_t>((total + 255) / 256, cap);
     append_kernel<<<unsigned(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
     return cuda_status(cudaGetLastError());
@@ -368,7 +362,7 @@ extern "C" int paged_kv_append_rope(const void* q, void* q_out, const void* k, c
     p.err = err;
     const int64_t total = int64_t(num_tokens) * (p.num_q_rows + 2 * p.num_kv_heads) *
                           (desc->head_dim / 16);
-    const int64_t blocks = std::min<int64_t>((total + 255) / 256, int64_t(std::max(sm_count(), 1)) * 8);
+    const int64_t blocks = std::min<int64_t>((total + 255) / 256, int64_t(std::max(num_sms(), 1)) * 8);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool bf = desc->dtype == PKV_BF16;
     if (desc->head_dim == 128) {

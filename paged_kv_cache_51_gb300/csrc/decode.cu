@@ -24,10 +24,12 @@
 //  * Persistent grid (a multiple of the SM count) over a work list that a
 //    one-CTA planner kernel builds on the device, so no host round trip.
 #include <algorithm>
+#include <atomic>
 #include <cfloat>
 #include <cuda_runtime.h>
 
 #include "decode_common.cuh"
+#include "launch_cache.h"
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -580,9 +582,13 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(MergeParams p) {
 // Host launchers
 // ---------------------------------------------------------------------------
 int num_sms() {
+    static std::atomic<int> cached[kMaxDevices];
     int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    n = cached[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
@@ -592,13 +598,8 @@ template <typename T, int D, int G>
 int launch_split_t(const AttnArgs& a) {
     using C = SplitCfg<T, D, G>;
     auto kern = decode_split_kernel<T, D, G>;
-    // per-device attribute setup is cheap and idempotent
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(C::kSmem));
-    if (e != cudaSuccess) return PKV_ERR_CUDA;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::kThreads, C::kSmem);
-    if (e != cudaSuccess || per_sm < 1) return PKV_ERR_CUDA;
+    const int per_sm = kernel_occupancy<decode_split_kernel<T, D, G>>(C::kThreads, int(C::kSmem));
+    if (per_sm < 1) return PKV_ERR_CUDA;
     const int64_t bound_units =
         int64_t(a.num_seqs) * a.ws.max_splits * a.desc->num_kv_heads;  // upper bound
     const int64_t grid = std::min<int64_t>(int64_t(num_sms()) * per_sm, bound_units);

@@ -22,6 +22,7 @@
 
 #include <algorithm>
 
+#include "launch_cache.h"
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -374,13 +375,6 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads)
     if (threadIdx.x == 0) pdl_wait_prerequisites();
 }
 
-int sms() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return n;
-}
-
 template <int D, int G>
 int launch_t(const AttnArgs& a) {
     using C = MmaCfg<D, G>;
@@ -389,16 +383,10 @@ int launch_t(const AttnArgs& a) {
     if (!make_cache_tensor_map(&mk, a.k_cache, a.desc) ||
         !make_cache_tensor_map(&mv, a.v_cache, a.desc))
         return PKV_ERR_CUDA;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
-        cudaSuccess)
-        return PKV_ERR_CUDA;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::kThreads, C::kSmem) !=
-            cudaSuccess ||
-        per_sm < 1)
-        return PKV_ERR_CUDA;
+    const int per_sm = kernel_occupancy<decode_split_mma_kernel<D, G>>(C::kThreads, C::kSmem);
+    if (per_sm < 1) return PKV_ERR_CUDA;
     const int64_t bound = int64_t(a.num_seqs) * a.ws.max_splits * a.desc->num_kv_heads;
-    const int64_t grid = std::min<int64_t>(int64_t(sms()) * per_sm, bound);
+    const int64_t grid = std::min<int64_t>(int64_t(num_sms()) * per_sm, bound);
     if (grid < 1) return PKV_OK;
     MmaParams p;
     p.q = static_cast<const __nv_bfloat16*>(a.q);

@@ -35,6 +35,7 @@
 #include <cmath>
 
 #include "decode_common.cuh"
+#include "launch_cache.h"
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -521,14 +522,8 @@ int launch_i8(const AttnArgs& a, const int8_t* kc, const int8_t* vc, const float
               const float* vs) {
     using C = I8Cfg<D, G>;
     auto kern = decode_split_int8_kernel<D, G>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
-        cudaSuccess)
-        return PKV_ERR_CUDA;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::kThreads, C::kSmem) !=
-            cudaSuccess ||
-        per_sm < 1)
-        return PKV_ERR_CUDA;
+    const int per_sm = kernel_occupancy<decode_split_int8_kernel<D, G>>(C::kThreads, C::kSmem);
+    if (per_sm < 1) return PKV_ERR_CUDA;
     const int64_t bound = int64_t(a.num_seqs) * a.ws.max_splits * a.desc->num_kv_heads;
     const int64_t grid = std::min<int64_t>(int64_t(num_sms()) * per_sm, bound);
     if (grid < 1) return PKV_OK;

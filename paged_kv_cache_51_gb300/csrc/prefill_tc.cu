@@ -49,6 +49,7 @@
 
 #include <algorithm>
 
+#include "launch_cache.h"
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -767,13 +768,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- host side -------------------------------------------------------------
 
-int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return n;
-}
-
 }  // namespace
 
 int prefill_supported(const pkv_cache_desc* d) {
@@ -813,11 +807,9 @@ int launch_prefill(const AttnArgs& a) {
     p.tokens_per_tile = kPrefillRows / p.group;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.err = a.err;
-    if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
-        return PKV_ERR_CUDA;
+    if (kernel_occupancy<prefill_kernel>(kThreads, kSmemBytes) < 1) return PKV_ERR_CUDA;
     const int64_t bound = int64_t(a.ws.max_prefill_items) * d->num_kv_heads;
-    const int64_t grid = std::min<int64_t>(sm_count(), bound);
+    const int64_t grid = std::min<int64_t>(num_sms(), bound);
     if (grid < 1) return PKV_OK;
     prefill_kernel<<<unsigned(grid), kThreads, kSmemBytes, a.stream>>>(mk, mv, mq, p);
     return cuda_status(cudaGetLastError());
