@@ -58,7 +58,10 @@ struct MmaCfg {
     static constexpr int kHalves = D / 64;                 // 64-dim boxes per tile
     static constexpr int kTileBytes = kBlockTokens * D * 2;
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kStages = 8;
+    // g = 8 runs 3 CTAs per SM on a 4-stage ring (measured faster on the
+    // prefix-sharing batch); smaller groups keep 8 stages at 2 CTAs per SM
+    static constexpr int kStages = G == 8 ? 4 : 8;
+    static constexpr int kMinBlocks = G == 8 ? 3 : 1;
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kComb = G * (D + 2);
     static constexpr int kCombOff = kRingBytes;
@@ -119,7 +122,7 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t tile, int t, int c) {
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(MmaCfg<D, G>::kThreads)
+__global__ void __launch_bounds__(MmaCfg<D, G>::kThreads, MmaCfg<D, G>::kMinBlocks)
     decode_split_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v, MmaParams p) {
     using C = MmaCfg<D, G>;
