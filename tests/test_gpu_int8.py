@@ -174,3 +174,54 @@ def test_int8_copy_on_write_moves_codes_and_scales(lib):
     assert np.array_equal(kl, kq) and np.array_equal(vl, vq)
     assert np.array_equal(ic.k_scales.cpu().numpy(), ks)
     assert np.array_equal(ic.v_scales.cpu().numpy(), vs)
+
+
+@pytest.mark.parametrize("cfg", [2, 3])
+def test_int8_full_size_sampled(lib, cfg):
+    """The benchmark's full batches (Llama-2-7B decode, Llama-3-8B GQA decode):
+    every slot of the step's bf16 pools quantised on the device, then the int8
+    decode call as timed; six sequences checked against the oracle, which
+    quantises those sequences' blocks itself (codes and scales bit-exact,
+    attention within the bf16 tolerance)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_51_gb300 import runner
+
+    w = workloads.make(cfg)
+    dc, step = runner.prepare(w)
+    step.run()
+    torch.cuda.synchronize()
+    nb, hkv, bs, d = dc.k_cache.shape
+    ic = lib.Int8Cache(nb, hkv, bs, d, w.num_q_heads)
+
+    def rows(c):
+        return c.transpose(1, 2).reshape(nb * bs, hkv, d).contiguous()
+
+    lib.device_error(clear=True)
+    lib.paged_kv_append_int8(rows(dc.k_cache), rows(dc.v_cache),
+                             torch.arange(nb * bs, dtype=torch.int64, device="cuda"), ic)
+    out = torch.empty_like(step.q)
+    lib.paged_attention_decode_int8(out, step.q, ic, step.tables, step.ctx, step.max_ctx)
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0
+    ost, _ = execute(w, with_attention=False)
+    bt, ctx, _ = ost.batch_metadata()
+    assert np.array_equal(bt[:, :step.tables.shape[1]], step.tables.cpu().numpy())
+    q_bits = step.q.cpu().view(torch.int16).numpy().view(np.uint16)
+    got = out_f64(out)
+    rng = np.random.default_rng(cfg)
+    for s in rng.choice(len(ctx), size=6, replace=False):
+        n = -(-int(ctx[s]) // bs)
+        blocks = bt[s, :n]
+        kq, ks = quant.quantize_rows(ost.k_cache[blocks], "bf16")
+        vq, vs = quant.quantize_rows(ost.v_cache[blocks], "bf16")
+        idx = torch.from_numpy(blocks.astype(np.int64)).cuda()
+        kl, vl = _logical_codes(ic.k_codes[idx], ic.v_codes[idx])
+        assert np.array_equal(kl, kq) and np.array_equal(vl, vq)
+        assert np.array_equal(ic.k_scales[idx].cpu().numpy().view(np.uint32), ks.view(np.uint32))
+        assert np.array_equal(ic.v_scales[idx].cpu().numpy().view(np.uint32), vs.view(np.uint32))
+        ref = quant.decode_int8(q_bits[s:s + 1], kq, ks, vq, vs, np.arange(n)[None], [int(ctx[s])],
+                                bs, "bf16")
+        diff = np.abs(got[s:s + 1] - ref)
+        tmax, tmean = TOL["bf16"]
+        assert float(diff.max()) <= tmax and float(diff.mean()) <= tmean
