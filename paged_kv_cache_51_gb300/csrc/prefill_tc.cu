@@ -137,22 +137,50 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                     uint32_t accumulate) {
+// Bursts of eight products from one asm block.  The issuing thread runs in step
+// with the tensor pipe (measured: each cycle it spends between two products is a
+// cycle the pipe idles), so a tile's products go out back to back with their
+// descriptors computed beforehand.
+//
+// S = Q K^T over K = 128 dims in eight K = 16 steps; the first step overwrites D.
+__device__ __forceinline__ void umma_ss8(uint32_t d, const uint64_t (&a)[8], const uint64_t (&b)[8],
+                                         uint32_t idesc) {
     asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        "{\n .reg .pred pz, pa;\n setp.ne.b32 pz, %17, %17;\n setp.eq.b32 pa, %17, %17;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %9, %17, pz;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %10, %17, pa;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %17, pa;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %17, pa;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %17, pa;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %17, pa;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %17, pa;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %17, pa;\n}\n" ::"r"(d),
+        "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]),
+        "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]),
+        "r"(idesc)
         : "memory");
 }
 
-// A operand from tensor memory (rows in lanes, K packed two bf16 per column)
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
-                                        uint32_t idesc, uint32_t accumulate) {
+// O_h += P_h V_h for both key halves h (four K = 16 steps each): D of half h at
+// d + 128 h, A (P_h, bf16 pairs in TMEM) at a + 64 h + 8 kk, B descriptors
+// b[4 h + kk].  The first step of each half accumulates only if `acc` is set.
+__device__ __forceinline__ void umma_ts8(uint32_t d, uint32_t a, const uint64_t (&b)[8],
+                                         uint32_t idesc, uint32_t acc) {
     asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+        "{\n .reg .pred pf, pa;\n .reg .b32 d1, a1, a2, a3, a4, a5, a6, a7;\n"
+        " setp.ne.b32 pf, %10, 0;\n setp.eq.b32 pa, %10, %10;\n"
+        " add.u32 d1, %0, 128;\n add.u32 a1, %1, 8;\n add.u32 a2, %1, 16;\n add.u32 a3, %1, 24;\n"
+        " add.u32 a4, %1, 64;\n add.u32 a5, %1, 72;\n add.u32 a6, %1, 80;\n add.u32 a7, %1, 88;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %11, pf;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], %3, %11, pa;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], %4, %11, pa;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], %5, %11, pa;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [d1], [a4], %6, %11, pf;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [d1], [a5], %7, %11, pa;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [d1], [a6], %8, %11, pa;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [d1], [a7], %9, %11, pa;\n}\n" ::"r"(d),
+        "r"(a), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]),
+        "l"(b[7]), "r"(acc), "r"(idesc)
         : "memory");
 }
 
@@ -499,30 +527,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------ MMA issuer ------------------------------
+        // The pipe idles for every instruction this thread runs between two
+        // products, so descriptors come from per-CTA bases plus constant offsets
+        // (shared-memory addresses stay below 256 KiB: adding to the 14-bit start
+        // field never carries), each tile's products go out in two bursts of
+        // eight, and each burst has one wait-and-fence in front of it.  The abort
+        // flag is read once per unit; a wait that can no longer be satisfied
+        // ends on its time limit.
         if (lane == 0) {
             uint32_t kt = 0;
             bool ok = true;
+            uint64_t qd[8];  // Q tile (one buffer): K-major, 128-byte swizzle
+            {
+                const uint64_t q0 = sdesc(base + kQOff, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    qd[kk] = q0 + uint64_t(((kk >> 2) * kSub + (kk & 3) * 32) >> 4);
+            }
+            static_assert(kQBufs == 1, "the Q descriptors assume a single Q buffer");
+            const uint64_t kd_base = sdesc(base + kKOff, 16, 1024);
+            const uint64_t vd_base = sdesc(base + kVOff, kKeys * 128, 1024);
             // O_h += P_h V_h over the 64 keys of half h, for both halves; P_h is
             // bf16 in TMEM over the first 32 columns of its scores.  The first
             // product of unit k waits until unit k - 1's epilogue has read O.
             auto pv = [&](uint32_t g, int j, uint32_t k) -> bool {
-                const uint32_t vs = base + kVOff + (g % kVStages) * kKBytes;
                 const uint32_t b = g & 1;
-                if (!mbar_wait(&bars[B_V_FULL + g % kVStages], (g / kVStages) & 1, p.err)) return false;
-                for (int h = 0; h < 2; ++h) {
-                    if (!mbar_wait(&bars[B_P_FULL + 2 * h + b], (g >> 1) & 1, p.err)) return false;
-                    if (j == 0 && h == 0 && !mbar_wait(&bars[B_O_EMPTY], (k & 1) ^ 1, p.err))
-                        return false;
-                    tc_after();
+                const uint32_t vs = g % kVStages;
+                if (!mbar_wait(&bars[B_V_FULL + vs], (g / kVStages) & 1, p.err) ||
+                    !mbar_wait(&bars[B_P_FULL + b], (g >> 1) & 1, p.err) ||
+                    !mbar_wait(&bars[B_P_FULL + 2 + b], (g >> 1) & 1, p.err) ||
+                    (j == 0 && !mbar_wait(&bars[B_O_EMPTY], (k & 1) ^ 1, p.err)))
+                    return false;
+                uint64_t vd[8];
+                const uint64_t v0 = vd_base + uint64_t(vs * (kKBytes >> 4));
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t a = tmem + b * kKeys + h * 64 + kk * 8;
-                        const uint64_t bd = sdesc(vs + (h * 4 + kk) * 16 * 128, kKeys * 128, 1024);
-                        umma_ts(tmem + kOCol + h * 128, a, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    umma_commit(&bars[B_O_DONE + 2 * h + b]);
-                }
-                umma_commit(&bars[B_V_EMPTY + g % kVStages]);
+                for (int i = 0; i < 8; ++i) vd[i] = v0 + uint64_t((i * 16 * 128) >> 4);
+                tc_after();
+                umma_ts8(tmem + kOCol, tmem + b * kKeys, vd, kIdescPV, j > 0 ? 1u : 0u);
+                umma_commit(&bars[B_O_DONE + b]);
+                umma_commit(&bars[B_O_DONE + 2 + b]);
+                umma_commit(&bars[B_V_EMPTY + vs]);
                 return true;
             };
             // the P V of the previous key tile is issued after the next Q K^T, so the
@@ -535,31 +579,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int u = unit_read(bars, unit_ring, k, p.err, ok, x);
                 mbar_arrive(&bars[B_U_EMPTY + k % kUnitSlots]);
                 if (u < 0 || !ok || *abort_flag) break;
-                const uint32_t qb = k % kQBufs;
-                ok = mbar_wait(&bars[B_Q_FULL + qb], (k / kQBufs) & 1, p.err) && !*abort_flag;
+                ok = mbar_wait(&bars[B_Q_FULL], k & 1, p.err);
                 if (!ok) break;
-                tc_after();
-                const uint32_t q_addr = base + kQOff + qb * kQBytes;
-                for (int j = 0; j < x.n_tiles && ok; ++j) {
+                for (int j = 0; j < x.n_tiles; ++j) {
                     const uint32_t g = kt + j;
+                    const uint32_t ks = g % kKStages;
+                    uint64_t kd[8];
+                    const uint64_t k0 = kd_base + uint64_t(ks * (kKBytes >> 4));
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        kd[kk] = k0 + uint64_t(((kk >> 2) * (kKeys * 128) + (kk & 3) * 32) >> 4);
                     // S/P buffer g & 1 last held P(g - 2), whose P V was issued before
                     // this product: tensor-core instructions run in issue order
-                    ok = mbar_wait(&bars[B_K_FULL + g % kKStages], (g / kKStages) & 1, p.err) &&
-                         !*abort_flag;
+                    ok = mbar_wait(&bars[B_K_FULL + ks], (g / kKStages) & 1, p.err);
                     if (!ok) break;
                     tc_after();
-                    const uint32_t ks = base + kKOff + (g % kKStages) * kKBytes;
-#pragma unroll
-                    for (int kk = 0; kk < kDim / 16; ++kk) {
-                        const uint64_t a = sdesc(q_addr + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
-                        const uint64_t b = sdesc(ks + (kk >> 2) * (kKeys * 128) + (kk & 3) * 32, 16,
-                                                 1024);
-                        umma(tmem + (g & 1) * kKeys, a, b, kIdescQK, kk > 0 ? 1u : 0u);
-                    }
+                    umma_ss8(tmem + (g & 1) * kKeys, qd, kd, kIdescQK);
                     umma_commit(&bars[B_S_FULL + (g & 1)]);
-                    umma_commit(&bars[B_K_EMPTY + g % kKStages]);
-                    if (j == x.n_tiles - 1) umma_commit(&bars[B_Q_EMPTY + qb]);
-                    if (pending) ok = pv(pend_g, pend_j, pend_k) && !*abort_flag;
+                    umma_commit(&bars[B_K_EMPTY + ks]);
+                    if (j == x.n_tiles - 1) umma_commit(&bars[B_Q_EMPTY]);
+                    if (pending && !pv(pend_g, pend_j, pend_k)) {
+                        ok = false;
+                        break;
+                    }
                     pending = true;
                     pend_g = g;
                     pend_j = j;
@@ -567,8 +609,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // the unit's last P V now: its epilogue waits for it, and the next
                 // unit's first Q K^T would wait for that unit's Q tile anyway
-                if (ok && pending) ok = pv(pend_g, pend_j, pend_k) && !*abort_flag;
+                if (ok && pending) ok = pv(pend_g, pend_j, pend_k);
                 pending = false;
+                if (!ok) break;
                 kt += x.n_tiles;
             }
             if (!ok) *abort_flag = 1;
