@@ -64,6 +64,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
     __shared__ unsigned long long warp_tok[32], warp_pairs[32];
     unsigned long long my_tok = 0, my_pairs = 0;   // this thread's work estimate
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // the kernels that consume the plan may launch now; each waits for this
+    // grid to complete before it reads the plan
+    pdl_launch_dependents();
     if (tid == 0) {
         carry_d = 0;
         carry_p = 0;
@@ -266,6 +269,7 @@ struct SplitParams {
     int32_t num_kv_heads;
     int32_t num_q_heads;
     int32_t max_splits;
+    int32_t wait_plan;   // launched right behind the planner: wait for its work list
     float scale_log2;
     int* err;
 };
@@ -320,6 +324,10 @@ __global__ void __launch_bounds__(SplitCfg<T, D, G>::kThreads)
         fence_mbar_init();
     }
     __syncthreads();
+    // behind the planner (programmatic launch): its work list must be complete
+    // before anything below reads it; the merge kernel may launch now
+    if (p.wait_plan) pdl_wait_prerequisites();
+    pdl_launch_dependents();
 
     const int Hkv = p.num_kv_heads, Hq = p.num_q_heads;
     const int n_units = p.n_items[0] * Hkv;
@@ -508,8 +516,9 @@ __global__ void __launch_bounds__(SplitCfg<T, D, G>::kThreads)
                 static_cast<T*>(p.out)[(size_t(qrow) * Hq + h) * D + d] = Elem<T>::store_val(O / L);
             } else {
                 const size_t slot = (size_t(seq) * Hq + h) * p.max_splits + split;
-                p.part_o[slot * D + d] = O;
-                if (d == 0) p.part_ml[slot] = make_float2(M, L);
+                const uint64_t keep = l2_evict_last_policy();
+                st_keep(p.part_o + slot * D + d, O, keep);
+                if (d == 0) st_keep(p.part_ml + slot, make_float2(M, L), keep);
             }
         }
         consumer_sync(C::kWarps * 32);
@@ -519,8 +528,14 @@ __global__ void __launch_bounds__(SplitCfg<T, D, G>::kThreads)
 }
 
 // ---------------------------------------------------------------------------
-// Merge kernel: one warp per (sequence, query head) with more than one split.
+// Merge kernel: one warp per (sequence, KV head) group whose row has more than
+// one split; for each of the group's G query heads
 //   M = max_k m_k,  L = sum_k l_k 2^(m_k - M),  out = sum_k O_k 2^(m_k - M) / L
+// It is launched behind the split kernel with programmatic dependent launch,
+// so it is resident when the split kernel ends and only waits for it.  Lane k
+// holds the (m, l) of split k (32 splits per pass) for every head, and all of
+// a pass's O rows are requested before they are used, so their latencies
+// overlap.  Splits are summed in index order.
 // ---------------------------------------------------------------------------
 struct MergeParams {
     void* out;
@@ -534,13 +549,15 @@ struct MergeParams {
     int32_t max_context_len;
 };
 
-template <typename T, int D>
+template <typename T, int D, int G>
 __global__ void __launch_bounds__(128) decode_merge_kernel(MergeParams p) {
+    pdl_wait_prerequisites();   // the split kernel's partials
     constexpr int DPL = D / 32;
     const int lane = threadIdx.x & 31;
     const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
-    if (wid >= p.num_seqs * p.num_q_heads) return;
-    const int seq = wid / p.num_q_heads, h = wid % p.num_q_heads;
+    const int Hkv = p.num_q_heads / G;
+    if (wid >= p.num_seqs * Hkv) return;
+    const int seq = wid / Hkv, kvh = wid % Hkv;
     int qrow = seq;
     if (p.query_start_loc) {
         qrow = p.query_start_loc[seq];
@@ -550,32 +567,69 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(MergeParams p) {
     if (ctx < 1 || ctx > p.max_context_len) return;          // flagged by the planner
     const int n = (ctx + kSplitTokens - 1) / kSplitTokens;
     if (n <= 1) return;                                     // written by the split kernel
-    const size_t base = (size_t(seq) * p.num_q_heads + h) * p.max_splits;
-    float M = -INFINITY;
-    for (int k = lane; k < n; k += 32) M = fmaxf(M, p.part_ml[base + k].x);
+    // slots of head j, split k: base + j * max_splits + k
+    const size_t base = (size_t(seq) * p.num_q_heads + size_t(kvh) * G) * p.max_splits;
+    float M[G];
 #pragma unroll
-    for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-    float L = 0.f;
-    for (int k = lane; k < n; k += 32) {
-        const float2 ml = p.part_ml[base + k];
-        L = fmaf(ml.y, exp2f(ml.x - M), L);
+    for (int j = 0; j < G; ++j) M[j] = -INFINITY;
+    for (int k = lane; k < n; k += 32)
+#pragma unroll
+        for (int j = 0; j < G; ++j) M[j] = fmaxf(M[j], p.part_ml[base + size_t(j) * p.max_splits + k].x);
+#pragma unroll
+    for (int j = 0; j < G; ++j)
+#pragma unroll
+        for (int off = 16; off; off >>= 1) M[j] = fmaxf(M[j], __shfl_xor_sync(kFull, M[j], off));
+    float L[G], acc[G][DPL];
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+        L[j] = 0.f;
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) acc[j][d] = 0.f;
+    }
+    for (int k0 = 0; k0 < n; k0 += 32) {
+        float w[G];
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            w[j] = 0.f;
+            if (k0 + lane < n) {
+                const float2 ml = __ldcs(p.part_ml + base + size_t(j) * p.max_splits + k0 + lane);
+                w[j] = exp2f(ml.x - M[j]);
+                L[j] = fmaf(ml.y, w[j], L[j]);
+            }
+        }
+        const int cnt = min(32, n - k0);
+#pragma unroll(G >= 8 ? 1 : 2)
+        for (int i = 0; i < cnt; ++i) {
+            float ov[G][DPL];
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                // read once: let the kept lines go
+                const float* src = p.part_o + (base + size_t(j) * p.max_splits + k0 + i) * D + lane * DPL;
+                if constexpr (DPL == 4) {
+                    const float4 v = __ldcs(reinterpret_cast<const float4*>(src));
+                    ov[j][0] = v.x; ov[j][1] = v.y; ov[j][2] = v.z; ov[j][3] = v.w;
+                } else {
+                    const float2 v = __ldcs(reinterpret_cast<const float2*>(src));
+                    ov[j][0] = v.x; ov[j][1] = v.y;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                const float wi = __shfl_sync(kFull, w[j], i);
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) acc[j][d] = fmaf(wi, ov[j][d], acc[j][d]);
+            }
+        }
     }
 #pragma unroll
-    for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
-    float acc[DPL];
+    for (int j = 0; j < G; ++j) {
 #pragma unroll
-    for (int d = 0; d < DPL; ++d) acc[d] = 0.f;
-    for (int k = 0; k < n; ++k) {
-        const float w = exp2f(p.part_ml[base + k].x - M);
-        float ov[DPL];
-        Elem<float>::template load<DPL>(p.part_o + (base + k) * D + lane * DPL, ov);
+        for (int off = 16; off; off >>= 1) L[j] += __shfl_xor_sync(kFull, L[j], off);
+        const float inv = 1.f / L[j];
+        T* o = static_cast<T*>(p.out) + (size_t(qrow) * p.num_q_heads + kvh * G + j) * D + lane * DPL;
 #pragma unroll
-        for (int d = 0; d < DPL; ++d) acc[d] = fmaf(w, ov[d], acc[d]);
+        for (int d = 0; d < DPL; ++d) o[d] = Elem<T>::store_val(acc[j][d] * inv);
     }
-    const float inv = 1.f / L;
-    T* o = static_cast<T*>(p.out) + (size_t(qrow) * p.num_q_heads + h) * D + lane * DPL;
-#pragma unroll
-    for (int d = 0; d < DPL; ++d) o[d] = Elem<T>::store_val(acc[d] * inv);
 }
 
 // ---------------------------------------------------------------------------
@@ -622,6 +676,7 @@ int launch_split_t(const AttnArgs& a) {
     p.num_kv_heads = a.desc->num_kv_heads;
     p.num_q_heads = a.desc->num_q_heads;
     p.max_splits = a.ws.max_splits;
+    p.wait_plan = a.pdl ? 0 : 1;   // behind a prefill kernel, the plan is complete
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.err = a.err;
     cudaLaunchConfig_t cfg = {};
@@ -633,7 +688,7 @@ int launch_split_t(const AttnArgs& a) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = a.pdl ? 1 : 0;
+    cfg.numAttrs = 1;
     return cuda_status(cudaLaunchKernelEx(&cfg, kern, p));
 }
 
@@ -648,7 +703,7 @@ int launch_split_d(const AttnArgs& a, int g) {
     }
 }
 
-template <typename T, int D>
+template <typename T, int D, int G>
 int launch_merge_t(const AttnArgs& a) {
     MergeParams p;
     p.out = a.out;
@@ -660,11 +715,30 @@ int launch_merge_t(const AttnArgs& a) {
     p.num_q_heads = a.desc->num_q_heads;
     p.max_splits = a.ws.max_splits;
     p.max_context_len = a.max_context_len;
-    const int64_t warps = int64_t(a.num_seqs) * a.desc->num_q_heads;
+    const int64_t warps = int64_t(a.num_seqs) * a.desc->num_kv_heads;
     const int64_t blocks = (warps + 3) / 4;
     if (blocks < 1) return PKV_OK;
-    decode_merge_kernel<T, D><<<unsigned(blocks), 128, 0, a.stream>>>(p);
-    return cuda_status(cudaGetLastError());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(blocks));
+    cfg.blockDim = dim3(128);
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, decode_merge_kernel<T, D, G>, p));
+}
+
+template <typename T, int D>
+int launch_merge_d(const AttnArgs& a) {
+    switch (a.desc->num_q_heads / a.desc->num_kv_heads) {
+        case 1: return launch_merge_t<T, D, 1>(a);
+        case 2: return launch_merge_t<T, D, 2>(a);
+        case 4: return launch_merge_t<T, D, 4>(a);
+        case 8: return launch_merge_t<T, D, 8>(a);
+        default: return PKV_ERR_UNSUPPORTED;
+    }
 }
 
 }  // namespace
@@ -685,9 +759,9 @@ int launch_decode_merge(const AttnArgs& a) {
     if (a.ws.max_splits <= 1) return PKV_OK;
     const bool bf = a.desc->dtype == PKV_BF16;
     if (a.desc->head_dim == 128)
-        return bf ? launch_merge_t<__nv_bfloat16, 128>(a) : launch_merge_t<float, 128>(a);
+        return bf ? launch_merge_d<__nv_bfloat16, 128>(a) : launch_merge_d<float, 128>(a);
     if (a.desc->head_dim == 64)
-        return bf ? launch_merge_t<__nv_bfloat16, 64>(a) : launch_merge_t<float, 64>(a);
+        return bf ? launch_merge_d<__nv_bfloat16, 64>(a) : launch_merge_d<float, 64>(a);
     return PKV_ERR_UNSUPPORTED;
 }
 

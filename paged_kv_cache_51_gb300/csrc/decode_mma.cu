@@ -47,6 +47,7 @@ struct MmaParams {
     int32_t num_kv_heads;
     int32_t num_q_heads;
     int32_t max_splits;
+    int32_t wait_plan;   // launched right behind the planner: wait for its work list
     float scale_log2;
     int* err;
 };
@@ -153,6 +154,10 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads, MmaCfg<D, G>::kMinBloc
         fence_mbar_init();
     }
     __syncthreads();
+    // behind the planner (programmatic launch): its work list must be complete
+    // before anything below reads it; the merge kernel may launch now
+    if (p.wait_plan) pdl_wait_prerequisites();
+    pdl_launch_dependents();
 
     const int Hkv = p.num_kv_heads, Hq = p.num_q_heads;
     const int n_units = p.n_items[0] * Hkv;
@@ -368,8 +373,9 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads, MmaCfg<D, G>::kMinBloc
                 p.out[(size_t(qrow) * Hq + h) * D + d] = __float2bfloat16_rn(O / L);
             } else {
                 const size_t slot = (size_t(seq) * Hq + h) * p.max_splits + split;
-                p.part_o[slot * D + d] = O;
-                if (d == 0) p.part_ml[slot] = make_float2(M, L);
+                const uint64_t keep = l2_evict_last_policy();
+                st_keep(p.part_o + slot * D + d, O, keep);
+                if (d == 0) st_keep(p.part_ml + slot, make_float2(M, L), keep);
             }
         }
         asm volatile("bar.sync 1, %0;" ::"r"(C::kWarps * 32) : "memory");
@@ -407,6 +413,7 @@ int launch_t(const AttnArgs& a) {
     p.num_kv_heads = a.desc->num_kv_heads;
     p.num_q_heads = a.desc->num_q_heads;
     p.max_splits = a.ws.max_splits;
+    p.wait_plan = a.pdl ? 0 : 1;   // behind a prefill kernel, the plan is complete
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.err = a.err;
     cudaLaunchConfig_t cfg = {};
@@ -418,7 +425,7 @@ int launch_t(const AttnArgs& a) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = a.pdl ? 1 : 0;
+    cfg.numAttrs = 1;
     return cuda_status(cudaLaunchKernelEx(&cfg, kern, mk, mv, p));
 }
 

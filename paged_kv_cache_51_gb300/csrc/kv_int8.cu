@@ -246,6 +246,10 @@ __global__ void __launch_bounds__(I8Cfg<D, G>::kThreads) decode_split_int8_kerne
         fence_mbar_init();
     }
     __syncthreads();
+    // launched right behind the planner (programmatic launch): its work list must
+    // be complete before anything below reads it; the merge kernel may launch now
+    pdl_wait_prerequisites();
+    pdl_launch_dependents();
     const int Hkv = p.num_kv_heads, Hq = p.num_q_heads;
     const int n_units = p.n_items[0] * Hkv;
     constexpr int kSplitBlocks = kSplitTokens / kBlockTokens;
@@ -507,8 +511,9 @@ __global__ void __launch_bounds__(I8Cfg<D, G>::kThreads) decode_split_int8_kerne
                 p.out[(size_t(seq) * Hq + h) * D + d] = __float2bfloat16_rn(O / L);
             } else {
                 const size_t slot = (size_t(seq) * Hq + h) * p.max_splits + split;
-                p.part_o[slot * D + d] = O;
-                if (d == 0) p.part_ml[slot] = make_float2(M, L);
+                const uint64_t keep = l2_evict_last_policy();
+                st_keep(p.part_o + slot * D + d, O, keep);
+                if (d == 0) st_keep(p.part_ml + slot, make_float2(M, L), keep);
             }
         }
         consumer_sync(C::kWarps * 32);
@@ -548,8 +553,17 @@ int launch_i8(const AttnArgs& a, const int8_t* kc, const int8_t* vc, const float
     p.max_splits = a.ws.max_splits;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.err = a.err;
-    kern<<<unsigned(grid), C::kThreads, C::kSmem, a.stream>>>(p);
-    return cuda_status(cudaGetLastError());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, kern, p));
 }
 
 template <int D>

@@ -161,6 +161,23 @@ __device__ __forceinline__ void pdl_wait_prerequisites() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// ---- L2 residency of split partials -------------------------------------------
+// Split partials are written while the whole KV stream passes through L2; stored
+// with an evict-last policy they are still there when the merge kernel reads them.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void st_keep(float* p, float v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_keep(float2* p, float2 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;" ::"l"(p), "f"(v.x), "f"(v.y),
+                 "l"(pol)
+                 : "memory");
+}
+
 // ---- element conversion -------------------------------------------------------
 template <typename T>
 struct Elem;

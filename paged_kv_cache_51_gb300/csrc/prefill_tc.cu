@@ -346,11 +346,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v,
                    const __grid_constant__ CUtensorMap tmap_q, PrefillParams p) {
+    // Launched right behind the planner (programmatic launch): wait for the plan.
     // The planner gives the prefill chunks only as many SMs as their share of
     // the batch's work; the other CTAs leave at once, and the decode kernel that
-    // follows in the stream may start right away on the SMs they free.
-    const int active = min(p.counters[2], int(gridDim.x));
+    // follows in the stream may start right away on the SMs they free (it reads
+    // the plan without waiting, so the trigger comes after this grid's wait).
+    pdl_wait_prerequisites();
     pdl_launch_dependents();
+    const int active = min(p.counters[2], int(gridDim.x));
     if (int(blockIdx.x) >= active) return;
 
     extern __shared__ unsigned char smem_raw[];
@@ -854,8 +857,17 @@ int launch_prefill(const AttnArgs& a) {
     const int64_t bound = int64_t(a.ws.max_prefill_items) * d->num_kv_heads;
     const int64_t grid = std::min<int64_t>(num_sms(), bound);
     if (grid < 1) return PKV_OK;
-    prefill_kernel<<<unsigned(grid), kThreads, kSmemBytes, a.stream>>>(mk, mv, mq, p);
-    return cuda_status(cudaGetLastError());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, prefill_kernel, mk, mv, mq, p));
 }
 
 }  // namespace pkv
