@@ -31,16 +31,22 @@
 //              too: the softmax of the next key tile runs while the previous
 //              P V product is still executing.  O is rescaled only when the
 //              running max grows by more than 2^8 (the one case that waits for
-//              the previous P V).  The epilogue merges the halves.
+//              the previous P V).  The epilogue merges the halves; a full
+//              unit's bf16 output tile is staged in the unit's Q buffer (the
+//              TMA box layout) and leaves by two TMA tensor stores, so the warps
+//              go on to the next unit at once (128 rows of scattered 16-byte
+//              global stores kept the load/store unit busy for ~3000 cycles).
+//              A partial unit writes its valid rows directly.
 //   warp 8     takes work units from a ticket (the planner orders them longest
 //              first) and publishes them to the other roles; TMA producer for
-//              the unit's Q tile and for K: blocks of each key tile into a
-//              3-stage K ring; a K stage is released as soon as its Q K^T
-//              product is done
+//              the unit's Q tile (two buffers) and for K: blocks of each key
+//              tile into a 2-stage K ring; a K stage is released as soon as its
+//              Q K^T product is done
 //   warp 9     TMA producer for V: a 2-stage V ring released by the P V product
-//   warp 10    TMEM owner and MMA issuer (one thread issues tcgen05.mma); the
-//              P V of a key tile is issued after the next tile's Q K^T, so the
-//              tensor pipe has work while the softmax runs
+//   warp 10    TMEM owner and MMA issuer (one thread issues tcgen05.mma): a step
+//              issues P V of key tile q - 2 and Q K^T of key tile q as bursts
+//              behind one group of waits, so the tensor pipe works on those
+//              while the softmax runs on tile s - 1 (across units as well)
 // Every wait is bounded; on a timeout the kernel records an error, stops
 // issuing work, drains its copies and MMAs and frees TMEM before it returns.
 #include <cuda.h>
@@ -61,11 +67,12 @@ constexpr int kDim = 128;                    // head dim
 constexpr int kKeys = 128;                   // keys per key tile
 constexpr int kBlkPerTile = kKeys / kBlockTokens;  // 8 cache blocks
 // Ring depths.  A key tile's TMA copies take about a microsecond to land, about
-// one tile period: K runs 3 deep, V (needed one tile later) 2 deep, Q single
-// (the next unit's Q loads once the current unit's last Q K^T is done).
-constexpr int kKStages = 3;
+// one tile period: K and V run 2 deep.  Q is double-buffered so the next unit's
+// Q is in place before its first Q K^T; a finished unit's Q buffer then holds
+// its output tile until the TMA stores have read it.
+constexpr int kKStages = 2;
 constexpr int kVStages = 2;
-constexpr int kQBufs = 1;
+constexpr int kQBufs = 2;
 constexpr int kSub = kRows * 128;            // one 64-column half of a 128-row operand (16 KiB)
 constexpr int kQBytes = 2 * kSub;            // one Q tile: 2 halves (dims 0-63, 64-127)
 constexpr int kKBytes = 2 * kKeys * 128;     // one K or V tile (2 halves of 128 key rows x 128 B)
@@ -92,10 +99,11 @@ enum {
     B_V_FULL = B_K_EMPTY + kKStages,
     B_V_EMPTY = B_V_FULL + kVStages,
     B_S_FULL = B_V_EMPTY + kVStages,
-    B_P_FULL = B_S_FULL + 2,        // [key half][S/P buffer]
-    B_O_DONE = B_P_FULL + 4,        // [key half][S/P buffer]: that buffer's P V has completed
-    B_Q_FULL = B_O_DONE + 4,        // [Q buffer]
-    B_Q_EMPTY = B_Q_FULL + kQBufs,  // [Q buffer]: the unit's last Q K^T has completed
+    B_P_FULL = B_S_FULL + 2,        // [S/P buffer]: every softmax warp has written its P
+    B_O_DONE = B_P_FULL + 2,        // [S/P buffer]: that buffer's P V has completed
+    B_Q_FULL = B_O_DONE + 2,        // [Q buffer]
+    B_Q_EMPTY = B_Q_FULL + kQBufs,  // [Q buffer]: every softmax warp has finished its unit's
+                                    // epilogue (output staged there or written directly)
     B_U_READY = B_Q_EMPTY + kQBufs, // [unit slot]
     B_U_EMPTY = B_U_READY + 4,      // [unit slot]
     B_O_EMPTY = B_U_EMPTY + 4,
@@ -291,6 +299,48 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// A full unit's output tile leaves shared memory by TMA tensor stores (one per
+// 64-dim half), so the softmax warps do not wait for 128 rows of scattered
+// global stores.  The issuing thread tracks the stores as one bulk group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y,
+                                             int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(z), "r"(src)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// the source of every committed store has been read (the staging tile may be reused)
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// every committed store has completed
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// max(a, b, c) in one instruction (three-input form of max.f32)
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Whether the phase with the given parity has completed, without waiting.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Block ids of a unit's key tiles, fetched 4 tiles (32 blocks, one per lane) at
 // a time and one group ahead, so a producer never waits on the block table.
 struct BlockIds {
@@ -345,7 +395,8 @@ __device__ __forceinline__ int unit_read(uint64_t* bars, const UnitSlot* ring, u
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v,
-                   const __grid_constant__ CUtensorMap tmap_q, PrefillParams p) {
+                   const __grid_constant__ CUtensorMap tmap_q,
+                   const __grid_constant__ CUtensorMap tmap_o, PrefillParams p) {
     // Launched right behind the planner (programmatic launch): wait for the plan.
     // The planner gives the prefill chunks only as many SMs as their share of
     // the batch's work; the other CTAs leave at once, and the decode kernel that
@@ -383,11 +434,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < kQBufs; ++s) {
             mbar_init(&bars[B_Q_FULL + s], 1);
-            mbar_init(&bars[B_Q_EMPTY + s], 1);
+            mbar_init(&bars[B_Q_EMPTY + s], kSoftWarps);
         }
         for (int s = 0; s < 2; ++s) mbar_init(&bars[B_S_FULL + s], 1);
-        for (int s = 0; s < 4; ++s) {
-            mbar_init(&bars[B_P_FULL + s], kSoftWarps / 2);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars[B_P_FULL + s], kSoftWarps);
             mbar_init(&bars[B_O_DONE + s], 1);
         }
         for (int s = 0; s < kUnitSlots; ++s) {
@@ -414,11 +465,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == kKProducerWarp) {
-        // ------- unit tickets, Q tiles and the K ring (one warp) -------
+        // ------- unit tickets, Q tiles, output stores and the K ring (one warp) -------
+        // Q buffer b holds unit k's Q and then, once its epilogue has staged it,
+        // unit k's output tile.  Before loading unit k + 2's Q there, this warp
+        // sends the staged tile out by TMA and waits until it has been read; the
+        // last two units' tiles go out after the loop.
         uint32_t kt = 0;
         bool ok = true;
+        bool out_staged[kQBufs] = {false, false};   // per Q buffer: its last unit was staged
+        int out_y[kQBufs] = {0, 0}, out_z[kQBufs] = {0, 0};
+        uint32_t k = 0;
+        auto send_output = [&](int qb) {
+            if (lane == 0 && out_staged[qb]) {
+                const uint32_t src = base + kQOff + qb * kQBytes;
+                tma_store_3d(&tmap_o, src, 0, out_y[qb], out_z[qb]);
+                tma_store_3d(&tmap_o, src + kSub, 64, out_y[qb], out_z[qb]);
+                bulk_commit();
+                bulk_wait_read();   // the buffer may take the next Q after this
+            }
+            out_staged[qb] = false;
+        };
         int next = lane == 0 ? atomicAdd(p.ticket, 1) : 0;
-        for (uint32_t k = 0;; ++k) {
+        for (;; ++k) {
             const int slot = k % kUnitSlots;
             ok = ok && __all_sync(0xffffffffu, mbar_wait(&bars[B_U_EMPTY + slot],
                                                          ((k / kUnitSlots) & 1) ^ 1, p.err));
@@ -436,11 +504,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&bars[B_U_READY + slot]);
             }
             if (u < 0) break;
-            // Q tile of the unit (two 64-dim halves)
+            // Q tile of the unit (two 64-dim halves); the buffer's previous unit
+            // has staged its output (or written it directly) by now
             const int qb = k % kQBufs;
             ok = __all_sync(0xffffffffu,
                             mbar_wait(&bars[B_Q_EMPTY + qb], ((k / kQBufs) & 1) ^ 1, p.err));
             if (!ok) break;
+            send_output(qb);
+            out_staged[qb] = x.nt == p.tokens_per_tile;
+            out_y[qb] = x.kvh * p.group;
+            out_z[qb] = x.q0 + x.t0;
             if (lane == 0) {
                 mbar_arrive_expect_tx(&bars[B_Q_FULL + qb], 2 * kSub);
                 const uint32_t qd = base + kQOff + qb * kQBytes;
@@ -477,13 +550,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
         }
+        // the last units' output tiles (k units were loaded)
+        for (uint32_t kk = k >= kQBufs ? k - kQBufs : 0; ok && kk < k; ++kk) {
+            const int qb = kk % kQBufs;
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&bars[B_Q_EMPTY + qb], (kk / kQBufs) & 1, p.err));
+            if (ok) send_output(qb);
+        }
         if (!ok) *abort_flag = 1;
-        // never leave with copies in flight: wait for the last fill of each stage
+        // never leave with copies in flight: wait for the last fill of each stage,
+        // and for the output stores to complete
         if (lane == 0) {
             for (int k = 0; k < kKStages && uint32_t(k) < kt; ++k) {
                 const uint32_t last = kt - 1 - k;
                 mbar_wait(&bars[B_K_FULL + last % kKStages], (last / kKStages) & 1, p.err);
             }
+            bulk_wait_all();
         }
     } else if (warp == kVProducerWarp) {
         // ------------------------------ V ring ------------------------------
@@ -530,92 +612,119 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------ MMA issuer ------------------------------
-        // The pipe idles for every instruction this thread runs between two
-        // products, so descriptors come from per-CTA bases plus constant offsets
-        // (shared-memory addresses stay below 256 KiB: adding to the 14-bit start
-        // field never carries), each tile's products go out in two bursts of
-        // eight, and each burst has one wait-and-fence in front of it.  The abort
+        // Key tiles are numbered over the CTA's whole sequence of units.  A step
+        // issues P V of tile q - 2 and Q K^T of tile q: S/P buffer q & 1 held
+        // P(q - 2), which the P V reads before the Q K^T overwrites it
+        // (tensor-core instructions run in issue order), while the softmax works
+        // on S(q - 1); after the last Q K^T the remaining P V go out alone.  The pipe idles for every instruction this thread runs
+        // between two products, so the step's waits come first, then one fence
+        // and the products as bursts of eight; descriptors come from per-CTA
+        // bases plus constant offsets (shared-memory addresses stay below
+        // 256 KiB: adding to the 14-bit start field never carries).  When the
+        // Q K^T side is not ready yet, the P V goes out first: the next unit's Q
+        // may be waiting for the epilogue that this P V completes.  The abort
         // flag is read once per unit; a wait that can no longer be satisfied
         // ends on its time limit.
         if (lane == 0) {
-            uint32_t kt = 0;
             bool ok = true;
-            uint64_t qd[8];  // Q tile (one buffer): K-major, 128-byte swizzle
+            uint64_t qd[8];  // Q buffer 0: K-major, 128-byte swizzle
             {
                 const uint64_t q0 = sdesc(base + kQOff, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     qd[kk] = q0 + uint64_t(((kk >> 2) * kSub + (kk & 3) * 32) >> 4);
             }
-            static_assert(kQBufs == 1, "the Q descriptors assume a single Q buffer");
             const uint64_t kd_base = sdesc(base + kKOff, 16, 1024);
             const uint64_t vd_base = sdesc(base + kVOff, kKeys * 128, 1024);
-            // O_h += P_h V_h over the 64 keys of half h, for both halves; P_h is
-            // bf16 in TMEM over the first 32 columns of its scores.  The first
-            // product of unit k waits until unit k - 1's epilogue has read O.
-            auto pv = [&](uint32_t g, int j, uint32_t k) -> bool {
-                const uint32_t b = g & 1;
-                const uint32_t vs = g % kVStages;
-                if (!mbar_wait(&bars[B_V_FULL + vs], (g / kVStages) & 1, p.err) ||
-                    !mbar_wait(&bars[B_P_FULL + b], (g >> 1) & 1, p.err) ||
-                    !mbar_wait(&bars[B_P_FULL + 2 + b], (g >> 1) & 1, p.err) ||
-                    (j == 0 && !mbar_wait(&bars[B_O_EMPTY], (k & 1) ^ 1, p.err)))
-                    return false;
-                uint64_t vd[8];
-                const uint64_t v0 = vd_base + uint64_t(vs * (kKBytes >> 4));
-#pragma unroll
-                for (int i = 0; i < 8; ++i) vd[i] = v0 + uint64_t((i * 16 * 128) >> 4);
-                tc_after();
-                umma_ts8(tmem + kOCol, tmem + b * kKeys, vd, kIdescPV, j > 0 ? 1u : 0u);
-                umma_commit(&bars[B_O_DONE + b]);
-                umma_commit(&bars[B_O_DONE + 2 + b]);
-                umma_commit(&bars[B_V_EMPTY + vs]);
-                return true;
-            };
-            // the P V of the previous key tile is issued after the next Q K^T, so the
-            // tensor pipe has work while the softmax runs (across units as well)
-            bool pending = false;
-            uint32_t pend_g = 0, pend_k = 0;
-            int pend_j = 0;
-            for (uint32_t k = 0;; ++k) {
-                Unit x;
-                const int u = unit_read(bars, unit_ring, k, p.err, ok, x);
-                mbar_arrive(&bars[B_U_EMPTY + k % kUnitSlots]);
-                if (u < 0 || !ok || *abort_flag) break;
-                ok = mbar_wait(&bars[B_Q_FULL], k & 1, p.err);
-                if (!ok) break;
-                for (int j = 0; j < x.n_tiles; ++j) {
-                    const uint32_t g = kt + j;
-                    const uint32_t ks = g % kKStages;
-                    uint64_t kd[8];
-                    const uint64_t k0 = kd_base + uint64_t(ks * (kKBytes >> 4));
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        kd[kk] = k0 + uint64_t(((kk >> 2) * (kKeys * 128) + (kk & 3) * 32) >> 4);
-                    // S/P buffer g & 1 last held P(g - 2), whose P V was issued before
-                    // this product: tensor-core instructions run in issue order
-                    ok = mbar_wait(&bars[B_K_FULL + ks], (g / kKStages) & 1, p.err);
-                    if (!ok) break;
-                    tc_after();
-                    umma_ss8(tmem + (g & 1) * kKeys, qd, kd, kIdescQK);
-                    umma_commit(&bars[B_S_FULL + (g & 1)]);
-                    umma_commit(&bars[B_K_EMPTY + ks]);
-                    if (j == x.n_tiles - 1) umma_commit(&bars[B_Q_EMPTY]);
-                    if (pending && !pv(pend_g, pend_j, pend_k)) {
-                        ok = false;
-                        break;
+            // per tile, bit (tile & 3) (a P V trails its Q K^T by two steps):
+            // whether it is its unit's first tile, and its unit's parity
+            uint32_t first_bits = 0, unit_par_bits = 0;
+            uint32_t k_next = 0;                 // next unit to read
+            uint32_t cur_unit = 0;               // unit of the Q K^T cursor
+            int cur_j = 0, cur_n = 0;            // its next tile, and its tile count
+            bool more = true;                    // units may remain
+            uint32_t n_qk = 0;                   // Q K^T products issued (tiles 0 .. n_qk - 1)
+            uint32_t n_pv = 0;                   // P V products issued
+            for (;;) {
+                if (ok && more && cur_j == cur_n) {
+                    Unit x;
+                    const int u = unit_read(bars, unit_ring, k_next, p.err, ok, x);
+                    mbar_arrive(&bars[B_U_EMPTY + k_next % kUnitSlots]);
+                    if (u < 0 || !ok || *abort_flag) {
+                        more = false;
+                    } else {
+                        cur_unit = k_next++;
+                        cur_j = 0;
+                        cur_n = x.n_tiles;
                     }
-                    pending = true;
-                    pend_g = g;
-                    pend_j = j;
-                    pend_k = k;
                 }
-                // the unit's last P V now: its epilogue waits for it, and the next
-                // unit's first Q K^T would wait for that unit's Q tile anyway
-                if (ok && pending) ok = pv(pend_g, pend_j, pend_k);
-                pending = false;
-                if (!ok) break;
-                kt += x.n_tiles;
+                const bool qk = ok && more && cur_j < cur_n;
+                // P V trails Q K^T by two tiles while products flow; once the
+                // units run out, the remaining ones go out in the next steps
+                const bool pv = ok && n_pv < n_qk && (!qk || n_qk >= n_pv + 2);
+                if (!qk && !pv) break;
+                const uint32_t t = n_pv;         // the P V tile
+                const uint32_t q = n_qk;         // the Q K^T tile
+                const bool t0 = pv && ((first_bits >> (t & 3)) & 1u);
+                const bool q_first = qk && cur_j == 0;
+                const uint32_t qb = cur_unit & 1;
+                // descriptors of both bursts, before any wait
+                uint64_t vd[8], qa[8], kd[8];
+                {
+                    const uint64_t v0 = vd_base + uint64_t((t % kVStages) * (kKBytes >> 4));
+                    const uint64_t k0 = kd_base + uint64_t((q % kKStages) * (kKBytes >> 4));
+                    const uint64_t qoff = uint64_t(qb) * (kQBytes >> 4);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        vd[i] = v0 + uint64_t((i * 16 * 128) >> 4);
+                        qa[i] = qd[i] + qoff;
+                        kd[i] = k0 + uint64_t(((i >> 2) * (kKeys * 128) + (i & 3) * 32) >> 4);
+                    }
+                }
+                if (pv) {
+                    // P of both key halves, V, and (first tile of a unit) the previous
+                    // unit's epilogue has read O
+                    ok = mbar_wait(&bars[B_P_FULL + (t & 1)], (t >> 1) & 1, p.err) &&
+                         mbar_wait(&bars[B_V_FULL + t % kVStages], (t / kVStages) & 1, p.err) &&
+                         (!t0 || mbar_wait(&bars[B_O_EMPTY], ((unit_par_bits >> (t & 3)) & 1u) ^ 1u,
+                                           p.err));
+                    if (!ok) break;
+                }
+                bool pv_out = !pv;
+                if (qk) {
+                    const bool ready = (!q_first || mbar_test(&bars[B_Q_FULL + qb], (cur_unit >> 1) & 1)) &&
+                                       mbar_test(&bars[B_K_FULL + q % kKStages], (q / kKStages) & 1);
+                    if (!ready) {
+                        if (!pv_out) {
+                            tc_after();
+                            umma_ts8(tmem + kOCol, tmem + (t & 1) * kKeys, vd, kIdescPV, t0 ? 0u : 1u);
+                            umma_commit(&bars[B_O_DONE + (t & 1)]);
+                            umma_commit(&bars[B_V_EMPTY + t % kVStages]);
+                            pv_out = true;
+                        }
+                        ok = (!q_first ||
+                              mbar_wait(&bars[B_Q_FULL + qb], (cur_unit >> 1) & 1, p.err)) &&
+                             mbar_wait(&bars[B_K_FULL + q % kKStages], (q / kKStages) & 1, p.err);
+                        if (!ok) break;
+                    }
+                }
+                tc_after();
+                if (!pv_out) {
+                    umma_ts8(tmem + kOCol, tmem + (t & 1) * kKeys, vd, kIdescPV, t0 ? 0u : 1u);
+                    umma_commit(&bars[B_O_DONE + (t & 1)]);
+                    umma_commit(&bars[B_V_EMPTY + t % kVStages]);
+                }
+                if (pv) ++n_pv;
+                if (qk) {
+                    umma_ss8(tmem + (q & 1) * kKeys, qa, kd, kIdescQK);
+                    umma_commit(&bars[B_S_FULL + (q & 1)]);
+                    umma_commit(&bars[B_K_EMPTY + q % kKStages]);
+                    const uint32_t bit = 1u << (q & 3);
+                    first_bits = q_first ? (first_bits | bit) : (first_bits & ~bit);
+                    unit_par_bits = (cur_unit & 1) ? (unit_par_bits | bit) : (unit_par_bits & ~bit);
+                    ++n_qk;
+                    ++cur_j;
+                }
             }
             if (!ok) *abort_flag = 1;
             // wait until every MMA issued here has completed before TMEM is freed
@@ -672,13 +781,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < 64; ++c) s[c] = (key0 + c <= limit) ? s[c] : -INFINITY;
                 }
                 // eight independent partial maxima instead of one 64-long chain
+                // (three-input maxima: half the instructions of a two-input tree)
                 float mx8[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+                for (int i = 0; i < 8; ++i) mx8[i] = max3f(s[i], s[i + 8], s[i + 16]);
 #pragma unroll
-                for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                for (int i = 0; i < 8; ++i) mx8[i] = max3f(mx8[i], s[i + 24], s[i + 32]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = max3f(mx8[i], s[i + 40], s[i + 48]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[i + 56]);
+                const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]),
+                                       fmaxf(mx8[6], mx8[7]));
                 const float m_new = fmaxf(m, mx * p.scale_log2);
                 const bool need = m_new > m + kRescaleThreshold;  // first visible keys included
                 float alpha = 1.f;
@@ -687,26 +801,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m = m_new;
                     l *= alpha;
                 }
-                // P = 2^(s * scale - m) in bf16
+                // P = 2^(s * scale - m) in bf16; the exponent arguments and the row
+                // sum use packed fp32x2 arithmetic (two lanes per instruction)
                 const float neg_m = m == -INFINITY ? 0.f : -m;
+                const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+                const float2 nm2 = make_float2(neg_m, neg_m);
                 uint32_t w[32];
-                float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                  make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                    const float p0 = exp2f(fmaf(s[2 * c], p.scale_log2, neg_m));
-                    const float p1 = exp2f(fmaf(s[2 * c + 1], p.scale_log2, neg_m));
-                    sum8[c & 7] += p0 + p1;
+                    const float2 e = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), sc2, nm2);
+                    const float p0 = exp2f(e.x), p1 = exp2f(e.y);
+                    sum4[c & 3] = __fadd2_rn(sum4[c & 3], make_float2(p0, p1));
                     w[c] = pack_bf16(p0, p1);
                 }
-                l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                     ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+                l += ((sum4[0].x + sum4[0].y) + (sum4[1].x + sum4[1].y)) +
+                     ((sum4[2].x + sum4[2].y) + (sum4[3].x + sum4[3].y));
                 const bool warp_need = __any_sync(0xffffffffu, need);
                 if (j > 0 && warp_need) {
                     // rescale O_h: wait for the previous P V of this half (buffer
                     // (g - 1) & 1; that buffer's older products have completed,
                     // since S(g) is full and was issued after them)
                     const uint32_t gp = g - 1;
-                    ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE + 2 * h + (gp & 1)],
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE + (gp & 1)],
                                                            (gp >> 1) & 1, p.err));
                     if (!ok) break;
                     tc_after();
@@ -749,17 +867,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_st();
                 tc_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[B_P_FULL + 2 * h + (g & 1)]);
+                if (lane == 0) mbar_arrive(&bars[B_P_FULL + (g & 1)]);
             }
             if (!ok) break;
             // ---- epilogue: merge the halves, O / l -> out (this thread: dims 64h..64h+63) ----
             const uint32_t glast = kt + x.n_tiles - 1;
             ok = __all_sync(0xffffffffu,
-                            mbar_wait(&bars[B_O_DONE + (glast & 1)], (glast >> 1) & 1, p.err) &&
-                                mbar_wait(&bars[B_O_DONE + 2 + (glast & 1)], (glast >> 1) & 1,
-                                          p.err));
+                            mbar_wait(&bars[B_O_DONE + (glast & 1)], (glast >> 1) & 1, p.err));
             if (!ok) break;
             tc_after();
+            // A full unit (every row a query) leaves through its own Q buffer, which
+            // its last Q K^T has finished with (that product was issued before
+            // the P V awaited above), and TMA stores; a partial one writes its
+            // valid rows directly.  Either way the buffer is handed back to the Q
+            // producer at the end.
+            const bool staged = x.nt == p.tokens_per_tile;
+            const uint32_t qbuf = k % kQBufs;
             float2* st_set = stat + (k & 1) * 2 * kRows;
             st_set[h * kRows + r] = make_float2(m, l);
             __syncwarp();
@@ -771,32 +894,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float a0 = exp2f(o0.x - M), a1 = exp2f(o1.x - M);
             const float inv = 1.f / (o0.y * a0 + o1.y * a1);
             const float w0 = a0 * inv, w1 = a1 * inv;
-            uint4* dst = reinterpret_cast<uint4*>(
-                p.out + (size_t(x.q0 + t) * p.num_q_heads + x.kvh * G + g_head) * kDim + h * 64);
+            // this thread's 64 output dims (bf16 pairs): chunk c = dims 8c .. 8c + 7
+            uint32_t packed[32];
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) {
                 uint32_t v0[32], v1[32];
                 tmem_ld32(tmem + lane_base + kOCol + h * 64 + c2 * 32, v0);
                 tmem_ld32(tmem + lane_base + kOCol + 128 + h * 64 + c2 * 32, v1);
                 tmem_wait_ld();
-                if (row_valid) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint32_t q4[4];
-#pragma unroll
-                        for (int kq = 0; kq < 4; ++kq) {
-                            const int i0 = e * 8 + 2 * kq;
-                            q4[kq] = pack_bf16(
-                                __uint_as_float(v0[i0]) * w0 + __uint_as_float(v1[i0]) * w1,
-                                __uint_as_float(v0[i0 + 1]) * w0 + __uint_as_float(v1[i0 + 1]) * w1);
-                        }
-                        dst[c2 * 4 + e] = make_uint4(q4[0], q4[1], q4[2], q4[3]);
-                    }
-                }
+                for (int i = 0; i < 16; ++i)
+                    packed[c2 * 16 + i] =
+                        pack_bf16(__uint_as_float(v0[2 * i]) * w0 + __uint_as_float(v1[2 * i]) * w1,
+                                  __uint_as_float(v0[2 * i + 1]) * w0 +
+                                      __uint_as_float(v1[2 * i + 1]) * w1);
             }
+            // O has been read: the next unit's first P V may overwrite it
             tc_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_O_EMPTY]);
+            if (staged) {
+                // row r of half h, 128-byte swizzled like the TMA box of the output map
+                unsigned char* row = smem + kQOff + qbuf * kQBytes + h * kSub + r * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) * 16)) =
+                        make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2],
+                                   packed[4 * c + 3]);
+                fence_async_smem();   // generic-proxy writes, before the TMA reads them
+            } else if (row_valid) {
+                uint4* dst = reinterpret_cast<uint4*>(
+                    p.out + (size_t(x.q0 + t) * p.num_q_heads + x.kvh * G + g_head) * kDim + h * 64);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2],
+                                        packed[4 * c + 3]);
+            }
+            // the unit is done with its Q buffer; a staged tile in it goes out with
+            // the producer's next use of the buffer
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_Q_EMPTY + qbuf]);
             kt += x.n_tiles;
         }
         if (!ok) *abort_flag = 1;
@@ -832,9 +969,11 @@ int launch_prefill(const AttnArgs& a) {
     const pkv_cache_desc* d = a.desc;
     if (!prefill_supported(d)) return PKV_ERR_UNSUPPORTED;
     const int group = d->num_q_heads / d->num_kv_heads;
-    CUtensorMap mk, mv, mq;
+    CUtensorMap mk, mv, mq, mo;
+    // the output has the query's shape: the same box serves the output tile's stores
     if (!make_cache_tensor_map(&mk, a.k_cache, d) || !make_cache_tensor_map(&mv, a.v_cache, d) ||
-        !make_query_tensor_map(&mq, a.q, a.num_query_tokens, d->num_q_heads, group))
+        !make_query_tensor_map(&mq, a.q, a.num_query_tokens, d->num_q_heads, group) ||
+        !make_query_tensor_map(&mo, a.out, a.num_query_tokens, d->num_q_heads, group))
         return PKV_ERR_CUDA;
     PrefillParams p;
     p.out = static_cast<__nv_bfloat16*>(a.out);
@@ -867,7 +1006,7 @@ int launch_prefill(const AttnArgs& a) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cuda_status(cudaLaunchKernelEx(&cfg, prefill_kernel, mk, mv, mq, p));
+    return cuda_status(cudaLaunchKernelEx(&cfg, prefill_kernel, mk, mv, mq, mo, p));
 }
 
 }  // namespace pkv
