@@ -73,6 +73,8 @@ constexpr int kBlkPerTile = kKeys / kBlockTokens;  // 8 cache blocks
 constexpr int kKStages = 2;
 constexpr int kVStages = 2;
 constexpr int kQBufs = 2;
+static_assert(kKStages == 2 && kVStages == 2,
+              "the rings are released through the two S/P buffers' barriers");
 constexpr int kSub = kRows * 128;            // one 64-column half of a 128-row operand (16 KiB)
 constexpr int kQBytes = 2 * kSub;            // one Q tile: 2 halves (dims 0-63, 64-127)
 constexpr int kKBytes = 2 * kKeys * 128;     // one K or V tile (2 halves of 128 key rows x 128 B)
@@ -95,10 +97,13 @@ constexpr int kBoxBytes = kBlockTokens * 128;  // one TMA box: 16 rows x 64 bf16
 // barrier indices
 enum {
     B_K_FULL = 0,
-    B_K_EMPTY = B_K_FULL + kKStages,
-    B_V_FULL = B_K_EMPTY + kKStages,
-    B_V_EMPTY = B_V_FULL + kVStages,
-    B_S_FULL = B_V_EMPTY + kVStages,
+    // A K stage is free once the Q K^T that read it has completed, and a V stage
+    // once its P V has: with two K stages, two V stages and two S/P buffers,
+    // stage i of each ring belongs to the tiles of S/P buffer i, so the
+    // producers wait on B_S_FULL and B_O_DONE (the next phase of either needs a
+    // tile the waiting producer has not loaded yet, so a wait cannot alias).
+    B_V_FULL = B_K_FULL + kKStages,
+    B_S_FULL = B_V_FULL + kVStages,
     B_P_FULL = B_S_FULL + 2,        // [S/P buffer]: every softmax warp has written its P
     B_O_DONE = B_P_FULL + 2,        // [S/P buffer]: that buffer's P V has completed
     B_Q_FULL = B_O_DONE + 2,        // [Q buffer]
@@ -426,11 +431,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&bars[B_K_FULL + s], 1);
-            mbar_init(&bars[B_K_EMPTY + s], 1);
         }
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(&bars[B_V_FULL + s], 1);
-            mbar_init(&bars[B_V_EMPTY + s], 1);
         }
         for (int s = 0; s < kQBufs; ++s) {
             mbar_init(&bars[B_Q_FULL + s], 1);
@@ -529,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nb = min(kBlkPerTile, x.nblk - j * kBlkPerTile);
                 const int blk = ids.tile(j, lane);
                 ok = __all_sync(0xffffffffu,
-                                mbar_wait(&bars[B_K_EMPTY + st], ((kt / kKStages) & 1) ^ 1, p.err));
+                                mbar_wait(&bars[B_S_FULL + st], ((kt / kKStages) & 1) ^ 1, p.err));
                 if (!ok || *abort_flag) {
                     ok = false;
                     break;
@@ -584,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nb = min(kBlkPerTile, x.nblk - j * kBlkPerTile);
                 const int blk = ids.tile(j, lane);
                 ok = __all_sync(0xffffffffu,
-                                mbar_wait(&bars[B_V_EMPTY + st], ((kt / kVStages) & 1) ^ 1, p.err));
+                                mbar_wait(&bars[B_O_DONE + st], ((kt / kVStages) & 1) ^ 1, p.err));
                 if (!ok || *abort_flag) {
                     ok = false;
                     break;
@@ -699,7 +702,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tc_after();
                             umma_ts8(tmem + kOCol, tmem + (t & 1) * kKeys, vd, kIdescPV, t0 ? 0u : 1u);
                             umma_commit(&bars[B_O_DONE + (t & 1)]);
-                            umma_commit(&bars[B_V_EMPTY + t % kVStages]);
                             pv_out = true;
                         }
                         ok = (!q_first ||
@@ -712,13 +714,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!pv_out) {
                     umma_ts8(tmem + kOCol, tmem + (t & 1) * kKeys, vd, kIdescPV, t0 ? 0u : 1u);
                     umma_commit(&bars[B_O_DONE + (t & 1)]);
-                    umma_commit(&bars[B_V_EMPTY + t % kVStages]);
                 }
                 if (pv) ++n_pv;
                 if (qk) {
                     umma_ss8(tmem + (q & 1) * kKeys, qa, kd, kIdescQK);
                     umma_commit(&bars[B_S_FULL + (q & 1)]);
-                    umma_commit(&bars[B_K_EMPTY + q % kKStages]);
                     const uint32_t bit = 1u << (q & 3);
                     first_bits = q_first ? (first_bits | bit) : (first_bits & ~bit);
                     unit_par_bits = (cur_unit & 1) ? (unit_par_bits | bit) : (unit_par_bits & ~bit);
