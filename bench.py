@@ -360,6 +360,113 @@ def mixed_batch_summary(steps, warmup):
     }
 
 
+def next_rows_summary(reps=20, warmup=3):
+    """The widened rows beside the hot path, each with its own figure.
+
+    rope_append: the fused rotary embedding + append over 16384 new tokens
+    (32 query / 8 KV heads, D 128, bf16, slots scattered over the pool): bytes
+    = k, v, q read + K/V rows and rotated q written + slots and positions +
+    the cos/sin rows touched, against the HBM copy peak, with the plain append
+    of the same K/V rows beside it.  Inputs are larger than L2.  The cos/sin
+    table holds random values (the kernel's time does not depend on them).
+    compose: the SplitFuse token-budget composer (host, C++ through the
+    binding), 2048-token budget, 512 decodes, 64 waiting prompts.
+    prefix_pool: the prefix-caching block pool (host): a 3000-token prompt per
+    sequence, 8 sequences per shared prompt, then one token appended per
+    sequence."""
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_51_gb300 as pkv
+
+    bw, _, _, _ = peaks()
+    dev = torch.device("cuda")
+    g = torch.Generator(device="cpu").manual_seed(7)
+    T, hq, hkv, d, bs, maxpos = 16384, 32, 8, 128, 16, 4096
+    nb = T // bs + 64
+    k = (torch.randn((T, hkv, d), generator=g) * 0.5).to(torch.bfloat16).to(dev)
+    v = (torch.randn((T, hkv, d), generator=g) * 0.5).to(torch.bfloat16).to(dev)
+    q = (torch.randn((T, hq, d), generator=g) * 0.5).to(torch.bfloat16).to(dev)
+    q_out = torch.empty_like(q)
+    slots = torch.randperm(nb * bs, generator=g)[:T].to(torch.int64).to(dev)
+    pos = (torch.arange(T, dtype=torch.int32) % maxpos).to(dev)
+    cos_sin = (torch.rand((maxpos, d), generator=g) * 2 - 1).to(dev)
+    kc = torch.zeros((nb, hkv, bs, d), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    desc = pkv.cache_desc(kc, hq)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        for a, b in ev:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+    rope_ms = timed(lambda: pkv.paged_kv_append_rope(k, v, slots, pos, cos_sin, kc, vc, desc,
+                                                     q=q, q_out=q_out))
+    plain_ms = timed(lambda: pkv.paged_kv_append(k, v, slots, kc, vc, desc))
+    if pkv.device_error() != 0:
+        raise SystemExit("device error in the append measurements")
+    kv_bytes = T * hkv * d * 2 * 2
+    q_bytes = T * hq * d * 2
+    rope_bytes = 2 * kv_bytes + 2 * q_bytes + T * (8 + 4) + min(T, maxpos) * d * 4
+    plain_bytes = 2 * kv_bytes + T * 8
+    del k, v, q, q_out, kc, vc
+    torch.cuda.empty_cache()
+
+    # SplitFuse composer (host)
+    rng = np.random.default_rng(3)
+    prompts = [max(1, int(x)) for x in rng.normal(1200, 360, 64)]
+    n_calls = 2000
+    t0 = time.perf_counter()
+    for _ in range(n_calls):
+        pkv.pkv_splitfuse_compose(2048, 512, prompts)
+    compose_us = (time.perf_counter() - t0) / n_calls * 1e6
+
+    # prefix-caching pool (host)
+    pool = pkv.BlockPool(65536, bs, 0, prefix_caching=True)
+    groups, per = 8, 8
+    shared = [[int(x) for x in rng.integers(0, 32000, 3000)] for _ in range(groups)]
+    t0 = time.perf_counter()
+    n_add = 0
+    for gi in range(groups):
+        for b in range(per):
+            st, _, _ = pool.add_tokens(gi * per + b, shared[gi])
+            if st != 0:
+                raise SystemExit("prefix pool: add_tokens failed")
+            n_add += 1
+    add_us = (time.perf_counter() - t0) / n_add * 1e6
+    t0 = time.perf_counter()
+    n_app = 0
+    for r in range(16):
+        for sid in range(groups * per):
+            st, _, _ = pool.append_token(sid, 1000 + r)
+            if st != 0:
+                raise SystemExit("prefix pool: append_token failed")
+            n_app += 1
+    append_us = (time.perf_counter() - t0) / n_app * 1e6
+    pool.close()
+    return {
+        "rope_append": {
+            "tokens": T, "heads": [hq, hkv], "head_dim": d, "ms": rope_ms,
+            "bytes": rope_bytes, "achieved_gbs": rope_bytes / (rope_ms * 1e-3) / 1e9,
+            "frac": rope_bytes / (rope_ms * 1e-3) / 1e9 / bw,
+            "plain_append_ms": plain_ms,
+            "plain_append_frac": plain_bytes / (plain_ms * 1e-3) / 1e9 / bw},
+        "compose": {"us_per_step": compose_us, "budget": 2048, "decodes": 512,
+                    "waiting_prompts": len(prompts)},
+        "prefix_pool": {"us_per_add_tokens_3000": add_us, "us_per_append_token": append_us,
+                        "note": "host, through the ctypes binding (marshalling included)"},
+    }
+
+
 def int8_decode_summary(w, dc, step, steps, warmup, bf16_attn_ms, full_size):
     """The same decode batch over an 8-bit copy of the cache: every slot of the
     bf16 pools quantised by the int8 append, then the int8 attention call timed
@@ -540,6 +647,9 @@ def run_gpu(args):
         mixed = mixed_batch_summary(min(args.steps, 200), args.warmup)
     cpu = cpu_baseline(args.config if args.config in (2, 3) else 2) if (
         world == 1 and not args.no_cpu) else None
+    nxt = None
+    if world == 1 and args.config == 2 and not args.no_next and not args.prefill_chunks:
+        nxt = next_rows_summary()
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -565,6 +675,7 @@ def run_gpu(args):
                      "peak_kind": f"{peak_kind} hbm_gbs (burst copy)"},
         "mixed_batch": mixed,
         "int8_kv_decode": int8,
+        "next_rows": nxt,
         "cpu_baseline": cpu,
         "e2e": {"value": step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
@@ -599,6 +710,8 @@ def main():
                     help="skip the mixed-batch (SplitFuse) sub-measurement")
     ap.add_argument("--no-int8", action="store_true",
                     help="skip the 8-bit KV cache decode sub-measurement")
+    ap.add_argument("--no-next", action="store_true",
+                    help="skip the widened rows (fused RoPE append, composer, prefix pool)")
     ap.add_argument("--cpu-worker", action="store_true")
     ap.add_argument("--cpu-seqs", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

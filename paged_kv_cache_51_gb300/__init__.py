@@ -12,6 +12,8 @@ import ctypes
 import math
 import os
 
+import numpy as np
+
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -179,9 +181,9 @@ class BlockPool:
 
     def add(self, seq_id, num_tokens):
         """Returns the slots of the prompt's tokens (list of int)."""
-        slots = (ctypes.c_int64 * num_tokens)()
-        _check(lib().pkv_seq_add(self._h, seq_id, num_tokens, slots), "pkv_seq_add")
-        return list(slots)
+        slots = np.empty(max(num_tokens, 1), dtype=np.int64)
+        _check(lib().pkv_seq_add(self._h, seq_id, num_tokens, slots.ctypes.data), "pkv_seq_add")
+        return slots[:num_tokens].tolist()
 
     def add_status(self, seq_id, num_tokens):
         slots = (ctypes.c_int64 * max(num_tokens, 1))()
@@ -190,12 +192,15 @@ class BlockPool:
 
     def add_tokens(self, seq_id, token_ids):
         """Returns (status, slots or None, num_cached_tokens)."""
-        n = len(token_ids)
-        toks = (ctypes.c_int32 * max(n, 1))(*[int(t) for t in token_ids])
-        slots = (ctypes.c_int64 * max(n, 1))()
+        toks = np.ascontiguousarray(np.asarray(token_ids, dtype=np.int64).astype(np.int32))
+        n = int(toks.shape[0])
+        if n == 0:
+            toks = np.zeros(1, dtype=np.int32)
+        slots = np.empty(max(n, 1), dtype=np.int64)
         cached = ctypes.c_int32()
-        st = lib().pkv_seq_add_tokens(self._h, seq_id, toks, n, slots, ctypes.byref(cached))
-        return st, (list(slots)[:n] if st == PKV_OK else None), cached.value
+        st = lib().pkv_seq_add_tokens(self._h, seq_id, toks.ctypes.data, n, slots.ctypes.data,
+                                      ctypes.byref(cached))
+        return st, (slots[:n].tolist() if st == PKV_OK else None), cached.value
 
     def append_token(self, seq_id, token_id):
         """Returns (status, slot, cow) with cow = (src, dst) or None."""
