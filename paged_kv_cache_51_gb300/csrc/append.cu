@@ -34,14 +34,20 @@ struct AppendParams {
     int* err;
 };
 
-// grid-stride over (token, kv head, vector); K and V handled by the same thread
+// grid-stride over (token, kv head, vector); K and V handled by the same thread.
+// Idx is the type of the flat index: 32-bit unsigned whenever the launch's
+// element count fits (its divisions are a few instructions, where 64-bit ones
+// by a run-time divisor are a long emulated sequence per 16-byte vector), else
+// 64-bit.  Cache offsets are always 64-bit.
+template <typename Idx>
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
-    const int64_t per_tok = int64_t(p.num_kv_heads) * p.vec_per_row;
-    const int64_t total = p.num_tokens * per_tok;
-    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
-         i += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t t = i / per_tok;
-        const int64_t r = i - t * per_tok;            // (head, vector) within the token
+    const Idx per_tok = Idx(p.num_kv_heads) * Idx(p.vec_per_row);
+    const Idx total = Idx(p.num_tokens) * per_tok;
+    const Idx vec = Idx(p.vec_per_row);
+    for (Idx i = Idx(blockIdx.x) * Idx(blockDim.x) + Idx(threadIdx.x); i < total;
+         i += Idx(gridDim.x) * Idx(blockDim.x)) {
+        const Idx t = i / per_tok;
+        const Idx r = i - t * per_tok;                // (head, vector) within the token
         const int64_t slot = __ldg(p.slots + t);
         if (slot < 0) continue;                       // padding token
         if (slot >= p.num_slots) {
@@ -50,9 +56,10 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
         }
         const int64_t blk = slot / p.block_size;
         const int64_t row = slot - blk * p.block_size;
-        const int64_t h = r / p.vec_per_row;
-        const int64_t c = r - h * p.vec_per_row;
-        const int64_t dst = ((blk * p.num_kv_heads + h) * p.block_size + row) * p.vec_per_row + c;
+        const Idx h = r / vec;
+        const Idx c = r - h * vec;
+        const int64_t dst =
+            ((blk * p.num_kv_heads + int64_t(h)) * p.block_size + row) * p.vec_per_row + int64_t(c);
         const uint4 kv = __ldg(p.k + i);
         const uint4 vv = __ldg(p.v + i);
         p.k_cache[dst] = kv;
@@ -158,16 +165,19 @@ __device__ __forceinline__ void store8<float>(float* p, const float (&x)[8]) {
     reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
 }
 
-template <typename T, int D>
+// (Idx as for append_kernel.)
+template <typename T, int D, typename Idx>
 __global__ void __launch_bounds__(256) append_rope_kernel(RopeParams p) {
     constexpr int kChunks = D / 16;           // 8-pair chunks per head row
     const int rows = p.num_q_rows + 2 * p.num_kv_heads;
-    const int64_t total = p.num_tokens * rows * kChunks;
-    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
-         i += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t t = i / (int64_t(rows) * kChunks);
-        const int r = int(i / kChunks % rows);
-        const int c = int(i % kChunks);
+    const Idx per_tok = Idx(rows) * Idx(kChunks);
+    const Idx total = Idx(p.num_tokens) * per_tok;
+    for (Idx i = Idx(blockIdx.x) * Idx(blockDim.x) + Idx(threadIdx.x); i < total;
+         i += Idx(gridDim.x) * Idx(blockDim.x)) {
+        const int64_t t = int64_t(i / per_tok);
+        const Idx rc = i - Idx(t) * per_tok;  // (row, chunk) within the token
+        const int r = int(rc / Idx(kChunks));
+        const int c = int(rc % Idx(kChunks));
         const bool is_q = r < p.num_q_rows;
         const bool is_v = r >= p.num_q_rows + p.num_kv_heads;
         const int h = is_q ? r : (r - p.num_q_rows) % p.num_kv_heads;
@@ -251,7 +261,10 @@ extern "C" int paged_kv_append(const void* k, const void* v, const int64_t* slot
     const int64_t total = int64_t(num_tokens) * desc->num_kv_heads * p.vec_per_row;
     const int64_t cap = int64_t(std::max(num_sms(), 1)) * 8;
     const int64_t blocks = std::min<int64_t>((total + 255) / 256, cap);
-    append_kernel<<<unsigned(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    if (total < (int64_t(1) << 31))
+        append_kernel<uint32_t><<<unsigned(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    else
+        append_kernel<int64_t><<<unsigned(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
     return cuda_status(cudaGetLastError());
 }
 
@@ -365,12 +378,23 @@ extern "C" int paged_kv_append_rope(const void* q, void* q_out, const void* k, c
     const int64_t blocks = std::min<int64_t>((total + 255) / 256, int64_t(std::max(num_sms(), 1)) * 8);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool bf = desc->dtype == PKV_BF16;
+    const bool narrow = total < (int64_t(1) << 31);
     if (desc->head_dim == 128) {
-        if (bf) append_rope_kernel<__nv_bfloat16, 128><<<unsigned(blocks), 256, 0, s>>>(p);
-        else append_rope_kernel<float, 128><<<unsigned(blocks), 256, 0, s>>>(p);
+        if (bf) {
+            if (narrow) append_rope_kernel<__nv_bfloat16, 128, uint32_t><<<unsigned(blocks), 256, 0, s>>>(p);
+            else append_rope_kernel<__nv_bfloat16, 128, int64_t><<<unsigned(blocks), 256, 0, s>>>(p);
+        } else {
+            if (narrow) append_rope_kernel<float, 128, uint32_t><<<unsigned(blocks), 256, 0, s>>>(p);
+            else append_rope_kernel<float, 128, int64_t><<<unsigned(blocks), 256, 0, s>>>(p);
+        }
     } else {
-        if (bf) append_rope_kernel<__nv_bfloat16, 64><<<unsigned(blocks), 256, 0, s>>>(p);
-        else append_rope_kernel<float, 64><<<unsigned(blocks), 256, 0, s>>>(p);
+        if (bf) {
+            if (narrow) append_rope_kernel<__nv_bfloat16, 64, uint32_t><<<unsigned(blocks), 256, 0, s>>>(p);
+            else append_rope_kernel<__nv_bfloat16, 64, int64_t><<<unsigned(blocks), 256, 0, s>>>(p);
+        } else {
+            if (narrow) append_rope_kernel<float, 64, uint32_t><<<unsigned(blocks), 256, 0, s>>>(p);
+            else append_rope_kernel<float, 64, int64_t><<<unsigned(blocks), 256, 0, s>>>(p);
+        }
     }
     return cuda_status(cudaGetLastError());
 }
