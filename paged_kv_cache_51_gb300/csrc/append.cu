@@ -105,9 +105,7 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(CopyParams p) {
 // with (c, s) from the caller's table at the token's position.  Each product
 // and sum is rounded on its own (no fused multiply-add), then the result is
 // rounded to the cache dtype, so the stored bytes are reproducible exactly.
-// One thread handles 8 rotation pairs of one (token, row), where the rows of a
-// token are its Hq query heads, then its Hkv key heads, then its Hkv value
-// heads (values are copied unrotated).
+// Values are copied unrotated.
 // ---------------------------------------------------------------------------
 struct RopeParams {
     const void* q;
@@ -165,48 +163,33 @@ __device__ __forceinline__ void store8<float>(float* p, const float (&x)[8]) {
     reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
 }
 
-// (Idx as for append_kernel.)
+// One thread per (token, 8-pair chunk): it loads the chunk's cos and sin once
+// and applies them to every rotated row of the token (its q heads, then its K
+// heads), then copies the chunk of its V heads.  Eight consecutive threads
+// cover a 256-byte row, so loads and stores stay coalesced.  (Idx as for
+// append_kernel.)
 template <typename T, int D, typename Idx>
 __global__ void __launch_bounds__(256) append_rope_kernel(RopeParams p) {
     constexpr int kChunks = D / 16;           // 8-pair chunks per head row
-    const int rows = p.num_q_rows + 2 * p.num_kv_heads;
-    const Idx per_tok = Idx(rows) * Idx(kChunks);
-    const Idx total = Idx(p.num_tokens) * per_tok;
+    const Idx total = Idx(p.num_tokens) * Idx(kChunks);
     for (Idx i = Idx(blockIdx.x) * Idx(blockDim.x) + Idx(threadIdx.x); i < total;
          i += Idx(gridDim.x) * Idx(blockDim.x)) {
-        const int64_t t = int64_t(i / per_tok);
-        const Idx rc = i - Idx(t) * per_tok;  // (row, chunk) within the token
-        const int r = int(rc / Idx(kChunks));
-        const int c = int(rc % Idx(kChunks));
-        const bool is_q = r < p.num_q_rows;
-        const bool is_v = r >= p.num_q_rows + p.num_kv_heads;
-        const int h = is_q ? r : (r - p.num_q_rows) % p.num_kv_heads;
-        int64_t dst_row = 0;
-        if (!is_q) {
-            const int64_t slot = __ldg(p.slots + t);
-            if (slot < 0) continue;                                    // padding token
-            if (slot >= p.num_slots) {
-                flag_error(p.err, PKV_DEV_BAD_SLOT);
-                continue;
-            }
-            const int64_t blk = slot / p.block_size;
-            dst_row = (blk * p.num_kv_heads + h) * p.block_size + (slot - blk * p.block_size);
-        }
-        const T* src = is_q ? static_cast<const T*>(p.q) + (t * p.num_q_rows + h) * D
-                            : static_cast<const T*>(is_v ? p.v : p.k) + (t * p.num_kv_heads + h) * D;
-        float x1[8], x2[8];
-        load8<T>(src + 8 * c, x1);
-        load8<T>(src + D / 2 + 8 * c, x2);
-        if (!is_v) {
-            const int pos = __ldg(p.positions + t);
-            if (pos < 0 || pos >= p.max_position) {
-                flag_error(p.err, PKV_DEV_BAD_POSITION);
-                continue;
-            }
+        const int64_t t = int64_t(i / Idx(kChunks));
+        const int c = int(i % Idx(kChunks));
+        const int pos = __ldg(p.positions + t);
+        const bool pos_ok = pos >= 0 && pos < p.max_position;
+        const int64_t slot = __ldg(p.slots + t);
+        // a bad position matters to the rows that rotate: q heads, and K heads
+        // whose slot is in range (a padding or out-of-range slot skips K and V)
+        if (!pos_ok && c == 0 && (p.num_q_rows > 0 || (slot >= 0 && slot < p.num_slots)))
+            flag_error(p.err, PKV_DEV_BAD_POSITION);
+        float co[8], si[8];
+        if (pos_ok) {
             const float* cs = p.cos_sin + int64_t(pos) * D;
-            float co[8], si[8];
             load8<float>(cs + 8 * c, co);
             load8<float>(cs + D / 2 + 8 * c, si);
+        }
+        auto rotate = [&](float (&x1)[8], float (&x2)[8]) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const float a = __fmul_rn(x1[j], co[j]), b = __fmul_rn(x2[j], si[j]);
@@ -214,11 +197,49 @@ __global__ void __launch_bounds__(256) append_rope_kernel(RopeParams p) {
                 x1[j] = __fsub_rn(a, b);
                 x2[j] = __fadd_rn(e, f);
             }
+        };
+        // q heads: rotated into q_out (no slot involved)
+        if (pos_ok) {
+            const T* qs = static_cast<const T*>(p.q) + t * p.num_q_rows * D + 8 * c;
+            T* qd = static_cast<T*>(p.q_out) + t * p.num_q_rows * D + 8 * c;
+#pragma unroll 4
+            for (int h = 0; h < p.num_q_rows; ++h) {
+                float x1[8], x2[8];
+                load8<T>(qs + h * D, x1);
+                load8<T>(qs + h * D + D / 2, x2);
+                rotate(x1, x2);
+                store8<T>(qd + h * D, x1);
+                store8<T>(qd + h * D + D / 2, x2);
+            }
         }
-        T* dst = is_q ? static_cast<T*>(p.q_out) + (t * p.num_q_rows + h) * D
-                      : static_cast<T*>(is_v ? p.v_cache : p.k_cache) + dst_row * D;
-        store8<T>(dst + 8 * c, x1);
-        store8<T>(dst + D / 2 + 8 * c, x2);
+        // K (rotated) and V (copied) heads into the token's slot
+        if (slot < 0) continue;                                        // padding token
+        if (slot >= p.num_slots) {
+            if (c == 0) flag_error(p.err, PKV_DEV_BAD_SLOT);
+            continue;
+        }
+        const int64_t blk = slot / p.block_size;
+        const int64_t row0 = blk * p.num_kv_heads * p.block_size + (slot - blk * p.block_size);
+        const T* ks = static_cast<const T*>(p.k) + t * p.num_kv_heads * D + 8 * c;
+        const T* vs = static_cast<const T*>(p.v) + t * p.num_kv_heads * D + 8 * c;
+        T* kd = static_cast<T*>(p.k_cache) + 8 * c;
+        T* vd = static_cast<T*>(p.v_cache) + 8 * c;
+#pragma unroll 4
+        for (int h = 0; h < p.num_kv_heads; ++h) {
+            const int64_t dst = (row0 + int64_t(h) * p.block_size) * D;
+            float x1[8], x2[8];
+            load8<T>(vs + h * D, x1);
+            load8<T>(vs + h * D + D / 2, x2);
+            store8<T>(vd + dst, x1);
+            store8<T>(vd + dst + D / 2, x2);
+            if (pos_ok) {
+                load8<T>(ks + h * D, x1);
+                load8<T>(ks + h * D + D / 2, x2);
+                rotate(x1, x2);
+                store8<T>(kd + dst, x1);
+                store8<T>(kd + dst + D / 2, x2);
+            }
+        }
     }
 }
 
@@ -373,8 +394,7 @@ extern "C" int paged_kv_append_rope(const void* q, void* q_out, const void* k, c
     p.max_position = max_position;
     p.num_slots = int64_t(desc->num_blocks) * desc->block_size;
     p.err = err;
-    const int64_t total = int64_t(num_tokens) * (p.num_q_rows + 2 * p.num_kv_heads) *
-                          (desc->head_dim / 16);
+    const int64_t total = int64_t(num_tokens) * (desc->head_dim / 16);   // (token, chunk) pairs
     const int64_t blocks = std::min<int64_t>((total + 255) / 256, int64_t(std::max(num_sms(), 1)) * 8);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool bf = desc->dtype == PKV_BF16;
