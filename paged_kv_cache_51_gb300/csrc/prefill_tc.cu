@@ -35,18 +35,19 @@
 //              unit's bf16 output tile is staged in the unit's Q buffer (the
 //              TMA box layout) and leaves by two TMA tensor stores, so the warps
 //              go on to the next unit at once (128 rows of scattered 16-byte
-//              global stores kept the load/store unit busy for ~3000 cycles).
-//              A partial unit writes its valid rows directly.
+//              global stores kept the load/store unit busy for ~3000 cycles);
+//              warp 8 issues those stores before it reuses the buffer.  A
+//              partial unit writes its valid rows directly.
 //   warp 8     takes work units from a ticket (the planner orders them longest
 //              first) and publishes them to the other roles; TMA producer for
 //              the unit's Q tile (two buffers) and for K: blocks of each key
 //              tile into a 2-stage K ring; a K stage is released as soon as its
-//              Q K^T product is done
+//              Q K^T product is done; sends staged output tiles out by TMA
 //   warp 9     TMA producer for V: a 2-stage V ring released by the P V product
 //   warp 10    TMEM owner and MMA issuer (one thread issues tcgen05.mma): a step
 //              issues P V of key tile q - 2 and Q K^T of key tile q as bursts
 //              behind one group of waits, so the tensor pipe works on those
-//              while the softmax runs on tile s - 1 (across units as well)
+//              while the softmax runs on tile q - 1 (across units as well)
 // Every wait is bounded; on a timeout the kernel records an error, stops
 // issuing work, drains its copies and MMAs and frees TMEM before it returns.
 #include <cuda.h>
