@@ -54,7 +54,23 @@ def _stamp(srcs, hdrs):
 
 
 def build(force=False, verbose=False):
-    """Compile and link the library; return its path.  Raises on compiler errors."""
+    """Compile and link the library; return its path.  Raises on compiler errors.
+
+    Processes that build at the same time (one per rank under torchrun) take
+    turns through a lock file next to the library; the later ones find the
+    fresh stamp and return at once."""
+    import fcntl
+
+    os.makedirs(os.path.dirname(LIB), exist_ok=True)
+    with open(LIB + ".lock", "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            return _build_locked(force, verbose)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(force, verbose):
     srcs, hdrs = _sources()
     stamp = _stamp(srcs, hdrs)
     stamp_file = LIB + ".stamp"
