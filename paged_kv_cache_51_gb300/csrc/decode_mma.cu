@@ -60,8 +60,9 @@ struct MmaCfg {
     static constexpr int kTileBytes = kBlockTokens * D * 2;
     static constexpr int kStageBytes = 2 * kTileBytes;
     // g = 8 runs 3 CTAs per SM on a 4-stage ring (measured faster on the
-    // prefix-sharing batch); smaller groups keep 8 stages at 2 CTAs per SM
-    static constexpr int kStages = G == 8 ? 4 : 8;
+    // prefix-sharing batch); smaller groups run 12 stages at 2 CTAs per SM
+    // (192 KB of tiles in flight per SM; measured 0.5 % faster than 8 stages)
+    static constexpr int kStages = G == 8 ? 4 : 12;
     static constexpr int kMinBlocks = G == 8 ? 3 : 1;
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kComb = G * (D + 2);
