@@ -190,20 +190,34 @@ def cpu_worker(config, n_seqs, seconds):
                       "passes": passes, "seqs": n_seqs}))
 
 
-def cpu_baseline(config, seconds=10.0, n_seqs=4):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker",
-                        "--config", str(config), "--cpu-seqs", str(n_seqs),
-                        "--cpu-seconds", str(seconds)],
-                       capture_output=True, text=True, env=env, cwd=ROOT)
-    if r.returncode != 0:
+def cpu_baseline(config, seconds=10.0, n_seqs=4, all_cores_seconds=5.0):
+    """The oracle timed on the host: once on one core (BLAS threads pinned to 1),
+    then once more with the host's default threading (all cores available)."""
+    def run(env, secs):
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker",
+                            "--config", str(config), "--cpu-seqs", str(n_seqs),
+                            "--cpu-seconds", str(secs)],
+                           capture_output=True, text=True, env=env, cwd=ROOT)
+        if r.returncode != 0:
+            return None, r.stderr.strip()[-200:]
+        return json.loads(r.stdout.strip().splitlines()[-1]), None
+
+    one = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    d, err = run(one, seconds)
+    if d is None:
         return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                "sample": f"failed: {r.stderr.strip()[-200:]}"}
-    d = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": d["value"], "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": (f"first {n_seqs} sequences of the same workload (same generator), float64 "
-                       f"NumPy oracle attention repeated {d['passes']}x over {d['seconds']:.1f} s "
-                       f"on one host core")}
+                "sample": f"failed: {err}"}
+    out = {"value": d["value"], "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": (f"first {n_seqs} sequences of the same workload (same generator), float64 "
+                      f"NumPy oracle attention repeated {d['passes']}x over {d['seconds']:.1f} s "
+                      f"on one host core")}
+    full = {k: v for k, v in os.environ.items()
+            if k not in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    d2, _ = run(full, all_cores_seconds)
+    if d2 is not None:
+        out["all_cores"] = {"value": d2["value"], "cores": os.cpu_count(),
+                            "note": "same sample, default NumPy/BLAS threading"}
+    return out
 
 
 def run_reference(args):
