@@ -27,6 +27,9 @@
  *     owns all memory; no entry point allocates device memory.
  *   - Device entry points only enqueue work on `stream` (a cudaStream_t passed
  *     as void*, NULL = legacy default stream) and return without waiting.
+ *     Stream order holds in full: the kernels of one call are chained with
+ *     programmatic dependent launch, but each waits for the work ahead of it
+ *     on the stream before it reads any input or plan.
  *     Arguments that can be checked on the host are checked before anything
  *     is launched (PKV_ERR_INVALID / PKV_ERR_UNSUPPORTED, nothing enqueued).
  *     Values that live in device memory (block ids, slots, lengths) are
