@@ -34,36 +34,52 @@ struct AppendParams {
     int* err;
 };
 
-// grid-stride over (token, kv head, vector); K and V handled by the same thread.
+// grid-stride over (token, kv head, vector); K and V handled by the same thread,
+// kAppendUnroll vectors per pass with all their loads issued before any store.
 // Idx is the type of the flat index: 32-bit unsigned whenever the launch's
 // element count fits (its divisions are a few instructions, where 64-bit ones
 // by a run-time divisor are a long emulated sequence per 16-byte vector), else
 // 64-bit.  Cache offsets are always 64-bit.
+constexpr int kAppendUnroll = 4;
+
 template <typename Idx>
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
     const Idx per_tok = Idx(p.num_kv_heads) * Idx(p.vec_per_row);
     const Idx total = Idx(p.num_tokens) * per_tok;
     const Idx vec = Idx(p.vec_per_row);
-    for (Idx i = Idx(blockIdx.x) * Idx(blockDim.x) + Idx(threadIdx.x); i < total;
-         i += Idx(gridDim.x) * Idx(blockDim.x)) {
-        const Idx t = i / per_tok;
-        const Idx r = i - t * per_tok;                // (head, vector) within the token
-        const int64_t slot = __ldg(p.slots + t);
-        if (slot < 0) continue;                       // padding token
-        if (slot >= p.num_slots) {
-            flag_error(p.err, PKV_DEV_BAD_SLOT);
-            continue;
+    const Idx stride = Idx(gridDim.x) * Idx(blockDim.x);
+    for (Idx i0 = Idx(blockIdx.x) * Idx(blockDim.x) + Idx(threadIdx.x); i0 < total;
+         i0 += Idx(kAppendUnroll) * stride) {
+        uint4 kv[kAppendUnroll], vv[kAppendUnroll];
+        int64_t slot[kAppendUnroll];
+#pragma unroll
+        for (int u = 0; u < kAppendUnroll; ++u) {
+            const Idx i = i0 + Idx(u) * stride;
+            if (i < total) {
+                slot[u] = __ldg(p.slots + i / per_tok);
+                kv[u] = __ldg(p.k + i);
+                vv[u] = __ldg(p.v + i);
+            }
         }
-        const int64_t blk = slot / p.block_size;
-        const int64_t row = slot - blk * p.block_size;
-        const Idx h = r / vec;
-        const Idx c = r - h * vec;
-        const int64_t dst =
-            ((blk * p.num_kv_heads + int64_t(h)) * p.block_size + row) * p.vec_per_row + int64_t(c);
-        const uint4 kv = __ldg(p.k + i);
-        const uint4 vv = __ldg(p.v + i);
-        p.k_cache[dst] = kv;
-        p.v_cache[dst] = vv;
+#pragma unroll
+        for (int u = 0; u < kAppendUnroll; ++u) {
+            const Idx i = i0 + Idx(u) * stride;
+            if (i >= total || slot[u] < 0) continue;      // past the end, or a padding token
+            if (slot[u] >= p.num_slots) {
+                flag_error(p.err, PKV_DEV_BAD_SLOT);
+                continue;
+            }
+            const Idx t = i / per_tok;
+            const Idx r = i - t * per_tok;                // (head, vector) within the token
+            const int64_t blk = slot[u] / p.block_size;
+            const int64_t row = slot[u] - blk * p.block_size;
+            const Idx h = r / vec;
+            const Idx c = r - h * vec;
+            const int64_t dst =
+                ((blk * p.num_kv_heads + int64_t(h)) * p.block_size + row) * p.vec_per_row + int64_t(c);
+            p.k_cache[dst] = kv[u];
+            p.v_cache[dst] = vv[u];
+        }
     }
 }
 
@@ -163,88 +179,170 @@ __device__ __forceinline__ void store8<float>(float* p, const float (&x)[8]) {
     reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
 }
 
-// One thread per (token, 8-pair chunk): it loads the chunk's cos and sin once
-// and applies them to every rotated row of the token (its q heads, then its K
-// heads), then copies the chunk of its V heads.  Eight consecutive threads
-// cover a 256-byte row, so loads and stores stay coalesced.  (Idx as for
-// append_kernel.)
+// Raw bytes of one 8-element chunk of a row (16 B of bf16, 32 B of fp32).
+template <typename T>
+struct Chunk8 {
+    uint4 w[sizeof(T) / 2];
+};
+template <typename T>
+__device__ __forceinline__ void load_raw(const T* p, Chunk8<T>& x) {
+#pragma unroll
+    for (int i = 0; i < int(sizeof(T)) / 2; ++i) x.w[i] = __ldg(reinterpret_cast<const uint4*>(p) + i);
+}
+template <typename T>
+__device__ __forceinline__ void store_raw(T* p, const Chunk8<T>& x) {
+#pragma unroll
+    for (int i = 0; i < int(sizeof(T)) / 2; ++i) reinterpret_cast<uint4*>(p)[i] = x.w[i];
+}
+__device__ __forceinline__ void widen(const Chunk8<__nv_bfloat16>& x, float (&f)[8]) {
+    const uint32_t w[4] = {x.w[0].x, x.w[0].y, x.w[0].z, x.w[0].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ void widen(const Chunk8<float>& x, float (&f)[8]) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        f[4 * i] = __uint_as_float(x.w[i].x);
+        f[4 * i + 1] = __uint_as_float(x.w[i].y);
+        f[4 * i + 2] = __uint_as_float(x.w[i].z);
+        f[4 * i + 3] = __uint_as_float(x.w[i].w);
+    }
+}
+
+// A token's rows, in order: its Hq query heads (rotated into q_out), its Hkv
+// K heads (rotated into the slot) and its Hkv V heads (copied into the slot).
+// One thread per (token, group of kRows rows, 8-pair chunk): it issues the
+// loads of all its rows' chunks before it rotates and stores any, so each
+// thread keeps kRows x 32 B (bf16) in flight, and it loads the chunk's cos
+// and sin once for the group.  Eight consecutive threads cover a 256-byte
+// row, so loads and stores stay coalesced.  (Idx as for append_kernel.)
+template <typename T>
+__host__ __device__ constexpr int rope_rows_per_thread() { return 16 / int(sizeof(T)); }
+
 template <typename T, int D, typename Idx>
-__global__ void __launch_bounds__(256) append_rope_kernel(RopeParams p) {
+__global__ void __launch_bounds__(256, 2) append_rope_kernel(RopeParams p) {
     constexpr int kChunks = D / 16;           // 8-pair chunks per head row
-    const Idx total = Idx(p.num_tokens) * Idx(kChunks);
+    constexpr int kRows = rope_rows_per_thread<T>();
+    const int hq = p.num_q_rows, hkv = p.num_kv_heads;
+    const int rows = hq + 2 * hkv;
+    const int groups = (rows + kRows - 1) / kRows;
+    const Idx per_tok = Idx(groups) * Idx(kChunks);
+    const Idx total = Idx(p.num_tokens) * per_tok;
     for (Idx i = Idx(blockIdx.x) * Idx(blockDim.x) + Idx(threadIdx.x); i < total;
          i += Idx(gridDim.x) * Idx(blockDim.x)) {
-        const int64_t t = int64_t(i / Idx(kChunks));
-        const int c = int(i % Idx(kChunks));
+        const Idx ti = i / per_tok;
+        const int r = int(i - ti * per_tok);
+        const int64_t t = int64_t(ti);
+        const int c = r % kChunks;
+        const int row_lo = (r / kChunks) * kRows;
         const int pos = __ldg(p.positions + t);
         const bool pos_ok = pos >= 0 && pos < p.max_position;
         const int64_t slot = __ldg(p.slots + t);
-        // a bad position matters to the rows that rotate: q heads, and K heads
-        // whose slot is in range (a padding or out-of-range slot skips K and V)
-        if (!pos_ok && c == 0 && (p.num_q_rows > 0 || (slot >= 0 && slot < p.num_slots)))
-            flag_error(p.err, PKV_DEV_BAD_POSITION);
+        const bool slot_ok = slot >= 0 && slot < p.num_slots;
+        if (row_lo == 0 && c == 0) {
+            // a bad position matters to the rows that rotate: q heads, and K
+            // heads whose slot is in range (a padding or out-of-range slot
+            // skips K and V)
+            if (!pos_ok && (hq > 0 || slot_ok)) flag_error(p.err, PKV_DEV_BAD_POSITION);
+            if (slot >= p.num_slots) flag_error(p.err, PKV_DEV_BAD_SLOT);
+        }
+        int64_t row0 = 0;
+        if (slot_ok) {
+            const int64_t blk = slot / p.block_size;
+            row0 = blk * hkv * p.block_size + (slot - blk * p.block_size);
+        }
+        // sources and destinations of the group's rows; a row that is not
+        // written this step (past the token's rows, or skipped) is inactive
+        Chunk8<T> x1[kRows], x2[kRows];
+        const T* src[kRows];
+        T* dst[kRows];
+        bool act[kRows], rot[kRows];
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) {
+            const int row = row_lo + j;
+            if (row < hq) {
+                const int64_t off = (t * hq + row) * D + 8 * c;
+                src[j] = static_cast<const T*>(p.q) + off;
+                dst[j] = static_cast<T*>(p.q_out) + off;
+                act[j] = pos_ok;
+                rot[j] = true;
+            } else if (row < hq + hkv) {
+                const int h = row - hq;
+                src[j] = static_cast<const T*>(p.k) + (t * hkv + h) * D + 8 * c;
+                dst[j] = static_cast<T*>(p.k_cache) + (row0 + int64_t(h) * p.block_size) * D + 8 * c;
+                act[j] = pos_ok && slot_ok;
+                rot[j] = true;
+            } else {
+                const int h = row - hq - hkv;
+                src[j] = static_cast<const T*>(p.v) + (t * hkv + h) * D + 8 * c;
+                dst[j] = static_cast<T*>(p.v_cache) + (row0 + int64_t(h) * p.block_size) * D + 8 * c;
+                act[j] = slot_ok && row < rows;
+                rot[j] = false;
+            }
+            if (act[j]) {
+                load_raw<T>(src[j], x1[j]);
+                load_raw<T>(src[j] + D / 2, x2[j]);
+            }
+        }
         float co[8], si[8];
-        if (pos_ok) {
+        if (pos_ok && row_lo < hq + hkv) {
             const float* cs = p.cos_sin + int64_t(pos) * D;
             load8<float>(cs + 8 * c, co);
             load8<float>(cs + D / 2 + 8 * c, si);
         }
-        auto rotate = [&](float (&x1)[8], float (&x2)[8]) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float a = __fmul_rn(x1[j], co[j]), b = __fmul_rn(x2[j], si[j]);
-                const float e = __fmul_rn(x1[j], si[j]), f = __fmul_rn(x2[j], co[j]);
-                x1[j] = __fsub_rn(a, b);
-                x2[j] = __fadd_rn(e, f);
+        for (int j = 0; j < kRows; ++j) {
+            if (!act[j]) continue;
+            if (!rot[j]) {
+                store_raw<T>(dst[j], x1[j]);
+                store_raw<T>(dst[j] + D / 2, x2[j]);
+                continue;
             }
-        };
-        // q heads: rotated into q_out (no slot involved)
-        if (pos_ok) {
-            const T* qs = static_cast<const T*>(p.q) + t * p.num_q_rows * D + 8 * c;
-            T* qd = static_cast<T*>(p.q_out) + t * p.num_q_rows * D + 8 * c;
-#pragma unroll 4
-            for (int h = 0; h < p.num_q_rows; ++h) {
-                float x1[8], x2[8];
-                load8<T>(qs + h * D, x1);
-                load8<T>(qs + h * D + D / 2, x2);
-                rotate(x1, x2);
-                store8<T>(qd + h * D, x1);
-                store8<T>(qd + h * D + D / 2, x2);
+            float a1[8], a2[8], y1[8], y2[8];
+            widen(x1[j], a1);
+            widen(x2[j], a2);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float a = __fmul_rn(a1[e], co[e]), b = __fmul_rn(a2[e], si[e]);
+                const float s = __fmul_rn(a1[e], si[e]), f = __fmul_rn(a2[e], co[e]);
+                y1[e] = __fsub_rn(a, b);
+                y2[e] = __fadd_rn(s, f);
             }
-        }
-        // K (rotated) and V (copied) heads into the token's slot
-        if (slot < 0) continue;                                        // padding token
-        if (slot >= p.num_slots) {
-            if (c == 0) flag_error(p.err, PKV_DEV_BAD_SLOT);
-            continue;
-        }
-        const int64_t blk = slot / p.block_size;
-        const int64_t row0 = blk * p.num_kv_heads * p.block_size + (slot - blk * p.block_size);
-        const T* ks = static_cast<const T*>(p.k) + t * p.num_kv_heads * D + 8 * c;
-        const T* vs = static_cast<const T*>(p.v) + t * p.num_kv_heads * D + 8 * c;
-        T* kd = static_cast<T*>(p.k_cache) + 8 * c;
-        T* vd = static_cast<T*>(p.v_cache) + 8 * c;
-#pragma unroll 4
-        for (int h = 0; h < p.num_kv_heads; ++h) {
-            const int64_t dst = (row0 + int64_t(h) * p.block_size) * D;
-            float x1[8], x2[8];
-            load8<T>(vs + h * D, x1);
-            load8<T>(vs + h * D + D / 2, x2);
-            store8<T>(vd + dst, x1);
-            store8<T>(vd + dst + D / 2, x2);
-            if (pos_ok) {
-                load8<T>(ks + h * D, x1);
-                load8<T>(ks + h * D + D / 2, x2);
-                rotate(x1, x2);
-                store8<T>(kd + dst, x1);
-                store8<T>(kd + dst + D / 2, x2);
-            }
+            store8<T>(dst[j], y1);
+            store8<T>(dst[j] + D / 2, y2);
         }
     }
 }
 
 namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Resident 256-thread blocks per SM of a grid-stride kernel (1 if the query
+// fails; its error is cleared so that it is not reported by a later launch).
+template <typename K>
+int resident_blocks_per_sm(K kernel) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 256, 0) != cudaSuccess || n < 1) {
+        (void)cudaGetLastError();
+        n = 1;
+    }
+    return n;
+}
+
+// Grid-stride launch of the RoPE append with no more blocks than are resident
+// at once (the kernel holds a group's rows in registers, so fewer than eight
+// 256-thread blocks fit on an SM: two, at the bound of 128 registers).
+template <typename T, int D, typename Idx>
+int launch_rope(const RopeParams& p, int64_t total, void* stream) {
+    static const int per_sm = resident_blocks_per_sm(append_rope_kernel<T, D, Idx>);
+    const int64_t blocks =
+        std::min<int64_t>((total + 255) / 256, int64_t(std::max(num_sms(), 1)) * per_sm);
+    append_rope_kernel<T, D, Idx><<<unsigned(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    return cuda_status(cudaGetLastError());
+}
 
 }  // namespace
 
@@ -280,12 +378,17 @@ extern "C" int paged_kv_append(const void* k, const void* v, const int64_t* slot
     p.num_slots = int64_t(desc->num_blocks) * desc->block_size;
     p.err = err;
     const int64_t total = int64_t(num_tokens) * desc->num_kv_heads * p.vec_per_row;
-    const int64_t cap = int64_t(std::max(num_sms(), 1)) * 8;
-    const int64_t blocks = std::min<int64_t>((total + 255) / 256, cap);
-    if (total < (int64_t(1) << 31))
+    const int64_t sms = std::max(num_sms(), 1);
+    const int64_t want = (total + 255) / 256;
+    if (total < (int64_t(1) << 31)) {
+        static const int per_sm = resident_blocks_per_sm(append_kernel<uint32_t>);
+        const int64_t blocks = std::min<int64_t>(want, sms * per_sm);
         append_kernel<uint32_t><<<unsigned(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
-    else
+    } else {
+        static const int per_sm = resident_blocks_per_sm(append_kernel<int64_t>);
+        const int64_t blocks = std::min<int64_t>(want, sms * per_sm);
         append_kernel<int64_t><<<unsigned(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    }
     return cuda_status(cudaGetLastError());
 }
 
@@ -394,27 +497,29 @@ extern "C" int paged_kv_append_rope(const void* q, void* q_out, const void* k, c
     p.max_position = max_position;
     p.num_slots = int64_t(desc->num_blocks) * desc->block_size;
     p.err = err;
-    const int64_t total = int64_t(num_tokens) * (desc->head_dim / 16);   // (token, chunk) pairs
-    const int64_t blocks = std::min<int64_t>((total + 255) / 256, int64_t(std::max(num_sms(), 1)) * 8);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool bf = desc->dtype == PKV_BF16;
+    const int rows_per_thread = bf ? rope_rows_per_thread<__nv_bfloat16>() : rope_rows_per_thread<float>();
+    const int64_t groups = (p.num_q_rows + 2 * int64_t(p.num_kv_heads) + rows_per_thread - 1) /
+                           rows_per_thread;
+    // (token, row group, chunk) triples
+    const int64_t total = int64_t(num_tokens) * groups * (desc->head_dim / 16);
     const bool narrow = total < (int64_t(1) << 31);
     if (desc->head_dim == 128) {
         if (bf) {
-            if (narrow) append_rope_kernel<__nv_bfloat16, 128, uint32_t><<<unsigned(blocks), 256, 0, s>>>(p);
-            else append_rope_kernel<__nv_bfloat16, 128, int64_t><<<unsigned(blocks), 256, 0, s>>>(p);
+            if (narrow) st = launch_rope<__nv_bfloat16, 128, uint32_t>(p, total, stream);
+            else st = launch_rope<__nv_bfloat16, 128, int64_t>(p, total, stream);
         } else {
-            if (narrow) append_rope_kernel<float, 128, uint32_t><<<unsigned(blocks), 256, 0, s>>>(p);
-            else append_rope_kernel<float, 128, int64_t><<<unsigned(blocks), 256, 0, s>>>(p);
+            if (narrow) st = launch_rope<float, 128, uint32_t>(p, total, stream);
+            else st = launch_rope<float, 128, int64_t>(p, total, stream);
         }
     } else {
         if (bf) {
-            if (narrow) append_rope_kernel<__nv_bfloat16, 64, uint32_t><<<unsigned(blocks), 256, 0, s>>>(p);
-            else append_rope_kernel<__nv_bfloat16, 64, int64_t><<<unsigned(blocks), 256, 0, s>>>(p);
+            if (narrow) st = launch_rope<__nv_bfloat16, 64, uint32_t>(p, total, stream);
+            else st = launch_rope<__nv_bfloat16, 64, int64_t>(p, total, stream);
         } else {
-            if (narrow) append_rope_kernel<float, 64, uint32_t><<<unsigned(blocks), 256, 0, s>>>(p);
-            else append_rope_kernel<float, 64, int64_t><<<unsigned(blocks), 256, 0, s>>>(p);
+            if (narrow) st = launch_rope<float, 64, uint32_t>(p, total, stream);
+            else st = launch_rope<float, 64, int64_t>(p, total, stream);
         }
     }
-    return cuda_status(cudaGetLastError());
+    return st;
 }

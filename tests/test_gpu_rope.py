@@ -105,3 +105,74 @@ def test_bad_rotary_position_is_flagged(lib):
     paged_kv_append_rope(k, k, slots, pos, tab, kc, vc, desc)
     assert lib.device_error() == 8                                  # PKV_DEV_BAD_POSITION
     assert torch.count_nonzero(kc) == 0                             # K row skipped
+
+
+def _dev(x, dtype):
+    return _torch_rows(x, dtype).to("cuda")
+
+
+def _host_bits(t, dtype):
+    t = t.cpu()
+    return t.numpy() if dtype == "f32" else t.view(torch.int16).numpy().view(np.uint16)
+
+
+# Head counts whose rows (q heads + 2 x KV heads) leave the kernel's last row
+# group part-filled (8 rows a thread for bf16, 4 for f32), with padding tokens,
+# and the form without q.
+@pytest.mark.parametrize("dtype,hq,hkv,d,with_q", [("bf16", 6, 3, 128, True),
+                                                  ("bf16", 10, 5, 64, False),
+                                                  ("f32", 3, 1, 64, True),
+                                                  ("bf16", 32, 8, 128, True)])
+def test_append_rope_ragged_row_groups_and_padding(lib, dtype, hq, hkv, d, with_q):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_51_gb300 import cache_desc, paged_kv_append_rope
+
+    nb, bs, max_pos, T = 400, 16, 2048, 3000
+    q, k, v, slots, pos = workloads.append_inputs(41 + hq, dtype, T, hq if with_q else 0, hkv, d,
+                                                  nb * bs, max_pos, pad_every=7)
+    tab = rope.rope_table(max_pos, d)
+    sdt = np.float32 if dtype == "f32" else np.uint16
+    ok = np.zeros((nb, hkv, bs, d), dtype=sdt)
+    ov = np.zeros_like(ok)
+    q_ref = rope.append_rope(ok, ov, q, k, v, slots, pos, tab, bs, dtype, cache.append)
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    kc = torch.zeros((nb, hkv, bs, d), dtype=tdt, device="cuda")
+    vc = torch.zeros_like(kc)
+    desc = cache_desc(kc, hq)
+    q_d = _dev(q, dtype) if with_q else None
+    q_out = torch.empty_like(q_d) if with_q else None
+    lib.device_error(clear=True)
+    paged_kv_append_rope(_dev(k, dtype), _dev(v, dtype), torch.from_numpy(slots).cuda(),
+                         torch.from_numpy(pos).cuda(), torch.from_numpy(tab).cuda(), kc, vc, desc,
+                         q=q_d, q_out=q_out)
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0
+    assert cache_bytes_equal(kc, ok)
+    assert cache_bytes_equal(vc, ov)
+    if with_q:
+        assert np.array_equal(_host_bits(q_out, dtype).view(np.uint8),
+                              np.ascontiguousarray(q_ref).view(np.uint8))
+
+
+def test_plain_append_several_grid_passes(lib):
+    # 6000 tokens x 8 KV heads x 16 vectors: more 16-byte vectors than one
+    # unrolled pass of the resident grid covers, with padding tokens
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_51_gb300 import cache_desc, paged_kv_append
+
+    nb, bs, hkv, d, T = 600, 16, 8, 128, 6000
+    _, k, v, slots, _ = workloads.append_inputs(43, "bf16", T, 0, hkv, d, nb * bs, 1, pad_every=5)
+    ok = np.zeros((nb, hkv, bs, d), dtype=np.uint16)
+    ov = np.zeros_like(ok)
+    cache.append(ok, ov, k, v, slots, bs)
+    kc = torch.zeros((nb, hkv, bs, d), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    lib.device_error(clear=True)
+    paged_kv_append(_dev(k, "bf16"), _dev(v, "bf16"), torch.from_numpy(slots).cuda(), kc, vc,
+                    cache_desc(kc, hkv))
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0
+    assert cache_bytes_equal(kc, ok)
+    assert cache_bytes_equal(vc, ov)

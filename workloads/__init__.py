@@ -261,6 +261,24 @@ def random_varlen(seed, dtype, hq, hkv, d, bs, spans, scale=1.0, slack=0.1):
                     notes={"context_lens": [p + qn for p, qn in spans]})
 
 
+def append_inputs(seed, dtype, num_tokens, hq, hkv, d, num_slots, max_pos, pad_every=0,
+                  scale=1.0):
+    """Inputs of one (rotary) append, for edge-case tests of the append kernels.
+
+    q [T, hq, d] (None when hq is 0), k, v [T, hkv, d] in the storage dtype;
+    slots: T distinct slots drawn from [0, num_slots), every pad_every-th token
+    padding (-1) when pad_every > 0; positions drawn from [0, max_pos)."""
+    rng = np.random.default_rng(seed)
+    q = _values(rng, (num_tokens, hq, d), dtype, scale) if hq > 0 else None
+    k = _values(rng, (num_tokens, hkv, d), dtype, scale)
+    v = _values(rng, (num_tokens, hkv, d), dtype, scale)
+    slots = rng.permutation(num_slots)[:num_tokens].astype(np.int64)
+    if pad_every > 0:
+        slots[::pad_every] = -1
+    positions = rng.integers(0, max_pos, size=num_tokens).astype(np.int32)
+    return q, k, v, slots, positions
+
+
 @dataclass
 class ServingTrace:
     """Requests for a multi-step run: prompt length, tokens to generate, the step at
