@@ -113,9 +113,9 @@ def lib():
         "pkv_device_error": (ctypes.c_int, [P(i32), i32]),
         "pkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "pkv_splitfuse_compose": (ctypes.c_int, [i32, i32, i32, p, p, P(i32), P(i32)]),
-        "paged_kv_append_int8": (ctypes.c_int, [p, p, p, i32, p, p, p, p, P(CacheDesc), p]),
-        "pkv_copy_blocks_int8": (ctypes.c_int, [p, i32, p, p, p, p, P(CacheDesc), p]),
-        "paged_attention_decode_int8": (ctypes.c_int, [p, p, p, p, p, p, P(CacheDesc), p, i32, p,
+        "paged_kv_append_int8": (ctypes.c_int, [p, p, p, i32, p, p, P(CacheDesc), p]),
+        "pkv_copy_blocks_int8": (ctypes.c_int, [p, i32, p, p, P(CacheDesc), p]),
+        "paged_attention_decode_int8": (ctypes.c_int, [p, p, p, p, P(CacheDesc), p, i32, p,
                                                        i32, i32, ctypes.c_float, p, sz, p]),
     }
     for name, (res, args) in sig.items():
@@ -440,30 +440,47 @@ def paged_attention_varlen(out, q, k_cache, v_cache, desc, block_tables, query_s
     return out
 
 
+def int8_tile_bytes(head_dim, block_size=16):
+    """Bytes of one (block, KV head) tile of the 8-bit cache: codes, then scales."""
+    return block_size * head_dim + block_size * 4
+
+
 class Int8Cache:
-    """The four pools of an 8-bit KV cache: codes int8 [NB, Hkv, bs, D] and
-    scales fp32 [NB, Hkv, bs], for K and for V (see paged_kv_append_int8 in
-    include/pagedkv.h for the format)."""
+    """The two pools of an 8-bit KV cache, K and V: uint8 [NB, Hkv, tile], one
+    tile per (block, KV head) holding its bs x D codes and then their bs fp32
+    scales (see paged_kv_append_int8 in include/pagedkv.h for the format).
+    k_codes / v_codes (int8 [NB, Hkv, bs, D]) and k_scales / v_scales (fp32
+    [NB, Hkv, bs]) are views into the pools."""
 
     def __init__(self, num_blocks, num_kv_heads, block_size, head_dim, num_q_heads,
                  device="cuda"):
-        shape = (num_blocks, num_kv_heads, block_size, head_dim)
-        self.k_codes = torch.zeros(shape, dtype=torch.int8, device=device)
-        self.v_codes = torch.zeros(shape, dtype=torch.int8, device=device)
-        self.k_scales = torch.zeros(shape[:3], dtype=torch.float32, device=device)
-        self.v_scales = torch.zeros(shape[:3], dtype=torch.float32, device=device)
+        tile = int8_tile_bytes(head_dim, block_size)
+        ncode = block_size * head_dim
+        self.k_pool = torch.zeros((num_blocks, num_kv_heads, tile), dtype=torch.uint8,
+                                  device=device)
+        self.v_pool = torch.zeros_like(self.k_pool)
+        self.k_codes, self.k_scales = self._views(self.k_pool, ncode, block_size, head_dim)
+        self.v_codes, self.v_scales = self._views(self.v_pool, ncode, block_size, head_dim)
         self.desc = CacheDesc(PKV_INT8, num_blocks, block_size, num_kv_heads, num_q_heads,
                               head_dim)
 
+    @staticmethod
+    def _views(pool, ncode, block_size, head_dim):
+        codes = pool[:, :, :ncode].view(torch.int8).unflatten(-1, (block_size, head_dim))
+        scales = pool[:, :, ncode:].view(torch.float32)
+        return codes, scales
+
     def tensors(self):
-        return self.k_codes, self.v_codes, self.k_scales, self.v_scales
+        return self.k_pool, self.v_pool
 
 
 def _need_int8_cache(c):
-    for t, dt, nm in ((c.k_codes, torch.int8, "k_codes"), (c.v_codes, torch.int8, "v_codes"),
-                      (c.k_scales, torch.float32, "k_scales"),
-                      (c.v_scales, torch.float32, "v_scales")):
-        _need(t, dt, nm)
+    d = c.desc
+    shape = (d.num_blocks, d.num_kv_heads, int8_tile_bytes(d.head_dim, d.block_size))
+    for t, nm in ((c.k_pool, "k_pool"), (c.v_pool, "v_pool")):
+        _need(t, torch.uint8, nm)
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{nm}: shape {tuple(t.shape)}, expected {shape}")
 
 
 def paged_kv_append_int8(k, v, slot_mapping, cache, stream=None):
@@ -474,8 +491,7 @@ def paged_kv_append_int8(k, v, slot_mapping, cache, stream=None):
     _need(slot_mapping, torch.int64, "slot_mapping")
     _need_int8_cache(cache)
     _check(lib().paged_kv_append_int8(_ptr(k), _ptr(v), _ptr(slot_mapping), k.shape[0],
-                                      _ptr(cache.k_codes), _ptr(cache.v_codes),
-                                      _ptr(cache.k_scales), _ptr(cache.v_scales),
+                                      _ptr(cache.k_pool), _ptr(cache.v_pool),
                                       ctypes.byref(cache.desc), _stream(stream)),
            "paged_kv_append_int8")
 
@@ -487,9 +503,8 @@ def pkv_copy_blocks_int8(block_pairs, cache, stream=None):
         return
     _need(block_pairs, torch.int32, "block_pairs")
     _need_int8_cache(cache)
-    _check(lib().pkv_copy_blocks_int8(_ptr(block_pairs), n, _ptr(cache.k_codes),
-                                      _ptr(cache.v_codes), _ptr(cache.k_scales),
-                                      _ptr(cache.v_scales), ctypes.byref(cache.desc),
+    _check(lib().pkv_copy_blocks_int8(_ptr(block_pairs), n, _ptr(cache.k_pool),
+                                      _ptr(cache.v_pool), ctypes.byref(cache.desc),
                                       _stream(stream)), "pkv_copy_blocks_int8")
 
 
@@ -507,9 +522,8 @@ def paged_attention_decode_int8(out, q, cache, block_tables, context_lens, max_c
         scale = 1.0 / math.sqrt(desc.head_dim)
     if ws is None:
         ws = workspace(decode_workspace_bytes(desc, S, max_context_len), q.device)
-    _check(lib().paged_attention_decode_int8(_ptr(out), _ptr(q), _ptr(cache.k_codes),
-                                             _ptr(cache.v_codes), _ptr(cache.k_scales),
-                                             _ptr(cache.v_scales), ctypes.byref(desc),
+    _check(lib().paged_attention_decode_int8(_ptr(out), _ptr(q), _ptr(cache.k_pool),
+                                             _ptr(cache.v_pool), ctypes.byref(desc),
                                              _ptr(block_tables), block_tables.shape[1],
                                              _ptr(context_lens), S, max_context_len, scale,
                                              _ptr(ws), ws.numel(), _stream(stream)),

@@ -419,45 +419,37 @@ extern "C" int pkv_copy_blocks(const int32_t* block_pairs, int32_t num_pairs, vo
     return cuda_status(cudaGetLastError());
 }
 
-extern "C" int pkv_copy_blocks_int8(const int32_t* block_pairs, int32_t num_pairs,
-                                    void* k_codes, void* v_codes, float* k_scales,
-                                    float* v_scales, const pkv_cache_desc* desc, void* stream) {
+extern "C" int pkv_copy_blocks_int8(const int32_t* block_pairs, int32_t num_pairs, void* k_pool,
+                                    void* v_pool, const pkv_cache_desc* desc, void* stream) {
     if (!desc) return PKV_ERR_INVALID;
     if (desc->dtype != PKV_INT8) return PKV_ERR_UNSUPPORTED;
     pkv_cache_desc bd = *desc;
     bd.dtype = PKV_BF16;
     int st = check_desc(&bd, false);
     if (st != PKV_OK) return st;
+    if (desc->block_size != 16) return PKV_ERR_UNSUPPORTED;   // the tile layout is 16 rows
     if (num_pairs < 0) return PKV_ERR_INVALID;
     if (num_pairs == 0) return PKV_OK;
     if (num_pairs > 65535) return PKV_ERR_UNSUPPORTED;
-    if (!block_pairs || !k_codes || !v_codes || !k_scales || !v_scales || !aligned16(k_codes) ||
-        !aligned16(v_codes) || !aligned16(k_scales) || !aligned16(v_scales) ||
+    if (!block_pairs || !k_pool || !v_pool || !aligned16(k_pool) || !aligned16(v_pool) ||
         (reinterpret_cast<uintptr_t>(block_pairs) & 3u))
         return PKV_ERR_INVALID;
-    const int64_t rows = int64_t(desc->num_kv_heads) * desc->block_size;   // per block
-    const int64_t code_bytes = rows * desc->head_dim, scale_bytes = rows * 4;
-    if (code_bytes % 16 || scale_bytes % 16) return PKV_ERR_UNSUPPORTED;
+    // whole blocks as bytes: every KV head's tile of codes and scales
+    const int64_t tile_bytes = int64_t(desc->block_size) * desc->head_dim + desc->block_size * 4;
+    const int64_t block_bytes = int64_t(desc->num_kv_heads) * tile_bytes;
+    if (block_bytes % 16) return PKV_ERR_UNSUPPORTED;
     int* err = device_error_ptr(&st);
     if (st != PKV_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // whole blocks as bytes: codes, then scales (the tile layout depends only on the row)
-    const int64_t bytes[2] = {code_bytes, scale_bytes};
-    void* kp[2] = {k_codes, k_scales};
-    void* vp[2] = {v_codes, v_scales};
-    for (int i = 0; i < 2; ++i) {
-        CopyParams p;
-        p.pairs = block_pairs;
-        p.k_cache = static_cast<uint4*>(kp[i]);
-        p.v_cache = static_cast<uint4*>(vp[i]);
-        p.vec_per_block = bytes[i] / 16;
-        p.num_blocks = desc->num_blocks;
-        p.err = err;
-        const unsigned gx = unsigned(std::min<int64_t>((p.vec_per_block + 255) / 256, 64));
-        copy_blocks_kernel<<<dim3(gx, unsigned(num_pairs)), 256, 0, s>>>(p);
-        if ((st = cuda_status(cudaGetLastError())) != PKV_OK) return st;
-    }
-    return PKV_OK;
+    CopyParams p;
+    p.pairs = block_pairs;
+    p.k_cache = static_cast<uint4*>(k_pool);
+    p.v_cache = static_cast<uint4*>(v_pool);
+    p.vec_per_block = block_bytes / 16;
+    p.num_blocks = desc->num_blocks;
+    p.err = err;
+    const unsigned gx = unsigned(std::min<int64_t>((p.vec_per_block + 255) / 256, 64));
+    copy_blocks_kernel<<<dim3(gx, unsigned(num_pairs)), 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    return cuda_status(cudaGetLastError());
 }
 
 extern "C" int paged_kv_append_rope(const void* q, void* q_out, const void* k, const void* v,

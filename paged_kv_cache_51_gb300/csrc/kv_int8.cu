@@ -7,12 +7,14 @@
 // (code = 0, scale = 0 for an all-zero row), each division rounded once in
 // fp32, so the stored codes are reproducible exactly.
 //
-// Tile layout.  One (block, KV head) tile holds 16 tokens.  K codes are
-// row-major [token][D] with the 16-byte chunks of row r XOR-swizzled
-// (chunk c stored at c ^ sw(r), sw(r) = r & 7 for D = 128 and (r >> 1) & 3 for
-// D = 64); V codes are dim-major [D][token].  Scales are [token] fp32.  Both
-// code layouts let a warp load its tensor-core fragments as 32-bit words with
-// no shared-memory bank conflicts.
+// Tile layout.  One (block, KV head) tile holds 16 tokens: their 16 * D codes,
+// then their 16 fp32 scales, in one contiguous run of 16 * D + 64 bytes, so a
+// decode stage is one bulk copy for K and one for V (the scales as separate
+// 64-byte copies cost 13 % of the call).  K codes are row-major [token][D] with
+// the 16-byte chunks of row r XOR-swizzled (chunk c stored at c ^ sw(r),
+// sw(r) = r & 7 for D = 128 and (r >> 1) & 3 for D = 64); V codes are
+// dim-major [D][token].  Both code layouts let a warp load its tensor-core
+// fragments as 32-bit words with no shared-memory bank conflicts.
 //
 // Decode runs both products on tensor cores (mma.sync m16n8k16, f16 in, fp32
 // accumulate), which keeps the kernel on the HBM roofline for every group size:
@@ -42,6 +44,12 @@
 namespace pkv {
 namespace {
 
+// bytes of one (block, KV head) tile: codes, then scales
+template <int D>
+__host__ __device__ constexpr int i8_tile_bytes() {
+    return kBlockTokens * D + kBlockTokens * 4;
+}
+
 // 16-byte chunk swizzle of the K tile row r
 template <int D>
 __host__ __device__ constexpr int k_swizzle(int r) {
@@ -56,10 +64,8 @@ struct AppendI8Params {
     const __nv_bfloat16* k;
     const __nv_bfloat16* v;
     const int64_t* slots;
-    int8_t* k_codes;
-    int8_t* v_codes;
-    float* k_scales;
-    float* v_scales;
+    unsigned char* k_pool;
+    unsigned char* v_pool;
     int64_t num_tokens;
     int32_t num_kv_heads;
     int32_t block_size;
@@ -111,12 +117,12 @@ __global__ void __launch_bounds__(256) append_int8_kernel(AppendI8Params p) {
         }
         const int64_t blk = slot / p.block_size;
         const int rr = int(slot - blk * p.block_size);           // token row within the tile
-        const int64_t tile = blk * p.num_kv_heads + h;
+        unsigned char* tile =
+            (is_v ? p.v_pool : p.k_pool) + (blk * p.num_kv_heads + h) * i8_tile_bytes<D>();
         if (!is_v) {
             // row-major, 16-byte chunk (lane * DPL) / 16 swizzled by the row
             const int d0 = lane * DPL;
-            int8_t* dst = p.k_codes + tile * (kBlockTokens * D) + rr * D +
-                          (((d0 >> 4) ^ k_swizzle<D>(rr)) << 4) + (d0 & 15);
+            unsigned char* dst = tile + rr * D + (((d0 >> 4) ^ k_swizzle<D>(rr)) << 4) + (d0 & 15);
             uint32_t packed = 0;
 #pragma unroll
             for (int i = 0; i < DPL; ++i) packed |= (uint32_t(code[i]) & 0xffu) << (8 * i);
@@ -127,11 +133,12 @@ __global__ void __launch_bounds__(256) append_int8_kernel(AppendI8Params p) {
             }
         } else {
             // dim-major: byte (d, rr) at d * 16 + rr
-            int8_t* dst = p.v_codes + tile * (kBlockTokens * D) + rr;
+            unsigned char* dst = tile + rr;
 #pragma unroll
-            for (int i = 0; i < DPL; ++i) dst[(lane * DPL + i) * kBlockTokens] = int8_t(code[i]);
+            for (int i = 0; i < DPL; ++i)
+                dst[(lane * DPL + i) * kBlockTokens] = static_cast<unsigned char>(code[i] & 0xff);
         }
-        if (lane == 0) (is_v ? p.v_scales : p.k_scales)[tile * kBlockTokens + rr] = scale;
+        if (lane == 0) reinterpret_cast<float*>(tile + kBlockTokens * D)[rr] = scale;
     }
 }
 
@@ -141,10 +148,8 @@ __global__ void __launch_bounds__(256) append_int8_kernel(AppendI8Params p) {
 struct SplitI8Params {
     const __nv_bfloat16* q;
     __nv_bfloat16* out;
-    const int8_t* k_codes;
-    const int8_t* v_codes;
-    const float* k_scales;
-    const float* v_scales;
+    const unsigned char* k_pool;
+    const unsigned char* v_pool;
     const int32_t* block_tables;
     const int32_t* context_lens;
     const int2* items;
@@ -166,11 +171,15 @@ struct I8Cfg {
     static constexpr int kWarps = 4;
     static constexpr int kThreads = (kWarps + 1) * 32;
     static constexpr int kKB = D / 16;                       // 16-dim blocks
-    static constexpr int kTileBytes = kBlockTokens * D;      // codes of one (block, head)
-    static constexpr int kScaleBytes = kBlockTokens * 4;     // their scales
-    // stage: [K codes][V codes][K scales][V scales]
-    static constexpr int kStageBytes = 2 * kTileBytes + 2 * kScaleBytes;
+    static constexpr int kCodeBytes = kBlockTokens * D;      // codes of one (block, head)
+    static constexpr int kTileBytes = i8_tile_bytes<D>();    // codes + their scales
+    // stage: [K codes][K scales][V codes][V scales], the two tiles as stored
+    static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kStages = 8;
+    // resident CTAs per SM the register allocation must allow (the compiler
+    // otherwise takes 109 registers for D = 128, g = 1, and a fourth CTA no
+    // longer fits: 0.2406 -> 0.264 ms on the Llama-2-7B batch)
+    static constexpr int kMinBlocks = D == 128 ? 4 : 5;
     static constexpr int kPB = 8 * kBlockTokens * 2;         // P' per warp: f16 [8 heads][16 tokens]
     static constexpr int kComb = G * (D + 2);
     static constexpr int kQBytes = G * D * 2;                // q of one unit (bf16)
@@ -183,7 +192,7 @@ struct I8Cfg {
     // full[kStages], empty[kStages], q_full[kQSlots], q_empty[kQSlots]
     static constexpr int kQueueOff = kBarOff + (2 * kStages + 2 * kQSlots) * 8;
     static constexpr int kSmem = kQueueOff + int(sizeof(UnitQueue));
-    static_assert(kStageBytes % 16 == 0 && kTileBytes % 16 == 0, "bulk copy alignment");
+    static_assert(kStageBytes % 128 == 0 && kTileBytes % 16 == 0, "bulk copy alignment");
     // Consumer warp w takes tiles w, w + kWarps, ... of a unit and waits on a
     // stage by parity alone.  With kStages a multiple of kWarps the previous use
     // of that stage is the same warp's own (finished) tile; otherwise it can be
@@ -219,7 +228,8 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1,
 __device__ __forceinline__ float exp2i(int k) { return __uint_as_float(uint32_t(127 + k) << 23); }
 
 template <int D, int G>
-__global__ void __launch_bounds__(I8Cfg<D, G>::kThreads) decode_split_int8_kernel(SplitI8Params p) {
+__global__ void __launch_bounds__(I8Cfg<D, G>::kThreads, I8Cfg<D, G>::kMinBlocks)
+    decode_split_int8_kernel(SplitI8Params p) {
     using C = I8Cfg<D, G>;
     constexpr int KB = C::kKB;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -294,13 +304,9 @@ __global__ void __launch_bounds__(I8Cfg<D, G>::kThreads) decode_split_int8_kerne
                         mbar_arrive_expect_tx(&full[st], C::kStageBytes);
                         const size_t row = size_t(blk) * Hkv + kvh;
                         unsigned char* dst = smem + size_t(st) * C::kStageBytes;
-                        bulk_g2s(dst, p.k_codes + row * C::kTileBytes, C::kTileBytes, &full[st]);
-                        bulk_g2s(dst + C::kTileBytes, p.v_codes + row * C::kTileBytes,
+                        bulk_g2s(dst, p.k_pool + row * C::kTileBytes, C::kTileBytes, &full[st]);
+                        bulk_g2s(dst + C::kTileBytes, p.v_pool + row * C::kTileBytes,
                                  C::kTileBytes, &full[st]);
-                        bulk_g2s(dst + 2 * C::kTileBytes, p.k_scales + row * kBlockTokens,
-                                 C::kScaleBytes, &full[st]);
-                        bulk_g2s(dst + 2 * C::kTileBytes + C::kScaleBytes,
-                                 p.v_scales + row * kBlockTokens, C::kScaleBytes, &full[st]);
                     }
                 }
                 __syncwarp();
@@ -380,8 +386,8 @@ __global__ void __launch_bounds__(I8Cfg<D, G>::kThreads) decode_split_int8_kerne
             const unsigned char* sb = smem + size_t(st) * C::kStageBytes;
             const unsigned char* kt = sb;
             const unsigned char* vt = sb + C::kTileBytes;
-            const float* ksc = reinterpret_cast<const float*>(sb + 2 * C::kTileBytes);
-            const float* vsc = ksc + kBlockTokens;
+            const float* ksc = reinterpret_cast<const float*>(kt + C::kCodeBytes);
+            const float* vsc = reinterpret_cast<const float*>(vt + C::kCodeBytes);
             const int nvalid = min(kBlockTokens, ctx - (b0 + jb) * kBlockTokens);
 
             // S = K q^T: rows tokens g, g + 8; columns heads 2t, 2t + 1
@@ -523,8 +529,7 @@ __global__ void __launch_bounds__(I8Cfg<D, G>::kThreads) decode_split_int8_kerne
 bool aligned(const void* q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) & (a - 1)) == 0; }
 
 template <int D, int G>
-int launch_i8(const AttnArgs& a, const int8_t* kc, const int8_t* vc, const float* ks,
-              const float* vs) {
+int launch_i8(const AttnArgs& a, const unsigned char* kp, const unsigned char* vp) {
     using C = I8Cfg<D, G>;
     auto kern = decode_split_int8_kernel<D, G>;
     const int per_sm = kernel_occupancy<decode_split_int8_kernel<D, G>>(C::kThreads, C::kSmem);
@@ -535,10 +540,8 @@ int launch_i8(const AttnArgs& a, const int8_t* kc, const int8_t* vc, const float
     SplitI8Params p;
     p.q = static_cast<const __nv_bfloat16*>(a.q);
     p.out = static_cast<__nv_bfloat16*>(a.out);
-    p.k_codes = kc;
-    p.v_codes = vc;
-    p.k_scales = ks;
-    p.v_scales = vs;
+    p.k_pool = kp;
+    p.v_pool = vp;
     p.block_tables = a.block_tables;
     p.context_lens = a.context_lens;
     p.items = a.ws.items;
@@ -567,13 +570,12 @@ int launch_i8(const AttnArgs& a, const int8_t* kc, const int8_t* vc, const float
 }
 
 template <int D>
-int launch_i8_d(const AttnArgs& a, int g, const int8_t* kc, const int8_t* vc, const float* ks,
-                const float* vs) {
+int launch_i8_d(const AttnArgs& a, int g, const unsigned char* kp, const unsigned char* vp) {
     switch (g) {
-        case 1: return launch_i8<D, 1>(a, kc, vc, ks, vs);
-        case 2: return launch_i8<D, 2>(a, kc, vc, ks, vs);
-        case 4: return launch_i8<D, 4>(a, kc, vc, ks, vs);
-        case 8: return launch_i8<D, 8>(a, kc, vc, ks, vs);
+        case 1: return launch_i8<D, 1>(a, kp, vp);
+        case 2: return launch_i8<D, 2>(a, kp, vp);
+        case 4: return launch_i8<D, 4>(a, kp, vp);
+        case 8: return launch_i8<D, 8>(a, kp, vp);
         default: return PKV_ERR_UNSUPPORTED;
     }
 }
@@ -584,9 +586,8 @@ int launch_i8_d(const AttnArgs& a, int g, const int8_t* kc, const int8_t* vc, co
 using namespace pkv;
 
 extern "C" int paged_kv_append_int8(const void* k, const void* v, const int64_t* slot_mapping,
-                                    int32_t num_tokens, void* k_codes, void* v_codes,
-                                    float* k_scales, float* v_scales, const pkv_cache_desc* desc,
-                                    void* stream) {
+                                    int32_t num_tokens, void* k_pool, void* v_pool,
+                                    const pkv_cache_desc* desc, void* stream) {
     if (!desc) return PKV_ERR_INVALID;
     if (desc->dtype != PKV_INT8) return PKV_ERR_UNSUPPORTED;
     pkv_cache_desc bd = *desc;
@@ -597,10 +598,9 @@ extern "C" int paged_kv_append_int8(const void* k, const void* v, const int64_t*
     if (desc->block_size != kBlockTokens) return PKV_ERR_UNSUPPORTED;   // the tile layout is 16 rows
     if (num_tokens < 0) return PKV_ERR_INVALID;
     if (num_tokens == 0) return PKV_OK;
-    if (!k || !v || !slot_mapping || !k_codes || !v_codes || !k_scales || !v_scales)
-        return PKV_ERR_INVALID;
-    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_codes, 16) || !aligned(v_codes, 16) ||
-        !aligned(k_scales, 16) || !aligned(v_scales, 16) || !aligned(slot_mapping, 8))
+    if (!k || !v || !slot_mapping || !k_pool || !v_pool) return PKV_ERR_INVALID;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+        !aligned(slot_mapping, 8))
         return PKV_ERR_INVALID;
     int* err = device_error_ptr(&st);
     if (st != PKV_OK) return st;
@@ -608,10 +608,8 @@ extern "C" int paged_kv_append_int8(const void* k, const void* v, const int64_t*
     p.k = static_cast<const __nv_bfloat16*>(k);
     p.v = static_cast<const __nv_bfloat16*>(v);
     p.slots = slot_mapping;
-    p.k_codes = static_cast<int8_t*>(k_codes);
-    p.v_codes = static_cast<int8_t*>(v_codes);
-    p.k_scales = k_scales;
-    p.v_scales = v_scales;
+    p.k_pool = static_cast<unsigned char*>(k_pool);
+    p.v_pool = static_cast<unsigned char*>(v_pool);
     p.num_tokens = num_tokens;
     p.num_kv_heads = desc->num_kv_heads;
     p.block_size = desc->block_size;
@@ -627,9 +625,8 @@ extern "C" int paged_kv_append_int8(const void* k, const void* v, const int64_t*
     return cuda_status(cudaGetLastError());
 }
 
-extern "C" int paged_attention_decode_int8(void* out, const void* q, const void* k_codes,
-                                           const void* v_codes, const float* k_scales,
-                                           const float* v_scales, const pkv_cache_desc* desc,
+extern "C" int paged_attention_decode_int8(void* out, const void* q, const void* k_pool,
+                                           const void* v_pool, const pkv_cache_desc* desc,
                                            const int32_t* block_tables, int32_t max_blocks_per_seq,
                                            const int32_t* context_lens, int32_t num_seqs,
                                            int32_t max_context_len, float scale, void* workspace,
@@ -644,12 +641,9 @@ extern "C" int paged_attention_decode_int8(void* out, const void* q, const void*
     if (num_seqs < 0 || max_blocks_per_seq < 1 || max_context_len < 1) return PKV_ERR_INVALID;
     if (!std::isfinite(scale)) return PKV_ERR_INVALID;
     if (num_seqs == 0) return PKV_OK;
-    if (!out || !q || !k_codes || !v_codes || !k_scales || !v_scales || !block_tables ||
-        !context_lens)
-        return PKV_ERR_INVALID;
-    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_codes, 16) || !aligned(v_codes, 16) ||
-        !aligned(k_scales, 16) || !aligned(v_scales, 16) || !aligned(block_tables, 4) ||
-        !aligned(context_lens, 4))
+    if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens) return PKV_ERR_INVALID;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4))
         return PKV_ERR_INVALID;
     const size_t need = pkv_decode_workspace_bytes(&qd, num_seqs, max_context_len);
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return PKV_ERR_WORKSPACE;
@@ -671,10 +665,9 @@ extern "C" int paged_attention_decode_int8(void* out, const void* q, const void*
     a.stream = static_cast<cudaStream_t>(stream);
     if ((st = launch_plan(a)) != PKV_OK) return st;
     const int g = qd.num_q_heads / qd.num_kv_heads;
-    const auto* kc = static_cast<const int8_t*>(k_codes);
-    const auto* vc = static_cast<const int8_t*>(v_codes);
-    st = qd.head_dim == 128 ? launch_i8_d<128>(a, g, kc, vc, k_scales, v_scales)
-                            : launch_i8_d<64>(a, g, kc, vc, k_scales, v_scales);
+    const auto* kp = static_cast<const unsigned char*>(k_pool);
+    const auto* vp = static_cast<const unsigned char*>(v_pool);
+    st = qd.head_dim == 128 ? launch_i8_d<128>(a, g, kp, vp) : launch_i8_d<64>(a, g, kp, vp);
     if (st != PKV_OK) return st;
     return launch_decode_merge(a);
 }

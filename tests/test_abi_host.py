@@ -180,34 +180,44 @@ def test_int8_entry_points_validate_on_the_host(lib):
     fake = ctypes.c_void_p(1 << 20)
     # the split partials do not depend on the cache type
     assert lib.decode_workspace_bytes(i8, 64, 4096) == lib.decode_workspace_bytes(bf, 64, 4096)
+    # a tile is the 16 rows' codes and then their fp32 scales
+    assert lib.int8_tile_bytes(128) == 16 * 128 + 64 and lib.int8_tile_bytes(64) == 1088
     # the 8-bit calls take only PKV_INT8, the others never take it
-    assert L.paged_kv_append_int8(fake, fake, fake, 4, fake, fake, fake, fake, ref(bf),
+    assert L.paged_kv_append_int8(fake, fake, fake, 4, fake, fake, ref(bf),
                                   None) == lib.PKV_ERR_UNSUPPORTED
-    assert L.paged_attention_decode_int8(fake, fake, fake, fake, fake, fake, ref(bf), fake, 4,
+    assert L.paged_attention_decode_int8(fake, fake, fake, fake, ref(bf), fake, 4,
                                          fake, 1, 16, 0.1, fake, 1 << 20,
                                          None) == lib.PKV_ERR_UNSUPPORTED
     assert L.paged_kv_append(fake, fake, fake, 4, fake, fake, ref(i8), None) == \
         lib.PKV_ERR_UNSUPPORTED
     assert L.paged_attention_decode(fake, fake, fake, fake, ref(i8), fake, 4, fake, 1, 16, 0.1,
                                     fake, 1 << 20, None) == lib.PKV_ERR_UNSUPPORTED
-    # null pointers, misaligned scales, head_dim, workspace, empty work
-    assert L.paged_kv_append_int8(None, fake, fake, 4, fake, fake, fake, fake, ref(i8),
+    # null pointers, a misaligned pool, head_dim, workspace, empty work
+    assert L.paged_kv_append_int8(None, fake, fake, 4, fake, fake, ref(i8),
                                   None) == lib.PKV_ERR_INVALID
-    assert L.paged_kv_append_int8(fake, fake, fake, 4, fake, fake, ctypes.c_void_p((1 << 20) + 4),
-                                  fake, ref(i8), None) == lib.PKV_ERR_INVALID
+    assert L.paged_kv_append_int8(fake, fake, fake, 4, fake, None, ref(i8),
+                                  None) == lib.PKV_ERR_INVALID
+    assert L.paged_kv_append_int8(fake, fake, fake, 4, ctypes.c_void_p((1 << 20) + 4), fake,
+                                  ref(i8), None) == lib.PKV_ERR_INVALID
+    assert L.paged_attention_decode_int8(fake, fake, fake, ctypes.c_void_p((1 << 20) + 8),
+                                         ref(i8), fake, 4, fake, 1, 16, 0.1, fake, 1 << 20,
+                                         None) == lib.PKV_ERR_INVALID
     d96 = lib.CacheDesc(lib.PKV_INT8, 100, 16, 8, 32, 96)
-    assert L.paged_kv_append_int8(fake, fake, fake, 4, fake, fake, fake, fake, ref(d96),
+    assert L.paged_kv_append_int8(fake, fake, fake, 4, fake, fake, ref(d96),
                                   None) == lib.PKV_ERR_UNSUPPORTED
-    assert L.paged_attention_decode_int8(fake, fake, fake, fake, fake, fake, ref(i8), fake, 4,
+    assert L.paged_attention_decode_int8(fake, fake, fake, fake, ref(i8), fake, 4,
                                          fake, 64, 4096, 0.1, fake, 256,
                                          None) == lib.PKV_ERR_WORKSPACE
-    assert L.paged_attention_decode_int8(fake, fake, fake, fake, fake, fake, ref(i8), fake, 4,
+    assert L.paged_attention_decode_int8(fake, fake, fake, fake, ref(i8), fake, 4,
                                          fake, 1, 16, float("nan"), fake, 1 << 20,
                                          None) == lib.PKV_ERR_INVALID
-    assert L.paged_kv_append_int8(None, None, None, 0, None, None, None, None, ref(i8), None) == 0
-    # copy-on-write for the 8-bit cache takes only PKV_INT8
-    assert L.pkv_copy_blocks_int8(fake, 2, fake, fake, fake, fake, ref(bf), None) == \
+    assert L.paged_kv_append_int8(None, None, None, 0, None, None, ref(i8), None) == 0
+    # copy-on-write for the 8-bit cache takes only PKV_INT8, with 16-row tiles
+    assert L.pkv_copy_blocks_int8(fake, 2, fake, fake, ref(bf), None) == \
         lib.PKV_ERR_UNSUPPORTED
-    assert L.pkv_copy_blocks_int8(None, 2, fake, fake, fake, fake, ref(i8), None) == \
+    b8 = lib.CacheDesc(lib.PKV_INT8, 100, 8, 8, 32, 128)
+    assert L.pkv_copy_blocks_int8(fake, 2, fake, fake, ref(b8), None) == \
+        lib.PKV_ERR_UNSUPPORTED
+    assert L.pkv_copy_blocks_int8(None, 2, fake, fake, ref(i8), None) == \
         lib.PKV_ERR_INVALID
-    assert L.pkv_copy_blocks_int8(None, 0, None, None, None, None, ref(i8), None) == 0
+    assert L.pkv_copy_blocks_int8(None, 0, None, None, ref(i8), None) == 0
