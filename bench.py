@@ -11,7 +11,8 @@ larger than needed.
 
 value    = algorithmic bytes of the step / device time of the step (inputs resident)
 e2e      = the same bytes / time of a step that also copies its inputs from pinned
-           host memory and reads the output back
+           host memory and reads the output back, the copies on two copy streams
+           overlapping the neighbouring steps (e2e.serial: the same in series)
 roofline = the decode attention call (planner + split + merge) against the
            measured HBM copy bandwidth
 --impl reference runs the float64 CPU oracle on a bounded sample instead.
@@ -300,7 +301,10 @@ def job_throughput(bytes_per_rank, world, ms):
 
 
 def time_steps(step, steps, warmup):
-    """Device time of `steps` steps and the mean time of the attention call inside them."""
+    """Device time of `steps` steps (one event pair around the whole loop), then
+    the mean time of the attention call alone, from a second loop of the same
+    steps with an event pair around each call (the events inside a step cost
+    about 2 us of it, so they stay out of the first loop)."""
     import torch
 
     stream = torch.cuda.current_stream()
@@ -309,15 +313,18 @@ def time_steps(step, steps, warmup):
     torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        step.run()
+    ev1.record(stream)
+    torch.cuda.synchronize()
     a_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in range(steps)]
-    ev0.record(stream)
     for i in range(steps):
         step.write_kv()
         a_ev[i][0].record(stream)
         step.attend()
         a_ev[i][1].record(stream)
-    ev1.record(stream)
     torch.cuda.synchronize()
     return ev0.elapsed_time(ev1) / steps, statistics.mean(a.elapsed_time(b) for a, b in a_ev)
 
@@ -602,7 +609,11 @@ def run_gpu(args):
     # ---- end to end through host buffers ----
     # Every input of a step (q, the new K/V rows, slot mapping, copy pairs, block
     # tables, lengths) sits in one pinned host buffer and goes to the device in
-    # one copy; the step's device tensors are views into the device copy.
+    # one copy; the step's device tensors are views into the device copy, and
+    # its output is read back into pinned host memory.  As a serving loop does,
+    # the uploads run on one copy stream and the read-backs on another, with two
+    # device input buffers and two outputs, so step i + 1's inputs arrive while
+    # step i computes.  Every step's own copies are inside the timed region.
     names = ("q", "k_new", "v_new", "slot_mapping", "tables", "ctx", "qsl", "pairs")
     host_in = {name: getattr(step, name).cpu() for name in names}
     offs, total = {}, 0
@@ -610,33 +621,84 @@ def run_gpu(args):
         offs[name] = total
         total += (t.numel() * t.element_size() + 255) // 256 * 256
     host_buf = torch.empty(max(total, 256), dtype=torch.uint8).pin_memory()
-    dev_buf = torch.empty(max(total, 256), dtype=torch.uint8, device="cuda")
     for name, t in host_in.items():
         n = t.numel() * t.element_size()
         if n:
             host_buf[offs[name]:offs[name] + n].copy_(t.contiguous().view(-1).view(torch.uint8))
-        setattr(step, name, dev_buf[offs[name]:offs[name] + n].view(t.dtype).view(t.shape))
-    host_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    dev_bufs = [torch.empty(max(total, 256), dtype=torch.uint8, device="cuda") for _ in range(2)]
+    views = [{name: b[offs[name]:offs[name] + t.numel() * t.element_size()]
+              .view(t.dtype).view(t.shape) for name, t in host_in.items()} for b in dev_bufs]
+    outs = [step.out, torch.empty_like(step.out)]
+    host_outs = [torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory() for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = host_out.numel() * host_out.element_size()
+    d2h = host_outs[0].numel() * host_outs[0].element_size()
     k_e2e = max(3, min(args.steps, 200))
+    up_stream, down_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    uploaded = [torch.cuda.Event() for _ in range(2)]
+    ran = [torch.cuda.Event() for _ in range(2)]
+    read_back = [torch.cuda.Event() for _ in range(2)]
+    n_done = [0]
 
     def e2e_step():
-        dev_buf.copy_(host_buf, non_blocking=True)
+        b = n_done[0] & 1
+        n_done[0] += 1
+        up_stream.wait_event(ran[b])              # the last step on dev_bufs[b] is done
+        with torch.cuda.stream(up_stream):
+            dev_bufs[b].copy_(host_buf, non_blocking=True)
+        uploaded[b].record(up_stream)
+        stream.wait_event(uploaded[b])
+        stream.wait_event(read_back[b])           # outs[b] has been read back
+        for name, t in views[b].items():
+            setattr(step, name, t)
+        step.out = outs[b]
         step.run()
-        host_out.copy_(step.out, non_blocking=True)
+        ran[b].record(stream)
+        down_stream.wait_event(ran[b])
+        with torch.cuda.stream(down_stream):
+            host_outs[b].copy_(outs[b], non_blocking=True)
+        read_back[b].record(down_stream)
+
+    def drain():
+        for ev in read_back + uploaded:
+            stream.wait_event(ev)
 
     for _ in range(3):
         e2e_step()
+    drain()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    up_stream.wait_event(e0)
     for _ in range(k_e2e):
         e2e_step()
+    drain()                                       # the last read-back is inside the region
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / k_e2e
+    if pkv.device_error() != 0:
+        raise SystemExit("device error in the end-to-end steps")
+    if not torch.equal(host_outs[(n_done[0] - 1) & 1], outs[(n_done[0] - 1) & 1].cpu()):
+        raise SystemExit("end-to-end read-back differs from the device output")
+
+    # the same steps with upload, step and read-back in series on one stream
+    def serial_step():
+        dev_bufs[0].copy_(host_buf, non_blocking=True)
+        for name, t in views[0].items():
+            setattr(step, name, t)
+        step.out = outs[0]
+        step.run()
+        host_outs[0].copy_(outs[0], non_blocking=True)
+
+    for _ in range(3):
+        serial_step()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(k_e2e):
+        serial_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    serial_ms = e0.elapsed_time(e1) / k_e2e
 
     value = job_throughput(step_bytes, world, ms_per_step)
     peak, peak_kind, tc_peak, _ = peaks()
@@ -692,7 +754,12 @@ def run_gpu(args):
         "next_rows": nxt,
         "cpu_baseline": cpu,
         "e2e": {"value": step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "copies": "uploads and read-backs on two copy streams, double-buffered, "
+                          "overlapping the neighbouring steps",
+                "serial": {"value": step_bytes / (serial_ms * 1e-3) / 1e9,
+                           "ms_per_step": serial_ms,
+                           "copies": "upload, step, read-back in series on one stream"}},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
