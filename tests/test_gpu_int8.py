@@ -144,13 +144,15 @@ def test_int8_bad_slot_is_flagged(lib):
     assert int(torch.count_nonzero(ic.k_codes)) == 2 * 64           # slot 1 written, 32 skipped
 
 
-def test_int8_copy_on_write_moves_codes_and_scales(lib):
-    """Block copies through pkv_copy_blocks_int8 equal the oracle's whole-block copy."""
+@pytest.mark.parametrize("d", [128, 64])
+def test_int8_copy_on_write_moves_codes_and_scales(lib, d):
+    """Block copies through pkv_copy_blocks_int8 equal the oracle's whole-block copy
+    (tiles of 2112 and 1088 bytes: codes, then scales)."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from oracle import cache as ocache
 
-    hkv, d, nb = 4, 128, 12
+    hkv, nb = 4, 12
     rng = np.random.default_rng(9)
     x = rng.standard_normal((nb * 16, hkv, d)).astype(np.float32)
     bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
