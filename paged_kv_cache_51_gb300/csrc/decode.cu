@@ -528,14 +528,16 @@ __global__ void __launch_bounds__(SplitCfg<T, D, G>::kThreads)
 }
 
 // ---------------------------------------------------------------------------
-// Merge kernel: one warp per (sequence, KV head) group whose row has more than
-// one split; for each of the group's G query heads
+// Merge kernel: one warp per (sequence, query head) whose row has more than
+// one split:
 //   M = max_k m_k,  L = sum_k l_k 2^(m_k - M),  out = sum_k O_k 2^(m_k - M) / L
 // It is launched behind the split kernel with programmatic dependent launch,
 // so it is resident when the split kernel ends and only waits for it.  Lane k
-// holds the (m, l) of split k (32 splits per pass) for every head, and all of
-// a pass's O rows are requested before they are used, so their latencies
-// overlap.  Splits are summed in index order.
+// holds the (m, l) of split k (32 splits per pass); the O rows of eight splits
+// are requested before any is used, so their latencies overlap, and they are
+// summed in split index order.  (One warp per KV-head group, with one split's
+// G rows in flight at a time, took 49 us on 64-split rows at G = 8: the
+// longest row's serial latency chain.)
 // ---------------------------------------------------------------------------
 struct MergeParams {
     void* out;
@@ -549,15 +551,16 @@ struct MergeParams {
     int32_t max_context_len;
 };
 
-template <typename T, int D, int G>
+template <typename T, int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(MergeParams p) {
     pdl_wait_prerequisites();   // the split kernel's partials
     constexpr int DPL = D / 32;
+    constexpr int kBatch = 8;   // splits whose O rows are requested together
     const int lane = threadIdx.x & 31;
     const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
-    const int Hkv = p.num_q_heads / G;
-    if (wid >= p.num_seqs * Hkv) return;
-    const int seq = wid / Hkv, kvh = wid % Hkv;
+    const int Hq = p.num_q_heads;
+    if (wid >= p.num_seqs * Hq) return;
+    const int seq = wid / Hq, h = wid % Hq;
     int qrow = seq;
     if (p.query_start_loc) {
         qrow = p.query_start_loc[seq];
@@ -567,69 +570,57 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(MergeParams p) {
     if (ctx < 1 || ctx > p.max_context_len) return;          // flagged by the planner
     const int n = (ctx + kSplitTokens - 1) / kSplitTokens;
     if (n <= 1) return;                                     // written by the split kernel
-    // slots of head j, split k: base + j * max_splits + k
-    const size_t base = (size_t(seq) * p.num_q_heads + size_t(kvh) * G) * p.max_splits;
-    float M[G];
+    // slot of split k: base + k
+    const size_t base = (size_t(seq) * Hq + h) * p.max_splits;
+    float M = -INFINITY;
+    for (int k = lane; k < n; k += 32) M = fmaxf(M, p.part_ml[base + k].x);
 #pragma unroll
-    for (int j = 0; j < G; ++j) M[j] = -INFINITY;
-    for (int k = lane; k < n; k += 32)
+    for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+    float L = 0.f, acc[DPL];
 #pragma unroll
-        for (int j = 0; j < G; ++j) M[j] = fmaxf(M[j], p.part_ml[base + size_t(j) * p.max_splits + k].x);
-#pragma unroll
-    for (int j = 0; j < G; ++j)
-#pragma unroll
-        for (int off = 16; off; off >>= 1) M[j] = fmaxf(M[j], __shfl_xor_sync(kFull, M[j], off));
-    float L[G], acc[G][DPL];
-#pragma unroll
-    for (int j = 0; j < G; ++j) {
-        L[j] = 0.f;
-#pragma unroll
-        for (int d = 0; d < DPL; ++d) acc[j][d] = 0.f;
-    }
+    for (int d = 0; d < DPL; ++d) acc[d] = 0.f;
     for (int k0 = 0; k0 < n; k0 += 32) {
-        float w[G];
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-            w[j] = 0.f;
-            if (k0 + lane < n) {
-                const float2 ml = __ldcs(p.part_ml + base + size_t(j) * p.max_splits + k0 + lane);
-                w[j] = exp2f(ml.x - M[j]);
-                L[j] = fmaf(ml.y, w[j], L[j]);
-            }
+        float w = 0.f;
+        if (k0 + lane < n) {
+            const float2 ml = __ldcs(p.part_ml + base + k0 + lane);
+            w = exp2f(ml.x - M);
+            L = fmaf(ml.y, w, L);
         }
-        const int cnt = min(32, n - k0);
-#pragma unroll(G >= 8 ? 1 : 2)
-        for (int i = 0; i < cnt; ++i) {
-            float ov[G][DPL];
+        const int cnt = min(32, n - k0);                    // the same in every lane
+        const float* src = p.part_o + (base + k0) * D + lane * DPL;
+        for (int i = 0; i < cnt; i += kBatch) {
+            // all of the batch's rows in flight, then summed in split order
+            float ov[kBatch][DPL];
 #pragma unroll
-            for (int j = 0; j < G; ++j) {
-                // read once: let the kept lines go
-                const float* src = p.part_o + (base + size_t(j) * p.max_splits + k0 + i) * D + lane * DPL;
-                if constexpr (DPL == 4) {
-                    const float4 v = __ldcs(reinterpret_cast<const float4*>(src));
-                    ov[j][0] = v.x; ov[j][1] = v.y; ov[j][2] = v.z; ov[j][3] = v.w;
-                } else {
-                    const float2 v = __ldcs(reinterpret_cast<const float2*>(src));
-                    ov[j][0] = v.x; ov[j][1] = v.y;
+            for (int u = 0; u < kBatch; ++u) {
+                if (i + u < cnt) {
+                    // read once: let the kept lines go
+                    const float* r = src + size_t(i + u) * D;
+                    if constexpr (DPL == 4) {
+                        const float4 v = __ldcs(reinterpret_cast<const float4*>(r));
+                        ov[u][0] = v.x; ov[u][1] = v.y; ov[u][2] = v.z; ov[u][3] = v.w;
+                    } else {
+                        const float2 v = __ldcs(reinterpret_cast<const float2*>(r));
+                        ov[u][0] = v.x; ov[u][1] = v.y;
+                    }
                 }
             }
 #pragma unroll
-            for (int j = 0; j < G; ++j) {
-                const float wi = __shfl_sync(kFull, w[j], i);
+            for (int u = 0; u < kBatch; ++u) {
+                if (i + u < cnt) {
+                    const float wi = __shfl_sync(kFull, w, i + u);
 #pragma unroll
-                for (int d = 0; d < DPL; ++d) acc[j][d] = fmaf(wi, ov[j][d], acc[j][d]);
+                    for (int d = 0; d < DPL; ++d) acc[d] = fmaf(wi, ov[u][d], acc[d]);
+                }
             }
         }
     }
 #pragma unroll
-    for (int j = 0; j < G; ++j) {
+    for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
+    const float inv = 1.f / L;
+    T* o = static_cast<T*>(p.out) + (size_t(qrow) * Hq + h) * D + lane * DPL;
 #pragma unroll
-        for (int off = 16; off; off >>= 1) L[j] += __shfl_xor_sync(kFull, L[j], off);
-        const float inv = 1.f / L[j];
-        T* o = static_cast<T*>(p.out) + (size_t(qrow) * p.num_q_heads + kvh * G + j) * D + lane * DPL;
-#pragma unroll
-        for (int d = 0; d < DPL; ++d) o[d] = Elem<T>::store_val(acc[j][d] * inv);
-    }
+    for (int d = 0; d < DPL; ++d) o[d] = Elem<T>::store_val(acc[d] * inv);
 }
 
 // ---------------------------------------------------------------------------
@@ -703,8 +694,8 @@ int launch_split_d(const AttnArgs& a, int g) {
     }
 }
 
-template <typename T, int D, int G>
-int launch_merge_t(const AttnArgs& a) {
+template <typename T, int D>
+int launch_merge_d(const AttnArgs& a) {
     MergeParams p;
     p.out = a.out;
     p.context_lens = a.context_lens;
@@ -715,7 +706,7 @@ int launch_merge_t(const AttnArgs& a) {
     p.num_q_heads = a.desc->num_q_heads;
     p.max_splits = a.ws.max_splits;
     p.max_context_len = a.max_context_len;
-    const int64_t warps = int64_t(a.num_seqs) * a.desc->num_kv_heads;
+    const int64_t warps = int64_t(a.num_seqs) * a.desc->num_q_heads;   // one per (seq, head)
     const int64_t blocks = (warps + 3) / 4;
     if (blocks < 1) return PKV_OK;
     cudaLaunchConfig_t cfg = {};
@@ -727,18 +718,7 @@ int launch_merge_t(const AttnArgs& a) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cuda_status(cudaLaunchKernelEx(&cfg, decode_merge_kernel<T, D, G>, p));
-}
-
-template <typename T, int D>
-int launch_merge_d(const AttnArgs& a) {
-    switch (a.desc->num_q_heads / a.desc->num_kv_heads) {
-        case 1: return launch_merge_t<T, D, 1>(a);
-        case 2: return launch_merge_t<T, D, 2>(a);
-        case 4: return launch_merge_t<T, D, 4>(a);
-        case 8: return launch_merge_t<T, D, 8>(a);
-        default: return PKV_ERR_UNSUPPORTED;
-    }
+    return cuda_status(cudaLaunchKernelEx(&cfg, decode_merge_kernel<T, D>, p));
 }
 
 }  // namespace
