@@ -221,3 +221,26 @@ def test_int8_entry_points_validate_on_the_host(lib):
     assert L.pkv_copy_blocks_int8(None, 2, fake, fake, ref(i8), None) == \
         lib.PKV_ERR_INVALID
     assert L.pkv_copy_blocks_int8(None, 0, None, None, ref(i8), None) == 0
+
+
+def test_int8_cache_views_follow_the_tile_layout(lib):
+    """The binding's code and scale views alias the fused pools as the header
+    lays a tile out: 16 rows of codes, then the 16 rows' fp32 scales."""
+    import numpy as np
+    import torch
+
+    for d in (128, 64):
+        c = lib.Int8Cache(3, 2, 16, d, 4, device="cpu")
+        tile = lib.int8_tile_bytes(d)
+        assert tuple(c.k_pool.shape) == (3, 2, tile) and c.k_pool.dtype == torch.uint8
+        assert tuple(c.k_codes.shape) == (3, 2, 16, d) and c.k_codes.dtype == torch.int8
+        assert tuple(c.v_scales.shape) == (3, 2, 16) and c.v_scales.dtype == torch.float32
+        c.k_codes[2, 1, 5, 7] = -3
+        c.v_scales[1, 0, 9] = 0.25
+        kb = c.k_pool.numpy()
+        vb = c.v_pool.numpy()
+        assert kb[2, 1, 5 * d + 7].view(np.int8) == -3
+        assert vb[1, 0, 16 * d + 4 * 9:16 * d + 4 * 10].view(np.float32)[0] == 0.25
+        assert np.count_nonzero(kb) == 1 and np.count_nonzero(vb) == 2   # 0.25 = 0x3e800000
+        kp, vp = c.tensors()
+        assert kp is c.k_pool and vp is c.v_pool
