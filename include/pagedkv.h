@@ -389,7 +389,8 @@ PKV_API int paged_kv_append_int8(const void* k, const void* v, const int64_t* sl
  * block src (every kv head: codes and scales) are copied to block dst, as
  * pkv_copy_blocks does for the other caches.  block_pairs: device int32
  * [num_pairs][2]; an id outside [0, num_blocks) sets PKV_DEV_BAD_COPY_PAIR and
- * that pair is skipped. */
+ * that pair is skipped.  desc->block_size must be 16 (the tile has 16 rows;
+ * PKV_ERR_UNSUPPORTED otherwise). */
 PKV_API int pkv_copy_blocks_int8(const int32_t* block_pairs, int32_t num_pairs, void* k_pool,
                                  void* v_pool, const pkv_cache_desc* desc, void* stream);
 
