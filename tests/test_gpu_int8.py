@@ -178,13 +178,14 @@ def test_int8_copy_on_write_moves_codes_and_scales(lib, d):
     assert np.array_equal(ic.v_scales.cpu().numpy(), vs)
 
 
-@pytest.mark.parametrize("cfg", [2, 3])
+@pytest.mark.parametrize("cfg", [2, 3, 5])
 def test_int8_full_size_sampled(lib, cfg):
-    """The benchmark's full batches (Llama-2-7B decode, Llama-3-8B GQA decode):
-    every slot of the step's bf16 pools quantised on the device, then the int8
-    decode call as timed; six sequences checked against the oracle, which
-    quantises those sequences' blocks itself (codes and scales bit-exact,
-    attention within the bf16 tolerance)."""
+    """The benchmark's full batches (Llama-2-7B decode, Llama-3-8B GQA decode,
+    g = 8 prefix sharing with 32k-token rows): every slot of the step's bf16
+    pools quantised on the device, then the int8 decode call as timed; six
+    sequences and the longest one checked against the oracle, which quantises
+    those sequences' blocks itself (codes and scales bit-exact, attention within
+    the bf16 tolerance)."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from paged_kv_cache_51_gb300 import runner
@@ -212,7 +213,9 @@ def test_int8_full_size_sampled(lib, cfg):
     q_bits = step.q.cpu().view(torch.int16).numpy().view(np.uint16)
     got = out_f64(out)
     rng = np.random.default_rng(cfg)
-    for s in rng.choice(len(ctx), size=6, replace=False):
+    picks = set(int(i) for i in rng.choice(len(ctx), size=6, replace=False))
+    picks.add(int(np.argmax(ctx)))
+    for s in sorted(picks):
         n = -(-int(ctx[s]) // bs)
         blocks = bt[s, :n]
         kq, ks = quant.quantize_rows(ost.k_cache[blocks], "bf16")
