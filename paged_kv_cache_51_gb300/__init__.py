@@ -133,6 +133,21 @@ def status_string(status):
         return "status"
 
 
+_I32_MIN, _I32_MAX = -(1 << 31), (1 << 31) - 1
+
+
+def _host_int32(values, name):
+    """A contiguous host int32 copy of `values` (a sequence of ints or an integer
+    array); a value outside int32 raises ValueError instead of wrapping."""
+    a = values if isinstance(values, np.ndarray) else np.fromiter(values, dtype=np.int64,
+                                                                   count=len(values))
+    if a.dtype.kind not in "iu":
+        raise TypeError(f"{name}: integers expected, got {a.dtype}")
+    if a.size and (int(a.min()) < _I32_MIN or int(a.max()) > _I32_MAX):
+        raise ValueError(f"{name}: a value is outside int32")
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
 def _check(status, what):
     if status != PKV_OK:
         raise PagedKVError(status, what)
@@ -147,11 +162,14 @@ class BlockPool:
     def __init__(self, num_blocks, block_size, watermark_blocks=0, free_order=None,
                  prefix_caching=False, sliding_window=0):
         self._h = ctypes.c_void_p()
-        arr = None
+        order = None
         if free_order is not None:
-            arr = (ctypes.c_int32 * num_blocks)(*[int(b) for b in free_order])
+            order = _host_int32(free_order, "free_order")
+            if order.shape != (num_blocks,):
+                raise ValueError(f"free_order: {order.shape[0]} entries, expected {num_blocks}")
         flags = PKV_POOL_PREFIX_CACHING if prefix_caching else 0
-        _check(lib().pkv_pool_create_ex(num_blocks, block_size, watermark_blocks, arr, flags,
+        _check(lib().pkv_pool_create_ex(num_blocks, block_size, watermark_blocks,
+                                        None if order is None else order.ctypes.data, flags,
                                         sliding_window, ctypes.byref(self._h)),
                "pkv_pool_create_ex")
         self.num_blocks = num_blocks
@@ -192,7 +210,7 @@ class BlockPool:
 
     def add_tokens(self, seq_id, token_ids):
         """Returns (status, slots or None, num_cached_tokens)."""
-        toks = np.ascontiguousarray(np.asarray(token_ids, dtype=np.int64).astype(np.int32))
+        toks = _host_int32(token_ids, "token_ids")
         n = int(toks.shape[0])
         if n == 0:
             toks = np.zeros(1, dtype=np.int32)
@@ -269,13 +287,16 @@ def pkv_splitfuse_compose(token_budget, num_decode, prompt_remaining):
 
     Returns (decode_admitted, chunks, tokens_used): the first decode_admitted
     decode sequences take one token each, prompt i takes chunks[i] tokens."""
-    n = len(prompt_remaining)
-    rem = (ctypes.c_int32 * max(n, 1))(*[int(r) for r in prompt_remaining])
-    out = (ctypes.c_int32 * max(n, 1))()
+    rem = _host_int32(prompt_remaining, "prompt_remaining")
+    n = int(rem.shape[0])
+    if n == 0:
+        rem = np.zeros(1, dtype=np.int32)
+    out = np.zeros(max(n, 1), dtype=np.int32)
     dec, used = ctypes.c_int32(), ctypes.c_int32()
-    _check(lib().pkv_splitfuse_compose(token_budget, num_decode, n, rem, out, ctypes.byref(dec),
-                                       ctypes.byref(used)), "pkv_splitfuse_compose")
-    return dec.value, list(out)[:n], used.value
+    _check(lib().pkv_splitfuse_compose(token_budget, num_decode, n, rem.ctypes.data,
+                                       out.ctypes.data, ctypes.byref(dec), ctypes.byref(used)),
+           "pkv_splitfuse_compose")
+    return dec.value, out[:n].tolist(), used.value
 
 
 # ----------------------------------------------------------------------------

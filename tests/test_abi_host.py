@@ -244,3 +244,22 @@ def test_int8_cache_views_follow_the_tile_layout(lib):
         assert np.count_nonzero(kb) == 1 and np.count_nonzero(vb) == 2   # 0.25 = 0x3e800000
         kp, vp = c.tensors()
         assert kp is c.k_pool and vp is c.v_pool
+
+
+def test_binding_refuses_values_outside_int32(lib):
+    """Token ids, prompt lengths and the free order cross the ABI as int32; the
+    binding raises on a value outside int32 instead of letting it wrap, and on a
+    free order of the wrong length instead of letting the pool read past it."""
+    pool = lib.BlockPool(64, 16, 0, prefix_caching=True)
+    with pytest.raises(ValueError):
+        pool.add_tokens(1, [5, 1 << 31])
+    with pytest.raises(ValueError):
+        pool.add_tokens(1, [-(1 << 31) - 1])
+    st, slots, cached = pool.add_tokens(1, [5, (1 << 31) - 1, -(1 << 31)])
+    assert st == lib.PKV_OK and len(slots) == 3 and cached == 0
+    with pytest.raises(ValueError):
+        lib.pkv_splitfuse_compose(16, 0, [3, 1 << 32])
+    with pytest.raises(ValueError):
+        lib.BlockPool(4, 16, 0, [0, 1, 2])
+    with pytest.raises(TypeError):
+        lib.pkv_splitfuse_compose(16, 0, np.array([1.5, 2.0]))
