@@ -235,9 +235,10 @@ PKV_API int pkv_splitfuse_compose(int32_t token_budget, int32_t num_decode, int3
  * Device entry points.
  * ======================================================================== */
 
-/* Copy-on-write block copies [Deploy §2.1 append_slots "copy the tokens";
- * Infra 二 copy-on-write]: for each pair i, K and V block pairs[2i+1] become
- * byte-for-byte copies of block pairs[2i] (all heads, all rows).
+/* Copy-on-write block copies [Deploy §2.1 append_slots (the new block gets the
+ * shared block's tokens); Infra 二 copy-on-write]: for each pair i, K and V
+ * block pairs[2i+1] become byte-for-byte copies of block pairs[2i] (all heads,
+ * all rows).
  * block_pairs: device int32 [num_pairs][2] (src, dst).  Destinations must be
  * distinct and no destination may also be a source (pairs run in parallel).
  * num_pairs == 0 is a no-op. */
@@ -317,7 +318,11 @@ PKV_API int paged_attention_decode(void* out, const void* q, const void* k_cache
  *   - PKV_ERR_WORKSPACE (nothing enqueued) when the batch's split partials
  *     (pkv_decode_workspace_bytes) exceed PKV_NOALLOC_SCRATCH_BYTES.
  *   - The first call on a device looks up the array's device address with that
- *     device current; make that first call before any stream capture.
+ *     device current; make that first call before any stream capture.  The
+ *     address is kept for the life of the device's primary context: after a
+ *     cudaDeviceReset (or any reset of that context) the library's device
+ *     state is gone, and no entry point may be called on that device again in
+ *     this process.
  *   - All calls share the one array, which keeps the last call's contents
  *     (nothing in it needs to start at zero).  Calls that overlap on the GPU
  *     (other streams, other threads) race on it and corrupt each other's
@@ -408,7 +413,9 @@ PKV_API int paged_attention_decode_int8(void* out, const void* q, const void* k_
 
 /* Read the current device's error word into *code_out (PKV_DEV_* code of the
  * first fault recorded since the last clear) and, if `clear` is non-zero,
- * reset it.  Synchronizes the device. */
+ * reset it.  Synchronizes the device.  The word's device address is looked up
+ * once per device and kept for the life of its primary context (see
+ * paged_attention_decode_noalloc on device resets). */
 PKV_API int pkv_device_error(int32_t* code_out, int32_t clear);
 
 /* Static description of a status code (never NULL). */

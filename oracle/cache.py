@@ -6,8 +6,8 @@
   the block manager only plans, the cache engine writes)].  A negative slot
   means "no write" (padding), a reading the pages leave open.
 * ``copy_blocks``: copy-on-write copies a whole physical block (every row, K
-  and V, all KV heads) from ``src`` to ``dst`` [Deploy §2.1 append_slots
-  "Copy on Write: Allocate a new block and copy the tokens"; Infra 二、2
+  and V, all KV heads) from ``src`` to ``dst``: a shared last block gets a
+  private copy before the write [Deploy §2.1 append_slots; Infra 二、2
   copy-on-write].
 
 The cache dtype is the input dtype (float32 or bf16 bit patterns); an append is

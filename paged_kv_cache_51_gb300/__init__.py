@@ -139,8 +139,16 @@ _I32_MIN, _I32_MAX = -(1 << 31), (1 << 31) - 1
 def _host_int32(values, name):
     """A contiguous host int32 copy of `values` (a sequence of ints or an integer
     array); a value outside int32 raises ValueError instead of wrapping."""
-    a = values if isinstance(values, np.ndarray) else np.fromiter(values, dtype=np.int64,
-                                                                   count=len(values))
+    if isinstance(values, np.ndarray):
+        a = values
+    else:
+        vals = list(values)
+        if any(isinstance(x, (bool, np.bool_)) or not isinstance(x, (int, np.integer))
+               for x in vals):
+            raise TypeError(f"{name}: integers expected")
+        if any(not _I32_MIN <= int(x) <= _I32_MAX for x in vals):
+            raise ValueError(f"{name}: a value is outside int32")
+        a = np.asarray(vals, dtype=np.int64).reshape(len(vals))
     if a.dtype.kind not in "iu":
         raise TypeError(f"{name}: integers expected, got {a.dtype}")
     if a.size and (int(a.min()) < _I32_MIN or int(a.max()) > _I32_MAX):
@@ -314,9 +322,27 @@ def cache_desc(k_cache, num_q_heads):
     return CacheDesc(dt, nb, bs, hkv, num_q_heads, d)
 
 
-def _stream(stream):
+def _devices_agree(named_devices, current, stream_device):
+    """Raise ValueError unless every (name, torch.device) pair and the stream's
+    device are the current CUDA device: the library's kernels run on the
+    current device and its device-side state (error word, scratch array) is
+    looked up there, so a pointer into another GPU's memory would fault or be
+    read over the peer link."""
+    if stream_device.type != "cuda" or stream_device.index != current:
+        raise ValueError(f"stream is on {stream_device}, but the current device is cuda:{current}")
+    for name, dev in named_devices:
+        if dev.type != "cuda" or dev.index != current:
+            raise ValueError(f"{name} is on {dev}, but the current device is cuda:{current}; "
+                             f"call under torch.cuda.device({dev})")
+
+
+def _stream_on_device(stream, *named):
+    """The stream handle for a launch, after checking that the stream and every
+    named tensor (name, tensor or None) are on the current CUDA device."""
     if stream is None:
         stream = torch.cuda.current_stream()
+    _devices_agree([(n, t.device) for n, t in named if t is not None],
+                   torch.cuda.current_device(), stream.device)
     return ctypes.c_void_p(stream.cuda_stream)
 
 
@@ -335,8 +361,10 @@ def pkv_copy_blocks(block_pairs, k_cache, v_cache, desc, stream=None):
     if n == 0:
         return
     _need(block_pairs, torch.int32, "block_pairs")
+    st = _stream_on_device(stream, ("block_pairs", block_pairs), ("k_cache", k_cache),
+                           ("v_cache", v_cache))
     _check(lib().pkv_copy_blocks(_ptr(block_pairs), n, _ptr(k_cache), _ptr(v_cache),
-                                 ctypes.byref(desc), _stream(stream)), "pkv_copy_blocks")
+                                 ctypes.byref(desc), st), "pkv_copy_blocks")
 
 
 def paged_kv_append(k, v, slot_mapping, k_cache, v_cache, desc, stream=None):
@@ -346,8 +374,10 @@ def paged_kv_append(k, v, slot_mapping, k_cache, v_cache, desc, stream=None):
     for t, nm in ((k, "k"), (v, "v"), (k_cache, "k_cache"), (v_cache, "v_cache")):
         _need(t, dt, nm)
     _need(slot_mapping, torch.int64, "slot_mapping")
+    st = _stream_on_device(stream, ("k", k), ("v", v), ("slot_mapping", slot_mapping),
+                           ("k_cache", k_cache), ("v_cache", v_cache))
     _check(lib().paged_kv_append(_ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache),
-                                 _ptr(v_cache), ctypes.byref(desc), _stream(stream)),
+                                 _ptr(v_cache), ctypes.byref(desc), st),
            "paged_kv_append")
 
 
@@ -367,10 +397,13 @@ def paged_kv_append_rope(k, v, slot_mapping, positions, cos_sin, k_cache, v_cach
         _need(q, dt, "q")
         q_out = q if q_out is None else q_out
         _need(q_out, dt, "q_out")
+    st = _stream_on_device(stream, ("q", q), ("q_out", q_out), ("k", k), ("v", v),
+                           ("slot_mapping", slot_mapping), ("positions", positions),
+                           ("cos_sin", cos_sin), ("k_cache", k_cache), ("v_cache", v_cache))
     _check(lib().paged_kv_append_rope(_ptr(q), _ptr(q_out), _ptr(k), _ptr(v), _ptr(slot_mapping),
                                       _ptr(positions), _ptr(cos_sin), cos_sin.shape[0], T,
                                       _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc),
-                                      _stream(stream)), "paged_kv_append_rope")
+                                      st), "paged_kv_append_rope")
     return q_out
 
 
@@ -399,13 +432,16 @@ def paged_attention_decode(out, q, k_cache, v_cache, desc, block_tables, context
     _need(context_lens, torch.int32, "context_lens")
     if scale is None:
         scale = 1.0 / math.sqrt(desc.head_dim)
+    st = _stream_on_device(stream, ("out", out), ("q", q), ("k_cache", k_cache),
+                           ("v_cache", v_cache), ("block_tables", block_tables),
+                           ("context_lens", context_lens), ("ws", ws))
     if ws is None:
         ws = workspace(decode_workspace_bytes(desc, S, max_context_len), q.device)
     _check(lib().paged_attention_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                         ctypes.byref(desc), _ptr(block_tables),
                                         block_tables.shape[1], _ptr(context_lens), S,
                                         max_context_len, scale, _ptr(ws), ws.numel(),
-                                        _stream(stream)), "paged_attention_decode")
+                                        st), "paged_attention_decode")
     return out
 
 
@@ -427,10 +463,13 @@ def paged_attention_decode_noalloc(out, q, k_cache, v_cache, desc, block_tables,
     _need(context_lens, torch.int32, "context_lens")
     if scale is None:
         scale = 1.0 / math.sqrt(desc.head_dim)
+    st = _stream_on_device(stream, ("out", out), ("q", q), ("k_cache", k_cache),
+                           ("v_cache", v_cache), ("block_tables", block_tables),
+                           ("context_lens", context_lens))
     _check(lib().paged_attention_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                                 ctypes.byref(desc), _ptr(block_tables),
                                                 block_tables.shape[1], _ptr(context_lens), S,
-                                                max_context_len, scale, _stream(stream)),
+                                                max_context_len, scale, st),
            "paged_attention_decode_noalloc")
     return out
 
@@ -449,6 +488,10 @@ def paged_attention_varlen(out, q, k_cache, v_cache, desc, block_tables, query_s
         _need(t, torch.int32, nm)
     if scale is None:
         scale = 1.0 / math.sqrt(desc.head_dim)
+    st = _stream_on_device(stream, ("out", out), ("q", q), ("k_cache", k_cache),
+                           ("v_cache", v_cache), ("block_tables", block_tables),
+                           ("query_start_loc", query_start_loc), ("context_lens", context_lens),
+                           ("ws", ws))
     if ws is None:
         ws = workspace(varlen_workspace_bytes(desc, S, Tq, max_query_len, max_context_len),
                        q.device)
@@ -456,7 +499,7 @@ def paged_attention_varlen(out, q, k_cache, v_cache, desc, block_tables, query_s
                                         ctypes.byref(desc), _ptr(block_tables),
                                         block_tables.shape[1], _ptr(query_start_loc),
                                         _ptr(context_lens), S, Tq, max_query_len, max_context_len,
-                                        scale, _ptr(ws), ws.numel(), _stream(stream)),
+                                        scale, _ptr(ws), ws.numel(), st),
            "paged_attention_varlen")
     return out
 
@@ -511,9 +554,11 @@ def paged_kv_append_int8(k, v, slot_mapping, cache, stream=None):
     _need(v, torch.bfloat16, "v")
     _need(slot_mapping, torch.int64, "slot_mapping")
     _need_int8_cache(cache)
+    st = _stream_on_device(stream, ("k", k), ("v", v), ("slot_mapping", slot_mapping),
+                           ("k_pool", cache.k_pool), ("v_pool", cache.v_pool))
     _check(lib().paged_kv_append_int8(_ptr(k), _ptr(v), _ptr(slot_mapping), k.shape[0],
                                       _ptr(cache.k_pool), _ptr(cache.v_pool),
-                                      ctypes.byref(cache.desc), _stream(stream)),
+                                      ctypes.byref(cache.desc), st),
            "paged_kv_append_int8")
 
 
@@ -524,9 +569,11 @@ def pkv_copy_blocks_int8(block_pairs, cache, stream=None):
         return
     _need(block_pairs, torch.int32, "block_pairs")
     _need_int8_cache(cache)
+    st = _stream_on_device(stream, ("block_pairs", block_pairs), ("k_pool", cache.k_pool),
+                           ("v_pool", cache.v_pool))
     _check(lib().pkv_copy_blocks_int8(_ptr(block_pairs), n, _ptr(cache.k_pool),
                                       _ptr(cache.v_pool), ctypes.byref(cache.desc),
-                                      _stream(stream)), "pkv_copy_blocks_int8")
+                                      st), "pkv_copy_blocks_int8")
 
 
 def paged_attention_decode_int8(out, q, cache, block_tables, context_lens, max_context_len,
@@ -541,13 +588,16 @@ def paged_attention_decode_int8(out, q, cache, block_tables, context_lens, max_c
     desc = cache.desc
     if scale is None:
         scale = 1.0 / math.sqrt(desc.head_dim)
+    st = _stream_on_device(stream, ("out", out), ("q", q), ("k_pool", cache.k_pool),
+                           ("v_pool", cache.v_pool), ("block_tables", block_tables),
+                           ("context_lens", context_lens), ("ws", ws))
     if ws is None:
         ws = workspace(decode_workspace_bytes(desc, S, max_context_len), q.device)
     _check(lib().paged_attention_decode_int8(_ptr(out), _ptr(q), _ptr(cache.k_pool),
                                              _ptr(cache.v_pool), ctypes.byref(desc),
                                              _ptr(block_tables), block_tables.shape[1],
                                              _ptr(context_lens), S, max_context_len, scale,
-                                             _ptr(ws), ws.numel(), _stream(stream)),
+                                             _ptr(ws), ws.numel(), st),
            "paged_attention_decode_int8")
     return out
 

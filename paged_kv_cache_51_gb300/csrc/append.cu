@@ -4,8 +4,8 @@
 // written into the cache; "大模型部署.md" §2.1: the block manager plans the
 // physical slot, the cache engine writes it):
 //     cache[slot / bs][h][slot % bs][:] = x[t][h][:]      for K and V.
-// Copy-on-write ("大模型部署.md" §2.1 append_slots, "Allocate a new block and
-// copy the tokens"): a whole block (all heads, all rows) of K and V.
+// Copy-on-write ("大模型部署.md" §2.1 append_slots: a shared last block gets a
+// private copy before the write): a whole block (all heads, all rows) of K and V.
 //
 // Both are pure byte movement, bound by HBM bandwidth: every thread moves one
 // 16-byte vector with a coalesced load and store; source rows are read once,

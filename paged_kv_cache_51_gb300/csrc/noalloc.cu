@@ -23,7 +23,10 @@ namespace {
 
 // Device address of g_noalloc_scratch, looked up once per device with that
 // device current.  In host code the array's name is only a host-side stand-in,
-// never a device address, so it is never passed to a kernel directly.
+// never a device address, so it is never passed to a kernel directly.  The
+// address stays valid while the device's primary context lives; a
+// cudaDeviceReset would unload the module, and the header rules out calls on
+// that device afterwards.
 int scratch_address(void** out) {
     static std::mutex mu;
     static void* addr[128] = {};

@@ -11,6 +11,7 @@ import re
 
 import numpy as np
 import pytest
+import torch
 
 from oracle.block_pool import LATER, NEVER, OK, BlockPoolModel
 from tests.conftest import ROOT, read_kv, read_rows
@@ -263,3 +264,79 @@ def test_binding_refuses_values_outside_int32(lib):
         lib.BlockPool(4, 16, 0, [0, 1, 2])
     with pytest.raises(TypeError):
         lib.pkv_splitfuse_compose(16, 0, np.array([1.5, 2.0]))
+    # integers beyond int64 and inputs without len() (generators) are handled too
+    with pytest.raises(ValueError):
+        pool.add_tokens(1, [7, 1 << 63])
+    with pytest.raises(ValueError):
+        lib.pkv_splitfuse_compose(16, 0, (x for x in [3, 1 << 40]))
+    st, slots, cached = pool.add_tokens(2, (t for t in [9, 8, 7]))
+    assert st == lib.PKV_OK and len(slots) == 3
+    assert lib.pkv_splitfuse_compose(16, 0, (x for x in [3, 4]))[1] == [3, 4]
+
+
+class _FakeStream:
+    def __init__(self, index):
+        self.device = torch.device("cuda", index)
+        self.cuda_stream = 0
+
+
+class _FakeTensor:
+    """Stands in for a CUDA tensor on device `index` (no memory, no kernel)."""
+
+    def __init__(self, index, dtype, shape):
+        self.device = torch.device("cuda", index)
+        self.dtype = dtype
+        self.shape = shape
+        self.is_cuda = True
+
+    def is_contiguous(self):
+        return True
+
+    def data_ptr(self):
+        return 0
+
+    def numel(self):
+        return 1 << 20
+
+
+def test_binding_refuses_tensors_off_the_current_device(lib, monkeypatch):
+    """The kernels run on the current device (its stream, its error word, its
+    scratch array), so a tensor or stream of another GPU is refused on the host
+    before the C call, and nothing is launched."""
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    monkeypatch.setattr(torch.cuda, "current_stream", lambda device=None: _FakeStream(0))
+    called = []
+    monkeypatch.setattr(lib, "lib", lambda: called.append(1) or (_ for _ in ()).throw(
+        AssertionError("the C library was called")))
+    bf = torch.bfloat16
+    desc = lib.CacheDesc(lib.PKV_BF16, 64, 16, 8, 32, 128)
+
+    def args(dev_of_q, dev_of_tables=0):
+        return dict(out=_FakeTensor(0, bf, (4, 32, 128)), q=_FakeTensor(dev_of_q, bf, (4, 32, 128)),
+                    k_cache=_FakeTensor(0, bf, (64, 8, 16, 128)),
+                    v_cache=_FakeTensor(0, bf, (64, 8, 16, 128)), desc=desc,
+                    block_tables=_FakeTensor(dev_of_tables, torch.int32, (4, 8)),
+                    context_lens=_FakeTensor(0, torch.int32, (4,)), max_context_len=100,
+                    ws=_FakeTensor(0, torch.uint8, (1 << 20,)))
+
+    with pytest.raises(ValueError, match="q is on cuda:1"):
+        lib.paged_attention_decode(**args(1))
+    with pytest.raises(ValueError, match="block_tables is on cuda:3"):
+        lib.paged_attention_decode(**args(0, 3))
+    a = args(0)
+    a.pop("ws")
+    a["q"] = _FakeTensor(2, bf, (4, 32, 128))
+    with pytest.raises(ValueError, match="q is on cuda:2"):
+        lib.paged_attention_decode_noalloc(**a)
+    with pytest.raises(ValueError, match="stream is on cuda:1"):
+        lib.paged_attention_decode(**args(0), stream=_FakeStream(1))
+    k = _FakeTensor(0, bf, (4, 8, 128))
+    with pytest.raises(ValueError, match="slot_mapping is on cuda:1"):
+        lib.paged_kv_append(k, k, _FakeTensor(1, torch.int64, (4,)),
+                            _FakeTensor(0, bf, (64, 8, 16, 128)),
+                            _FakeTensor(0, bf, (64, 8, 16, 128)), desc)
+    assert not called
+    # the pure check itself
+    lib._devices_agree([("a", torch.device("cuda", 0))], 0, torch.device("cuda", 0))
+    with pytest.raises(ValueError):
+        lib._devices_agree([("a", torch.device("cpu"))], 0, torch.device("cuda", 0))

@@ -12,7 +12,8 @@ import pytest
 torch = pytest.importorskip("torch")
 
 import workloads  # noqa: E402
-from tests.gpu_parity import TOL, cache_bytes_equal, errors, out_f64, run_both  # noqa: E402
+from tests.gpu_parity import (TOL, assert_within_derived_bound, cache_bytes_equal,  # noqa: E402
+                              errors, out_f64, run_both)
 
 pytestmark = pytest.mark.gpu
 
@@ -77,12 +78,16 @@ def test_head_shapes(rt, lib, dtype, hq, hkv, d):
 
 
 def test_large_scores_stay_finite(rt, lib):
-    # values of scale 8 give scores in the hundreds: exercises max subtraction
-    w = workloads.random_decode(4, "f32", 8, 8, 64, 16, [300, 1200], scale=8.0)
+    # queries of scale 64 over N(0,1) keys give scores of standard deviation 64,
+    # a few hundred at the maximum: exp without the max subtraction would
+    # overflow fp32.  Keys and values keep config 1's magnitudes, so only the
+    # score-rounding term of the derived bound grows.
+    w = workloads.random_decode(4, "f32", 8, 8, 64, 16, [300, 1200], scale=1.0, q_scale=64.0)
     ost, oout, dc, step, out = run_both(w, rt)
-    assert np.isfinite(out_f64(out)).all()
-    mx, _ = errors(out, oout)
-    assert mx <= 1e-4
+    assert lib.device_error() == 0
+    got = out_f64(out)
+    assert np.isfinite(got).all()
+    assert_within_derived_bound(w, ost, oout, got)
 
 
 def test_batch_invariance_bitwise(rt, lib):

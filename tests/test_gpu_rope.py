@@ -9,7 +9,8 @@ torch = pytest.importorskip("torch")
 import workloads  # noqa: E402
 from oracle import attention, cache, rope  # noqa: E402
 from oracle.run import OracleState  # noqa: E402
-from tests.gpu_parity import TOL, cache_bytes_equal, out_f64  # noqa: E402
+from tests.gpu_parity import (TOL, assert_within_derived_bound, cache_bytes_equal,  # noqa: E402
+                              out_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -28,8 +29,7 @@ def test_append_rope_bit_exact_then_decode(lib, dtype, hq, hkv, d):
     from paged_kv_cache_51_gb300 import paged_attention_decode, paged_kv_append_rope, runner
 
     lib.device_error(clear=True)
-    scale = 2.0 if dtype == "f32" else 1.0
-    w = workloads.random_decode(31, dtype, hq, hkv, d, 16, [5, 200, 1031, 2999], scale=scale)
+    w = workloads.random_decode(31, dtype, hq, hkv, d, 16, [5, 200, 1031, 2999], scale=1.0)
     max_pos = 4096
     tab = rope.rope_table(max_pos, d)
     # history on both sides (plain appends), then the step's tokens through the rotary append
@@ -84,9 +84,14 @@ def test_append_rope_bit_exact_then_decode(lib, dtype, hq, hkv, d):
     torch.cuda.synchronize()
     bt, octx, _ = ost.batch_metadata()
     ref = attention.decode(q_ref, ost.k_cache, ost.v_cache, bt, octx, w.block_size, w.dtype)
-    d_ = np.abs(out_f64(out) - ref)
-    tmax, tmean = TOL[dtype]
-    assert float(d_.max()) <= tmax * (4 if dtype == "f32" else 1) and float(d_.mean()) <= tmean
+    if dtype == "f32":
+        # values N(0,1) as config 1, but 128 dimensions and up to 3000 keys:
+        # the derived bound (stated tolerance + first-order score rounding)
+        assert_within_derived_bound(w, ost, ref, out_f64(out), q=q_ref)
+    else:
+        d_ = np.abs(out_f64(out) - ref)
+        tmax, tmean = TOL[dtype]
+        assert float(d_.max()) <= tmax and float(d_.mean()) <= tmean
 
 
 def test_bad_rotary_position_is_flagged(lib):

@@ -7,7 +7,8 @@ torch = pytest.importorskip("torch")
 
 import workloads  # noqa: E402
 from oracle.run import execute  # noqa: E402
-from tests.gpu_parity import TOL, cache_bytes_equal, errors, out_f64, run_both  # noqa: E402
+from tests.gpu_parity import (TOL, assert_within_derived_bound, cache_bytes_equal,  # noqa: E402
+                              errors, out_f64, run_both)
 
 pytestmark = pytest.mark.gpu
 
@@ -81,16 +82,18 @@ def test_never_written_rows_may_hold_nan(rt, lib):
 
 
 def test_large_scores_use_lazy_rescale_correctly(rt, lib):
-    # scale 6: scores of a few hundred; the running max keeps growing across tiles
+    # queries of scale 64 over the configurations' keys (N(0,1) * 0.5): scores
+    # of standard deviation 32, about a hundred at the maximum, so a row's
+    # running max keeps growing by more than the lazy-rescale threshold across
+    # key tiles.  Values keep the configurations' magnitudes, so only the
+    # score-rounding term of the derived bound grows.
     spans = [(600, 200), (0, 256)]
-    w = workloads.random_varlen(15, "bf16", 32, 8, 128, 16, spans, scale=3.0)
+    w = workloads.random_varlen(15, "bf16", 32, 8, 128, 16, spans, scale=0.5, q_scale=64.0)
     ost, oout, dc, step, out = run_both(w, rt)
     assert lib.device_error() == 0
     got = out_f64(out)
     assert np.isfinite(got).all()
-    # values up to ~10 in magnitude: compare relative to the output scale
-    d = np.abs(got - oout)
-    assert float(d.max()) <= 2e-2 * max(1.0, float(np.abs(oout).max()))
+    assert_within_derived_bound(w, ost, oout, got)
 
 
 def test_unsupported_prefill_shapes_are_refused(rt, lib):

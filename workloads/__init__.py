@@ -91,8 +91,10 @@ def _blocks(n, bs):
     return -(-n // bs)
 
 
-def _decode_workload(name, rng, dtype, hq, hkv, d, bs, ctx, scale, pool=None, slack=0.1):
-    """One query token per sequence; sequence s holds ctx[s]-1 cached tokens before the step."""
+def _decode_workload(name, rng, dtype, hq, hkv, d, bs, ctx, scale, pool=None, slack=0.1,
+                     q_scale=None):
+    """One query token per sequence; sequence s holds ctx[s]-1 cached tokens before the step.
+    Queries are drawn at ``q_scale`` (default: ``scale``)."""
     ctx = [int(c) for c in ctx]
     need = sum(_blocks(c, bs) for c in ctx)
     nb = pool if pool is not None else int(np.ceil(need * (1.0 + slack)))
@@ -110,7 +112,7 @@ def _decode_workload(name, rng, dtype, hq, hkv, d, bs, ctx, scale, pool=None, sl
         row += 1
     k_rows = _values(rng, (row, hkv, d), dtype, scale)
     v_rows = _values(rng, (row, hkv, d), dtype, scale)
-    q = _values(rng, (len(ctx), hq, d), dtype, scale)
+    q = _values(rng, (len(ctx), hq, d), dtype, scale if q_scale is None else q_scale)
     batch = [(s, 1) for s in range(len(ctx))]
     return Workload(name, dtype, hq, hkv, d, bs, nb, free_order, setup, step, batch, q,
                     k_rows, v_rows, notes={"context_lens": ctx})
@@ -231,15 +233,18 @@ def make(config, seed=0, **kw):
     return {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}[config](seed=seed, **kw)
 
 
-def random_decode(seed, dtype, hq, hkv, d, bs, ctx, scale=1.0, pool=None, slack=0.1):
-    """A decode workload with explicit context lengths (for edge-case tests)."""
+def random_decode(seed, dtype, hq, hkv, d, bs, ctx, scale=1.0, pool=None, slack=0.1,
+                  q_scale=None):
+    """A decode workload with explicit context lengths (for edge-case tests);
+    ``q_scale`` draws the queries at another scale than the keys and values."""
     rng = np.random.default_rng(seed)
     return _decode_workload(f"decode-{dtype}-{hq}x{hkv}x{d}", rng, dtype, hq, hkv, d, bs, ctx,
-                            scale, pool=pool, slack=slack)
+                            scale, pool=pool, slack=slack, q_scale=q_scale)
 
 
-def random_varlen(seed, dtype, hq, hkv, d, bs, spans, scale=1.0, slack=0.1):
-    """A mixed batch from explicit (cached_prefix, qlen) spans (for edge-case tests)."""
+def random_varlen(seed, dtype, hq, hkv, d, bs, spans, scale=1.0, slack=0.1, q_scale=None):
+    """A mixed batch from explicit (cached_prefix, qlen) spans (for edge-case tests);
+    ``q_scale`` draws the queries at another scale than the keys and values."""
     rng = np.random.default_rng(seed)
     need = sum(_blocks(p + q, bs) for p, q in spans)
     nb = int(np.ceil(need * (1.0 + slack))) + 1
@@ -255,7 +260,8 @@ def random_varlen(seed, dtype, hq, hkv, d, bs, spans, scale=1.0, slack=0.1):
     k_rows = _values(rng, (row, hkv, d), dtype, scale)
     v_rows = _values(rng, (row, hkv, d), dtype, scale)
     batch = [(s, qn) for s, (_, qn) in enumerate(spans)]
-    q = _values(rng, (sum(qn for _, qn in spans), hq, d), dtype, scale)
+    q = _values(rng, (sum(qn for _, qn in spans), hq, d), dtype,
+                scale if q_scale is None else q_scale)
     return Workload(f"varlen-{dtype}", dtype, hq, hkv, d, bs, nb, free_order, setup, step, batch,
                     q, k_rows, v_rows,
                     notes={"context_lens": [p + qn for p, qn in spans]})
