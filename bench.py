@@ -381,6 +381,78 @@ def mixed_batch_summary(steps, warmup):
     }
 
 
+GQA_SOURCES = ("decode.cu", "decode_mma.cu", "decode_common.cuh", "pkv_device.cuh")
+
+
+def configs_summary(steps, warmup, with_int8=True):
+    """The other decode workloads, each timed as a whole step and as its parts.
+
+    Config 3 (Llama-3-8B-shaped GQA decode, 256 sequences, 32/8 heads, contexts
+    log-uniform in [1024, 8192], plus the append of its 256 new tokens) and
+    config 5 (8 groups x 8 branches sharing a 3000-token prompt's blocks, with
+    copy-on-write of the shared tail, plus 4 sequences at 32768 tokens; 64/8
+    heads).  Lengths, pool, block tables, forks and copies are the workloads'
+    own seeded draws; the K/V and q values are drawn on the device from the
+    same distribution (N(0,1) x 0.5, bf16), since the kernels' speed does not
+    depend on them (full-size parity of both workloads is in the GPU tests).
+    Every input is larger than L2 (config 5: about 0.7 GB of unique KV)."""
+    import torch
+
+    import paged_kv_cache_51_gb300 as pkv
+    import workloads
+    from paged_kv_cache_51_gb300 import runner
+
+    bw, kind, _, _ = peaks()
+    stream = torch.cuda.current_stream()
+    res = {}
+    for cfg in (3, 5):
+        w = workloads.make(cfg, values=False)
+        dc, step = runner.prepare(w)
+        acc = accounting(w, step)
+        ms, attn_ms = time_steps(step, steps, warmup)
+        if pkv.device_error() != 0:
+            raise SystemExit(f"device error in config {cfg}")
+        # the step's copy-on-write + append alone
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(steps):
+            step.write_kv()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        app_ms = a0.elapsed_time(a1) / steps
+        step_bytes = acc["attn_bytes"] + acc["append_bytes"]
+        attn_gbs = acc["attn_bytes"] / (attn_ms * 1e-3) / 1e9
+        r = {
+            "workload": w.name, "batch": len(w.batch), "heads": [w.num_q_heads, w.num_kv_heads],
+            "context_tokens": acc["context_tokens"], "ms_per_step": ms,
+            "step_gbs": step_bytes / (ms * 1e-3) / 1e9,
+            "attention": {"ms": attn_ms, "bytes": acc["attn_bytes"], "achieved_gbs": attn_gbs,
+                          "frac": attn_gbs / bw,
+                          "kernel": "planner + decode_split_mma_kernel + merge"},
+            "append": {"tokens": int(step.slot_mapping.numel()),
+                       "copy_pairs": int(step.pairs.shape[0]), "ms": app_ms,
+                       "bytes": acc["append_bytes"],
+                       "achieved_gbs": acc["append_bytes"] / (app_ms * 1e-3) / 1e9,
+                       "note": "copy-on-write + append of the step's tokens, launch-bound "
+                               "at this size"},
+            "peak": bw, "peak_kind": f"{kind} hbm_gbs (burst copy)",
+            "values": "drawn on the device, N(0,1) x 0.5 in bf16",
+        }
+        if cfg == 5:
+            dram = ncu_traffic("decode_prefix_sharing_g8.md", GQA_SOURCES)
+            r["attention"]["bytes_note"] = (
+                "logical bytes: every branch's reads of its shared prompt blocks count")
+            r["attention"]["dram_bytes_ncu"] = dram
+            r["attention"]["dram_gbs"] = (dram / (attn_ms * 1e-3) / 1e9) if dram else None
+        if with_int8:
+            step.run()
+            r["int8"] = int8_decode_summary(w, dc, step, steps, warmup, attn_ms, False)
+        res[f"config{cfg}"] = r
+        del dc, step
+        torch.cuda.empty_cache()
+    return res
+
+
 def next_rows_summary(reps=20, warmup=3):
     """The widened rows beside the hot path, each with its own figure.
 
@@ -726,6 +798,9 @@ def run_gpu(args):
     nxt = None
     if world == 1 and args.config == 2 and not args.no_next and not args.prefill_chunks:
         nxt = next_rows_summary()
+    others = None
+    if world == 1 and args.config == 2 and not args.no_configs and not args.prefill_chunks:
+        others = configs_summary(min(args.steps, 100), args.warmup, not args.no_int8)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -750,6 +825,7 @@ def run_gpu(args):
                      "bytes_per_launch": attn_b, "ms_per_launch": attn_ms,
                      "peak_kind": f"{peak_kind} hbm_gbs (burst copy)"},
         "mixed_batch": mixed,
+        "configs": others,
         "int8_kv_decode": int8,
         "next_rows": nxt,
         "cpu_baseline": cpu,
@@ -793,6 +869,8 @@ def main():
                     help="skip the 8-bit KV cache decode sub-measurement")
     ap.add_argument("--no-next", action="store_true",
                     help="skip the widened rows (fused RoPE append, composer, prefix pool)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the GQA (config 3) and prefix-sharing (config 5) workloads")
     ap.add_argument("--cpu-worker", action="store_true")
     ap.add_argument("--cpu-seqs", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -142,13 +142,19 @@ def _host_int32(values, name):
     if isinstance(values, np.ndarray):
         a = values
     else:
-        vals = list(values)
-        if any(isinstance(x, (bool, np.bool_)) or not isinstance(x, (int, np.integer))
-               for x in vals):
+        vals = values if isinstance(values, (list, tuple)) else list(values)
+        if len(vals) == 0:
+            return np.zeros(0, dtype=np.int32)
+        try:
+            a = np.asarray(vals)
+        except OverflowError as e:
+            raise ValueError(f"{name}: a value is outside int32") from e
+        if a.dtype.kind in "fO":
+            # numpy widens ints beyond int64 (or int64 mixed with uint64) to
+            # object or float: out of range if every element is an int
+            if all(isinstance(x, (int, np.integer)) and not isinstance(x, bool) for x in vals):
+                raise ValueError(f"{name}: a value is outside int32")
             raise TypeError(f"{name}: integers expected")
-        if any(not _I32_MIN <= int(x) <= _I32_MAX for x in vals):
-            raise ValueError(f"{name}: a value is outside int32")
-        a = np.asarray(vals, dtype=np.int64).reshape(len(vals))
     if a.dtype.kind not in "iu":
         raise TypeError(f"{name}: integers expected, got {a.dtype}")
     if a.size and (int(a.min()) < _I32_MIN or int(a.max()) > _I32_MAX):

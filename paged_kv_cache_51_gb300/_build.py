@@ -25,8 +25,9 @@ CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-fvisibility=hidden", "-I",
              os.path.join(ROOT, "include")]
 
 
-# per-file extra flags: the prefill softmax uses the hardware exp2 directly
-EXTRA_FLAGS = {"prefill_tc.cu": ["--use_fast_math"]}
+# per-file extra flags (none: the prefill softmax calls the hardware exp2
+# through inline PTX, so no unit needs fast-math code generation)
+EXTRA_FLAGS = {}
 
 
 def _nvcc():

@@ -328,6 +328,15 @@ __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// 2^x on the MUFU unit in one instruction (PTX ex2.approx.ftz.f32: a few ulps
+// of relative error, subnormal results flushed to zero).  The softmax weights
+// and rescale factors only; everything else in this file keeps IEEE fp32.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 // max(a, b, c) in one instruction (three-input form of max.f32)
 __device__ __forceinline__ float max3f(float a, float b, float c) {
     float r;
@@ -798,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool need = m_new > m + kRescaleThreshold;  // first visible keys included
                 float alpha = 1.f;
                 if (need) {
-                    alpha = exp2f(m - m_new);
+                    alpha = ex2_approx(m - m_new);
                     m = m_new;
                     l *= alpha;
                 }
@@ -813,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
                     const float2 e = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), sc2, nm2);
-                    const float p0 = exp2f(e.x), p1 = exp2f(e.y);
+                    const float p0 = ex2_approx(e.x), p1 = ex2_approx(e.y);
                     sum4[c & 3] = __fadd2_rn(sum4[c & 3], make_float2(p0, p1));
                     w[c] = pack_bf16(p0, p1);
                 }
@@ -892,7 +901,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             const float2 o0 = st_set[r], o1 = st_set[kRows + r];
             const float M = fmaxf(o0.x, o1.x);
-            const float a0 = exp2f(o0.x - M), a1 = exp2f(o1.x - M);
+            const float a0 = ex2_approx(o0.x - M), a1 = ex2_approx(o1.x - M);
             const float inv = 1.f / (o0.y * a0 + o1.y * a1);
             const float w0 = a0 * inv, w1 = a1 * inv;
             // this thread's 64 output dims (bf16 pairs): chunk c = dims 8c .. 8c + 7

@@ -31,7 +31,11 @@ def _torch_rows(rows, dtype):
 
 
 class DeviceCache:
-    def __init__(self, w, device="cuda"):
+    def __init__(self, w, device="cuda", value_seed=0):
+        """A workload without value rows (``k_rows`` None) gets its K/V rows and
+        queries drawn on the device: N(0,1) times the workload's value scale,
+        rounded to the cache dtype, from a torch generator seeded with
+        ``value_seed``.  Timing runs use this; parity runs use the host rows."""
         self.w = w
         self.device = torch.device(device)
         tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
@@ -42,6 +46,29 @@ class DeviceCache:
         self.pool = BlockPool(w.num_blocks, w.block_size, 0, w.free_order)
         self._slots, self._rows, self._pairs = [], [], []
         self.step_slots, self.step_rows, self.step_pairs = [], [], []
+        self._dev_rows = None
+        if w.k_rows is None:
+            g = torch.Generator(device=self.device)
+            g.manual_seed(value_seed)
+            sc = w.notes["value_scale"]
+            n = w.notes["value_rows"]
+
+            def draw(shape_):
+                x = torch.randn(shape_, generator=g, device=self.device, dtype=torch.float32)
+                return (x * sc).to(tdt)
+
+            self._dev_rows = (draw((n, w.num_kv_heads, w.head_dim)),
+                              draw((n, w.num_kv_heads, w.head_dim)),
+                              draw((sum(q for _, q in w.batch), w.num_q_heads, w.head_dim)))
+
+    def _value_rows(self, rows):
+        """K and V rows (indices into the workload's value rows) in the cache dtype."""
+        w = self.w
+        if self._dev_rows is not None:
+            idx = torch.as_tensor(np.asarray(rows, dtype=np.int64)).to(self.device)
+            return self._dev_rows[0][idx], self._dev_rows[1][idx]
+        r = np.asarray(rows)
+        return _torch_rows(w.k_rows[r], w.dtype), _torch_rows(w.v_rows[r], w.dtype)
 
     # ---- planning -------------------------------------------------------
     def _apply(self, op, record):
@@ -78,7 +105,6 @@ class DeviceCache:
 
     # ---- device work ----------------------------------------------------
     def flush(self, chunk_tokens=1 << 16):
-        w = self.w
         if self._pairs:
             pairs = torch.tensor(self._pairs, dtype=torch.int32).to(self.device)
             pkv_copy_blocks(pairs, self.k_cache, self.v_cache, self.desc)
@@ -86,10 +112,9 @@ class DeviceCache:
         slots, rows = self._slots, self._rows
         for a in range(0, len(slots), chunk_tokens):
             s = torch.tensor(slots[a:a + chunk_tokens], dtype=torch.int64).to(self.device)
-            r = np.asarray(rows[a:a + chunk_tokens])
-            k = _torch_rows(w.k_rows[r], w.dtype).to(self.device)
-            v = _torch_rows(w.v_rows[r], w.dtype).to(self.device)
-            paged_kv_append(k, v, s, self.k_cache, self.v_cache, self.desc)
+            k, v = self._value_rows(rows[a:a + chunk_tokens])
+            paged_kv_append(k.to(self.device), v.to(self.device), s, self.k_cache, self.v_cache,
+                            self.desc)
         self._slots, self._rows = [], []
 
     def run_setup(self):
@@ -105,12 +130,11 @@ class DeviceCache:
             self._apply(op, record=True)
         # the step's copies and appends stay queued: hand them to the caller
         self._slots, self._rows, self._pairs = [], [], []
-        w = self.w
-        r = np.asarray(self.step_rows)
+        k, v = self._value_rows(self.step_rows)
         return {
             "slot_mapping": torch.tensor(self.step_slots, dtype=torch.int64),
-            "k": _torch_rows(w.k_rows[r], w.dtype),
-            "v": _torch_rows(w.v_rows[r], w.dtype),
+            "k": k,
+            "v": v,
             "pairs": torch.tensor(self.step_pairs, dtype=torch.int32).reshape(-1, 2),
         }
 
@@ -126,6 +150,8 @@ class DeviceCache:
         return tables, ctx, qsl
 
     def q_tensor(self):
+        if self._dev_rows is not None:
+            return self._dev_rows[2]
         return _torch_rows(self.w.q, self.w.dtype)
 
 

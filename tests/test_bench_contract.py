@@ -55,3 +55,23 @@ def test_reference_covers_decode_configs_only():
 
     with pytest.raises(SystemExit):
         bench.oracle_sample(4, 1)
+
+
+@pytest.mark.parametrize("cfg", [3, 5])
+def test_structure_only_workloads_match_the_full_ones(cfg):
+    """The bench's GQA and prefix-sharing lines run the workloads' own seeded
+    structure (lengths, pool, operations, batch) with values drawn on the
+    device; the structure must be the one the parity tests use."""
+    import workloads
+
+    kw = {"batch": 8} if cfg == 3 else {"groups": 2, "branches": 3, "prompt": 100, "n_long": 1,
+                                        "long_ctx": 600}
+    full = workloads.make(cfg, **kw)
+    bare = workloads.make(cfg, values=False, **kw)
+    assert bare.k_rows is None and bare.v_rows is None and bare.q is None
+    assert bare.notes["value_rows"] == full.k_rows.shape[0]
+    assert bare.notes["value_scale"] == 0.5
+    assert (bare.free_order == full.free_order).all()
+    assert bare.setup == full.setup and bare.step == full.step and bare.batch == full.batch
+    assert bare.num_blocks == full.num_blocks
+    assert bare.notes["context_lens"] == full.notes["context_lens"]

@@ -92,9 +92,10 @@ def _blocks(n, bs):
 
 
 def _decode_workload(name, rng, dtype, hq, hkv, d, bs, ctx, scale, pool=None, slack=0.1,
-                     q_scale=None):
+                     q_scale=None, values=True):
     """One query token per sequence; sequence s holds ctx[s]-1 cached tokens before the step.
-    Queries are drawn at ``q_scale`` (default: ``scale``)."""
+    Queries are drawn at ``q_scale`` (default: ``scale``).  ``values=False``
+    leaves the value rows to the caller (see ``_no_values``)."""
     ctx = [int(c) for c in ctx]
     need = sum(_blocks(c, bs) for c in ctx)
     nb = pool if pool is not None else int(np.ceil(need * (1.0 + slack)))
@@ -110,12 +111,27 @@ def _decode_workload(name, rng, dtype, hq, hkv, d, bs, ctx, scale, pool=None, sl
         else:
             step.append(("add", s, 1, row))
         row += 1
+    batch = [(s, 1) for s in range(len(ctx))]
+    notes = {"context_lens": ctx}
+    if not values:
+        return _no_values(Workload(name, dtype, hq, hkv, d, bs, nb, free_order, setup, step,
+                                   batch, None, None, None, notes=notes), row, scale)
     k_rows = _values(rng, (row, hkv, d), dtype, scale)
     v_rows = _values(rng, (row, hkv, d), dtype, scale)
     q = _values(rng, (len(ctx), hq, d), dtype, scale if q_scale is None else q_scale)
-    batch = [(s, 1) for s in range(len(ctx))]
     return Workload(name, dtype, hq, hkv, d, bs, nb, free_order, setup, step, batch, q,
-                    k_rows, v_rows, notes={"context_lens": ctx})
+                    k_rows, v_rows, notes=notes)
+
+
+def _no_values(w, n_rows, scale):
+    """A workload whose structure (lengths, pool, operations, batch) is drawn but
+    whose value rows are not: ``k_rows``, ``v_rows`` and ``q`` are None and the
+    notes give the row count and the value scale, for a consumer that draws
+    values of the same distribution itself (timing runs, whose speed does not
+    depend on the values)."""
+    w.notes["value_rows"] = int(n_rows)
+    w.notes["value_scale"] = float(scale)
+    return w
 
 
 def config1(seed=0):
@@ -132,11 +148,12 @@ def config2(seed=0, batch=64):
     return _decode_workload(CONFIG_NAMES[2], rng, "bf16", 32, 32, 128, 16, ctx, 0.5)
 
 
-def config3(seed=0, batch=256):
+def config3(seed=0, batch=256, values=True):
     """Llama-3-8B-shaped GQA decode: bf16, 32/8 heads, ctx log-uniform in [1024, 8192]."""
     rng = np.random.default_rng(seed)
     ctx = np.rint(np.exp(rng.uniform(np.log(1024), np.log(8192), size=batch))).astype(int)
-    return _decode_workload(CONFIG_NAMES[3], rng, "bf16", 32, 8, 128, 16, ctx, 0.5)
+    return _decode_workload(CONFIG_NAMES[3], rng, "bf16", 32, 8, 128, 16, ctx, 0.5,
+                            values=values)
 
 
 def config4(seed=0, n_decode=512, chunk=512, prefixes=(0, 1024, 3072)):
@@ -174,7 +191,7 @@ def config4(seed=0, n_decode=512, chunk=512, prefixes=(0, 1024, 3072)):
 
 
 def config5(seed=0, groups=8, branches=8, prompt=3000, max_private=200, n_long=4,
-            long_ctx=32768):
+            long_ctx=32768, values=True):
     """Parallel sampling + long context: bf16, 64/8 heads.  Each group's prompt is
     forked into ``branches`` branches that share its blocks; the prompt sequence is
     then freed; each branch generates U{1..max_private} private tokens, the last of
@@ -222,6 +239,10 @@ def config5(seed=0, groups=8, branches=8, prompt=3000, max_private=200, n_long=4
         batch.append((sid, 1))
         ctx.append(long_ctx)
         sid += 1
+    if not values:
+        return _no_values(Workload(CONFIG_NAMES[5], "bf16", hq, hkv, d, bs, nb, free_order,
+                                   setup, step, batch, None, None, None,
+                                   notes={"context_lens": ctx}), row, 0.5)
     k_rows = _values(rng, (row, hkv, d), "bf16", 0.5)
     v_rows = _values(rng, (row, hkv, d), "bf16", 0.5)
     q = _values(rng, (len(batch), hq, d), "bf16", 0.5)
