@@ -27,6 +27,13 @@ Readings of points the pages leave open:
     0 .. ctx-qlen+i (causal) [Ch15 §15.6 两阶段与 Chunked Prefill;
     FastGen §3.2 动态分割融合].
   * scale defaults to 1/sqrt(head_dim).
+  * Sliding window ``window`` = W > 0 [Deploy §2.1 block_sliding_window: the
+    pages keep only a window of blocks per sequence and say nothing about the
+    mask]: a query attends the W most recent keys up to and including its own
+    position, i.e. table indices max(0, a - W + 1) .. a for a query at table
+    index a.  The table must list the sequence's blocks in logical order (it
+    may start past logical block 0, so table index = position - first
+    position of the table); W = 0 means no window.
 """
 
 import math
@@ -57,12 +64,13 @@ def gather_sequence(cache, table_row, ctx, block_size):
     return dense[:ctx]
 
 
-def softmax_attention(q, k, v, scale, n_visible=None):
+def softmax_attention(q, k, v, scale, n_visible=None, first_visible=None):
     """Exact attention for a set of query rows against one key/value sequence.
 
     q: [nq, D] float64; k, v: [n, D] float64.  ``n_visible[i]`` (optional) is
     how many leading keys query row i may see (causal masking); all keys if
-    None.  Returns [nq, D] float64.
+    None.  ``first_visible[i]`` (optional) is the first key row i may see (a
+    sliding window); key 0 if None.  Returns [nq, D] float64.
     """
     s = (q @ k.T) * scale
     if n_visible is not None:
@@ -71,6 +79,14 @@ def softmax_attention(q, k, v, scale, n_visible=None):
             raise ValueError("every query must see between 1 and n keys")
         cols = np.arange(k.shape[0])[None, :]
         s = np.where(cols < n_visible[:, None], s, -np.inf)
+    if first_visible is not None:
+        first_visible = np.asarray(first_visible)
+        last = (np.asarray(n_visible) if n_visible is not None
+                else np.full(q.shape[0], k.shape[0]))
+        if np.any(first_visible < 0) or np.any(first_visible >= last):
+            raise ValueError("every query must see at least one key")
+        cols = np.arange(k.shape[0])[None, :]
+        s = np.where(cols >= first_visible[:, None], s, -np.inf)
     s = s - s.max(axis=1, keepdims=True)
     p = np.exp(s)
     return (p @ v) / p.sum(axis=1, keepdims=True)
@@ -82,12 +98,19 @@ def _check_heads(num_q_heads, num_kv_heads):
     return num_q_heads // num_kv_heads
 
 
-def decode(q, k_cache, v_cache, block_tables, context_lens, block_size, dtype, scale=None):
+def _first_visible(last, window):
+    """First key a query whose last visible key is ``last`` attends (table indices)."""
+    return np.maximum(0, np.asarray(last) - window + 1) if window else None
+
+
+def decode(q, k_cache, v_cache, block_tables, context_lens, block_size, dtype, scale=None,
+           window=0):
     """One query token per sequence.
 
     q: [S, Hq, D] (cache dtype storage); caches [NB, Hkv, bs, D];
     block_tables [S, W] int; context_lens [S] (>= 1, includes the query's own
-    token).  Returns float64 [S, Hq, D].
+    token); ``window`` > 0: a sliding window of that many keys.  Returns
+    float64 [S, Hq, D].
     """
     S, Hq, D = q.shape
     Hkv = k_cache.shape[1]
@@ -102,19 +125,21 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, block_size, dtype, s
             raise ValueError("context length must be >= 1")
         kd = widen(gather_sequence(k_cache, block_tables[s], ctx, block_size), dtype)
         vd = widen(gather_sequence(v_cache, block_tables[s], ctx, block_size), dtype)
+        first = _first_visible([ctx - 1], window)
         for h in range(Hq):
             kvh = h // g
-            out[s, h] = softmax_attention(qf[s, h][None, :], kd[:, kvh], vd[:, kvh], scale)[0]
+            out[s, h] = softmax_attention(qf[s, h][None, :], kd[:, kvh], vd[:, kvh], scale,
+                                          first_visible=first)[0]
     return out
 
 
 def varlen(q, k_cache, v_cache, block_tables, query_start_loc, context_lens, block_size,
-           dtype, scale=None):
+           dtype, scale=None, window=0):
     """Ragged batch: sequence s owns query rows query_start_loc[s] .. query_start_loc[s+1]-1.
 
     Rows of a sequence are its last ``qlen`` positions; row i sees keys
-    0 .. ctx-qlen+i.  A sequence with qlen == 1 is a decode row.  Returns
-    float64 [Tq, Hq, D].
+    0 .. ctx-qlen+i (with a sliding window W > 0: from max(0, ctx-qlen+i-W+1)).
+    A sequence with qlen == 1 is a decode row.  Returns float64 [Tq, Hq, D].
     """
     Tq, Hq, D = q.shape
     Hkv = k_cache.shape[1]
@@ -138,8 +163,9 @@ def varlen(q, k_cache, v_cache, block_tables, query_start_loc, context_lens, blo
         kd = widen(gather_sequence(k_cache, block_tables[s], ctx, block_size), dtype)
         vd = widen(gather_sequence(v_cache, block_tables[s], ctx, block_size), dtype)
         n_visible = ctx - qlen + 1 + np.arange(qlen)
+        first = _first_visible(n_visible - 1, window)
         for h in range(Hq):
             kvh = h // g
             out[r0:r1, h] = softmax_attention(qf[r0:r1, h], kd[:, kvh], vd[:, kvh], scale,
-                                              n_visible)
+                                              n_visible, first)
     return out

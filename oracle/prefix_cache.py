@@ -42,7 +42,19 @@ Readings where the pages are silent:
     a later token of the same prompt takes get slot -1 (skip); the exported
     table lists the physical blocks of the last W_b logical blocks in logical
     order, with context min(len, window).
+  * Sliding window with prefill chunks: a chunk of C queries needs the C + W - 1
+    most recent keys at once, more than a ring of exactly W tokens holds, so a
+    pool that serves chunks of up to ``max_chunk`` tokens keeps
+    R_b = W_b + ceil((max_chunk - 1) / block_size) ring blocks (max_chunk = 1:
+    the pages' ring).  The ring then holds the last R_b * block_size tokens.
+    For a step whose last ``qlen`` tokens are queries, ``logical_table`` lists
+    the ring entries of logical blocks first .. last in logical order, where
+    ``first`` holds the first key any of those queries attends, with context
+    = len - first * block_size; attention then applies the window as a mask
+    (the rows below the window in the first entry may hold newer tokens).
 """
+
+import math
 
 from .block_pool import LATER, NEVER, OK, PoolError
 
@@ -251,17 +263,21 @@ class PrefixCachingPool:
 
 
 class SlidingWindowPool:
-    """Block pool whose tables are rings of ceil(window / block_size) blocks."""
+    """Block pool whose tables are rings of window / block_size blocks, plus
+    ceil((max_chunk - 1) / block_size) for pools that serve prefill chunks."""
 
-    def __init__(self, num_blocks, block_size, window, watermark_blocks=0, free_order=None):
-        if num_blocks < 1 or block_size < 1 or watermark_blocks < 0:
+    def __init__(self, num_blocks, block_size, window, watermark_blocks=0, free_order=None,
+                 max_chunk=1):
+        if num_blocks < 1 or block_size < 1 or watermark_blocks < 0 or max_chunk < 1:
             raise PoolError("bad pool parameters")
         if window < block_size or window % block_size:
             raise PoolError("window must be a positive multiple of block_size")
         self.num_blocks = num_blocks
         self.block_size = block_size
         self.window = window
-        self.ring = window // block_size
+        self.max_chunk = max_chunk
+        self.ring = window // block_size + math.ceil((max_chunk - 1) / block_size)
+        self.capacity = self.ring * block_size    # tokens the ring holds
         self.watermark_blocks = watermark_blocks
         order = list(range(num_blocks)) if free_order is None else [int(b) for b in free_order]
         if sorted(order) != list(range(num_blocks)):
@@ -312,7 +328,7 @@ class SlidingWindowPool:
             return st, None
         self.tables[seq] = [self._take() for _ in range(self.blocks_needed(n))]
         self.lens[seq] = n
-        return OK, [self.slot_of(seq, p) if p + self.window >= n else -1 for p in range(n)]
+        return OK, [self.slot_of(seq, p) if p + self.capacity >= n else -1 for p in range(n)]
 
     def fork(self, parent, child):
         if parent not in self.tables or child in self.tables:
@@ -348,8 +364,25 @@ class SlidingWindowPool:
         del self.lens[seq]
 
     def window_table(self, seq):
-        """(physical blocks of the last W_b logical blocks in logical order, context length)."""
+        """(physical blocks of the last W_b logical blocks in logical order, context length):
+        exactly the last ``window`` tokens, for decode without a mask; only a ring of
+        exactly W_b blocks (max_chunk = 1) has that property."""
+        if self.ring != self.window // self.block_size:
+            raise PoolError("a ring with chunk room needs logical_table and a window mask")
         n, bs = self.lens[seq], self.block_size
         nb = -(-n // bs)
         first = max(0, nb - self.ring)
         return [self.tables[seq][j % self.ring] for j in range(first, nb)], min(n, self.window)
+
+    def logical_table(self, seq, qlen=1):
+        """(ring entries of logical blocks first .. last in logical order, context) for a
+        step whose last ``qlen`` tokens are queries under the window: ``first`` is the
+        block of the first key the first query attends, context = len - first * bs."""
+        n, bs = self.lens[seq], self.block_size
+        if not 1 <= qlen <= n:
+            raise PoolError("query span must be 1 .. sequence length")
+        if qlen + self.window - 1 > self.capacity:
+            raise PoolError("the ring cannot hold the keys of that many queries")
+        first = max(0, n - qlen - self.window + 1) // bs
+        nb = -(-n // bs)
+        return [self.tables[seq][j % self.ring] for j in range(first, nb)], n - first * bs

@@ -98,3 +98,49 @@ def execute(w, with_attention=True, scale=None):
     st.run_step()
     out = st.attention(scale) if with_attention else None
     return st, out
+
+
+def execute_window_trace(tr):
+    """Run a sliding-window trace (``workloads.WindowTrace``) with the oracle's
+    window pool (ring with room for ``max_chunk`` queries), cache mirror and
+    windowed attention.  Returns (per-step float64 outputs [Tq, Hq, D], final
+    K cache, final V cache)."""
+    from .prefix_cache import SlidingWindowPool
+
+    pool = SlidingWindowPool(tr.num_blocks, tr.block_size, tr.window, 0, tr.free_order,
+                             tr.max_chunk)
+    dt = np.float32 if tr.dtype == "f32" else np.uint16
+    shape = (tr.num_blocks, tr.num_kv_heads, tr.block_size, tr.head_dim)
+    kc, vc = np.zeros(shape, dtype=dt), np.zeros(shape, dtype=dt)
+    lens, outs = {}, []
+    for i, step in enumerate(tr.steps):
+        for seq, qlen in step:
+            n = lens.get(seq, 0)
+            rows = tr.row_offset[seq] + np.arange(n, n + qlen)
+            if n == 0:
+                st, slots = pool.add_sequence(seq, qlen)
+                if st != OK:
+                    raise RuntimeError(f"window pool refused a chunk: {st}")
+            else:
+                slots = []
+                for _ in range(qlen):
+                    slot, cow = pool.append_slot(seq)
+                    if slot is None:
+                        raise RuntimeError("window pool exhausted")
+                    if cow is not None:
+                        cache.copy_blocks(kc, vc, [cow])
+                    slots.append(slot)
+            cache.append(kc, vc, tr.k_rows[rows], tr.v_rows[rows], slots, tr.block_size)
+            lens[seq] = n + qlen
+        tabs = [pool.logical_table(seq, qlen) for seq, qlen in step]
+        width = max(len(t) for t, _ in tabs)
+        bt = np.full((len(step), width), -1, dtype=np.int32)
+        for j, (t, _) in enumerate(tabs):
+            bt[j, :len(t)] = t
+        ctx = np.array([c for _, c in tabs], dtype=np.int32)
+        qsl = np.zeros(len(step) + 1, dtype=np.int32)
+        qsl[1:] = np.cumsum([q for _, q in step])
+        q = tr.q_rows[tr.q_offset[i]:tr.q_offset[i + 1]]
+        outs.append(attention.varlen(q, kc, vc, bt, qsl, ctx, tr.block_size, tr.dtype,
+                                     window=tr.window))
+    return outs, kc, vc

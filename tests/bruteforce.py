@@ -37,8 +37,9 @@ def attend(qvec, keys, vals, scale):
     return [math.fsum(wts[j] * vals[j][i] for j in range(len(keys))) / tot for i in range(d)]
 
 
-def run(w, rows_by_seq=None, scale=None):
-    """Return out[qrow][head] = list of D floats for every query row of the batch."""
+def run(w, rows_by_seq=None, scale=None, window=0):
+    """Return out[qrow][head] = list of D floats for every query row of the batch
+    (``window`` > 0: each query sees only its ``window`` most recent tokens)."""
     rows_by_seq = rows_by_seq or dense_sequences(w)
     hq, hkv, d = w.num_q_heads, w.num_kv_heads, w.head_dim
     g = hq // hkv
@@ -50,13 +51,41 @@ def run(w, rows_by_seq=None, scale=None):
         toks = rows_by_seq[seq]
         ctx = len(toks)
         for i in range(qlen):
-            visible = toks[:ctx - qlen + i + 1]
+            last = ctx - qlen + i
+            visible = toks[max(0, last - window + 1) if window else 0:last + 1]
             heads = []
             for h in range(hq):
                 kv = h // g
                 qv = [widen_scalar(x, w.dtype) for x in w.q[r, h]]
                 ks = [[widen_scalar(x, w.dtype) for x in w.k_rows[t, kv]] for t in visible]
                 vs = [[widen_scalar(x, w.dtype) for x in w.v_rows[t, kv]] for t in visible]
+                heads.append(attend(qv, ks, vs, scale))
+            out.append(heads)
+            r += 1
+    return out
+
+
+def window_trace_step(tr, step_index, lens_after):
+    """Dense windowed attention of one step of a sliding-window trace, straight
+    from the trace's unpaged rows: query i of (seq, qlen) sits at position
+    lens_after[seq] - qlen + i and sees positions max(0, pos - window + 1) .. pos."""
+    hq, hkv, d = tr.num_q_heads, tr.num_kv_heads, tr.head_dim
+    g = hq // hkv
+    scale = 1.0 / math.sqrt(d)
+    out = []
+    r = tr.q_offset[step_index]
+    for seq, qlen in tr.steps[step_index]:
+        n = lens_after[seq]
+        for i in range(qlen):
+            pos = n - qlen + i
+            first = max(0, pos - tr.window + 1)
+            rows = [tr.row_offset[seq] + t for t in range(first, pos + 1)]
+            heads = []
+            for h in range(hq):
+                kv = h // g
+                qv = [widen_scalar(x, tr.dtype) for x in tr.q_rows[r, h]]
+                ks = [[widen_scalar(x, tr.dtype) for x in tr.k_rows[t, kv]] for t in rows]
+                vs = [[widen_scalar(x, tr.dtype) for x in tr.v_rows[t, kv]] for t in rows]
                 heads.append(attend(qv, ks, vs, scale))
             out.append(heads)
             r += 1

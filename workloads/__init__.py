@@ -349,6 +349,67 @@ def serving_trace(seed=0, n_requests=6, prompt_range=(20, 700), gen_range=(1, 6)
                         k_rows, v_rows, q_rows)
 
 
+@dataclass
+class WindowTrace:
+    """A multi-step run of sequences under a sliding window.
+
+    ``steps[i]`` lists (seq, qlen) in query-row order: a sequence's first
+    entry adds its first prompt chunk, later entries append qlen tokens (the
+    rest of the prompt in chunks of at most ``max_chunk``, then one token per
+    decode step), and every entry's qlen new tokens are that step's queries.
+    Token p of sequence s has K/V rows ``row_offset[s] + p``; step i's query
+    rows are ``q_rows[q_offset[i]:q_offset[i + 1]]``."""
+    dtype: str
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    window: int
+    max_chunk: int
+    num_blocks: int
+    free_order: np.ndarray
+    steps: list
+    row_offset: list
+    q_offset: list
+    k_rows: np.ndarray
+    v_rows: np.ndarray
+    q_rows: np.ndarray
+
+
+def window_trace(seed=0, dtype="bf16", hq=32, hkv=8, d=128, bs=16, window=256, max_chunk=200,
+                 prompts=(700, 130, 1000), gens=(3, 40, 2), scale=0.5):
+    """A seeded windowed run: every step, each unfinished prompt takes a chunk of
+    U{1..max_chunk} tokens (at most what is left) and each finished one decodes
+    one token, until every sequence has its prompt and generated tokens."""
+    rng = np.random.default_rng(seed)
+    lengths = [p + g for p, g in zip(prompts, gens)]
+    done = [0] * len(prompts)
+    steps = []
+    while any(n < L for n, L in zip(done, lengths)):
+        step = []
+        for s, (p, L) in enumerate(zip(prompts, lengths)):
+            if done[s] >= L:
+                continue
+            if done[s] < p:
+                c = min(int(rng.integers(1, max_chunk, endpoint=True)), p - done[s])
+            else:
+                c = 1
+            step.append((s, c))
+            done[s] += c
+        steps.append(step)
+    ring = window // bs + _blocks(max_chunk - 1, bs)
+    nb = len(prompts) * ring + 4
+    free_order = rng.permutation(nb).astype(np.int32)
+    offs = [int(x) for x in np.concatenate([[0], np.cumsum(lengths)[:-1]])]
+    q_off = [int(x) for x in np.concatenate([[0], np.cumsum([sum(q for _, q in st)
+                                                              for st in steps])])]
+    k_rows = _values(rng, (sum(lengths), hkv, d), dtype, scale)
+    v_rows = _values(rng, (sum(lengths), hkv, d), dtype, scale)
+    q_rows = _values(rng, (q_off[-1], hq, d), dtype, scale)
+    return WindowTrace(dtype, hq, hkv, d, bs, window, max_chunk, nb, free_order, steps, offs,
+                       q_off, k_rows, v_rows, q_rows)
+
+
 class TokenValues:
     """K/V rows that depend only on (token id, position), as a model's K/V depend
     on the token prefix: row(t, p) = bf16(E[t] + P[p]) with E, P seeded normal
