@@ -153,6 +153,24 @@ PKV_API int pkv_pool_destroy(pkv_pool* pool);
 PKV_API int pkv_pool_create_ex(int32_t num_blocks, int32_t block_size, int32_t watermark_blocks,
                                const int32_t* free_order, int32_t flags, int32_t sliding_window,
                                pkv_pool** out);
+
+/* Sliding-window pool that also serves prefill chunks [Deploy §2.1
+ * block_sliding_window; the pages leave the attention mask open, and the
+ * reading taken is that a query at position p sees keys max(0, p - W + 1) .. p,
+ * W = sliding_window].  A chunk of C queries needs its C + W - 1 most recent
+ * keys at once, more than a ring of W_b = W / block_size blocks holds, so the
+ * ring here has W_b + ceil((max_chunk - 1) / block_size) blocks and holds the
+ * last ring * block_size tokens; max_chunk = 1 is the pool of
+ * pkv_pool_create_ex.  Everything else is as there: admission counts
+ * min(blocks, ring); a prompt token whose slot a later token of the same
+ * prompt takes gets slot -1; a shared ring block is copied before a write.
+ * Chunked prompts are added with their first chunk (pkv_seq_add) and grown
+ * chunk by chunk (pkv_seq_append_slot per token); attention takes tables from
+ * pkv_window_tables and the window from paged_attention_varlen_window.
+ * sliding_window: a positive multiple of block_size; max_chunk >= 1. */
+PKV_API int pkv_pool_create_window(int32_t num_blocks, int32_t block_size,
+                                   int32_t watermark_blocks, const int32_t* free_order,
+                                   int32_t sliding_window, int32_t max_chunk, pkv_pool** out);
 /* Free blocks, parked (evictable) blocks included. */
 PKV_API int pkv_pool_num_free(const pkv_pool* pool, int32_t* out);
 /* Parked blocks of a prefix-caching pool (0 otherwise). */
@@ -213,9 +231,26 @@ PKV_API int pkv_block_hash(const pkv_pool* pool, int32_t block, uint64_t* hash_o
 
 /* Export block tables and context lengths of `n` sequences (host buffers):
  * tables_out [n][max_blocks] padded with -1, ctx_lens_out [n] (optional).
- * PKV_ERR_INVALID if a table needs more than max_blocks entries. */
+ * PKV_ERR_INVALID if a table needs more than max_blocks entries.  A window
+ * pool whose ring has room for chunks (pkv_pool_create_window, max_chunk > 1)
+ * has no exact-window export: PKV_ERR_UNSUPPORTED (use pkv_window_tables). */
 PKV_API int pkv_block_tables(const pkv_pool* pool, const int64_t* seq_ids, int32_t n,
                      int32_t max_blocks, int32_t* tables_out, int32_t* ctx_lens_out);
+
+/* Tables of a sliding-window pool for paged_attention_varlen_window (host
+ * buffers).  For sequence i of length L whose last query_lens[i] = q tokens
+ * are this step's queries, the first key any of them attends is
+ * f = max(0, L - q - W + 1); the row lists the ring entries of logical blocks
+ * f / block_size .. ceil(L / block_size) - 1 in logical order (the first and
+ * the last entry may be the same physical block) and ctx_lens_out[i] =
+ * L - (f / block_size) * block_size, so table index t is position
+ * (f / block_size) * block_size + t.  Rows are padded with -1 to max_blocks.
+ * PKV_ERR_INVALID (nothing written) for an unknown sequence, q outside
+ * [1, L], q + W - 1 above the ring's tokens, or a row wider than max_blocks;
+ * PKV_ERR_UNSUPPORTED for a pool without a window. */
+PKV_API int pkv_window_tables(const pkv_pool* pool, const int64_t* seq_ids,
+                              const int32_t* query_lens, int32_t n, int32_t max_blocks,
+                              int32_t* tables_out, int32_t* ctx_lens_out);
 
 /* Compose one forward pass of a mixed batch under a token budget [FastGen
  * §3.2 动态分割融合: split long prompts, fuse short ones, keep every pass the
@@ -359,6 +394,30 @@ PKV_API int paged_attention_varlen(void* out, const void* q, const void* k_cache
                            int32_t num_query_tokens, int32_t max_query_len,
                            int32_t max_context_len, float scale, void* workspace,
                            size_t workspace_bytes, void* stream);
+
+/* paged_attention_varlen under a sliding window of `window` keys [Deploy §2.1
+ * block_sliding_window keeps a ring of blocks per sequence; the pages leave the
+ * mask open, and the reading taken is that a query sees its `window` most
+ * recent keys, its own included]: row i of sequence s attends table indices
+ *   max(0, a - window + 1) .. a,   a = context_lens[s] - qlen_s + i,
+ * where the table lists the sequence's blocks in logical order from any block
+ * (table index = position - the table's first position): the layout
+ * pkv_window_tables exports, whose context_lens count from that first block.
+ * Keys below a row's window are masked; decode rows (qlen 1) skip the blocks
+ * and 512-token splits below their window, and the split of a sequence
+ * depends only on its context length and the window, so results do not depend
+ * on the batch.  window = 0 is paged_attention_varlen; window < 0 is
+ * PKV_ERR_INVALID.  Other arguments, workspace and errors as for
+ * paged_attention_varlen. */
+PKV_API int paged_attention_varlen_window(void* out, const void* q, const void* k_cache,
+                                          const void* v_cache, const pkv_cache_desc* desc,
+                                          const int32_t* block_tables,
+                                          int32_t max_blocks_per_seq,
+                                          const int32_t* query_start_loc,
+                                          const int32_t* context_lens, int32_t num_seqs,
+                                          int32_t num_query_tokens, int32_t max_query_len,
+                                          int32_t max_context_len, int32_t window, float scale,
+                                          void* workspace, size_t workspace_bytes, void* stream);
 
 /* 8-bit KV cache [Deploy §2.5 LMDeploy, 2. TurboMind 推理引擎解析 (the KV cache
  * kept in 8 bits, halving the bytes decode reads)].  The pages give no format;

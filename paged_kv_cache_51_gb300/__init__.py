@@ -49,7 +49,8 @@ EXPORTS = (
     "paged_attention_varlen", "pkv_device_error", "pkv_status_string", "pkv_splitfuse_compose",
     "paged_kv_append_int8", "paged_attention_decode_int8", "pkv_copy_blocks_int8",
     "pkv_pool_create_ex", "pkv_pool_num_evictable", "pkv_pool_set_clock", "pkv_seq_add_tokens",
-    "pkv_seq_append_token", "pkv_block_hash",
+    "pkv_seq_append_token", "pkv_block_hash", "pkv_pool_create_window", "pkv_window_tables",
+    "paged_attention_varlen_window",
 )
 
 PKV_POOL_PREFIX_CACHING = 1
@@ -83,6 +84,11 @@ def lib():
     sig = {
         "pkv_pool_create": (ctypes.c_int, [i32, i32, i32, p, P(p)]),
         "pkv_pool_create_ex": (ctypes.c_int, [i32, i32, i32, p, i32, i32, P(p)]),
+        "pkv_pool_create_window": (ctypes.c_int, [i32, i32, i32, p, i32, i32, P(p)]),
+        "pkv_window_tables": (ctypes.c_int, [p, p, p, i32, i32, p, p]),
+        "paged_attention_varlen_window": (ctypes.c_int, [p, p, p, p, P(CacheDesc), p, i32, p, p,
+                                                         i32, i32, i32, i32, i32, ctypes.c_float,
+                                                         p, sz, p]),
         "pkv_pool_num_evictable": (ctypes.c_int, [p, P(i32)]),
         "pkv_pool_set_clock": (ctypes.c_int, [p, i64]),
         "pkv_seq_add_tokens": (ctypes.c_int, [p, i64, p, i32, p, P(i32)]),
@@ -174,22 +180,33 @@ class BlockPool:
     """Host block pool (C++): ref-counted blocks, block tables, copy-on-write."""
 
     def __init__(self, num_blocks, block_size, watermark_blocks=0, free_order=None,
-                 prefix_caching=False, sliding_window=0):
+                 prefix_caching=False, sliding_window=0, max_chunk=1):
+        """``sliding_window`` > 0 with ``max_chunk`` > 1: a window pool whose ring
+        also holds the keys of prefill chunks of up to max_chunk tokens
+        (pkv_pool_create_window)."""
         self._h = ctypes.c_void_p()
         order = None
         if free_order is not None:
             order = _host_int32(free_order, "free_order")
             if order.shape != (num_blocks,):
                 raise ValueError(f"free_order: {order.shape[0]} entries, expected {num_blocks}")
-        flags = PKV_POOL_PREFIX_CACHING if prefix_caching else 0
-        _check(lib().pkv_pool_create_ex(num_blocks, block_size, watermark_blocks,
-                                        None if order is None else order.ctypes.data, flags,
-                                        sliding_window, ctypes.byref(self._h)),
-               "pkv_pool_create_ex")
+        optr = None if order is None else order.ctypes.data
+        if max_chunk != 1:
+            if prefix_caching or sliding_window < 1:
+                raise ValueError("max_chunk applies to sliding-window pools only")
+            _check(lib().pkv_pool_create_window(num_blocks, block_size, watermark_blocks, optr,
+                                                sliding_window, max_chunk, ctypes.byref(self._h)),
+                   "pkv_pool_create_window")
+        else:
+            flags = PKV_POOL_PREFIX_CACHING if prefix_caching else 0
+            _check(lib().pkv_pool_create_ex(num_blocks, block_size, watermark_blocks, optr, flags,
+                                            sliding_window, ctypes.byref(self._h)),
+                   "pkv_pool_create_ex")
         self.num_blocks = num_blocks
         self.block_size = block_size
         self.prefix_caching = prefix_caching
         self.sliding_window = sliding_window
+        self.max_chunk = max_chunk
 
     def close(self):
         if self._h:
@@ -293,6 +310,23 @@ class BlockPool:
         ctx = torch.empty(n, dtype=torch.int32)
         _check(lib().pkv_block_tables(self._h, ids.data_ptr(), n, max_blocks, tables.data_ptr(),
                                       ctx.data_ptr()), "pkv_block_tables")
+        return tables, ctx
+
+
+    def window_tables(self, seq_ids, query_lens, max_blocks):
+        """Logically ordered tables of a sliding-window pool for a step whose last
+        query_lens[i] tokens of sequence seq_ids[i] are queries (pkv_window_tables).
+        Returns (tables int32 tensor [n, max_blocks] padded with -1, ctx int32 [n])."""
+        n = len(seq_ids)
+        ids = torch.tensor(list(seq_ids), dtype=torch.int64)
+        ql = _host_int32(query_lens, "query_lens")
+        if ql.shape != (n,):
+            raise ValueError("query_lens: one entry per sequence")
+        tables = torch.empty((n, max_blocks), dtype=torch.int32)
+        ctx = torch.empty(n, dtype=torch.int32)
+        _check(lib().pkv_window_tables(self._h, ids.data_ptr(), ql.ctypes.data if n else None, n,
+                                       max_blocks, tables.data_ptr(), ctx.data_ptr()),
+               "pkv_window_tables")
         return tables, ctx
 
 
@@ -482,8 +516,10 @@ def paged_attention_decode_noalloc(out, q, k_cache, v_cache, desc, block_tables,
 
 def paged_attention_varlen(out, q, k_cache, v_cache, desc, block_tables, query_start_loc,
                            context_lens, max_query_len, max_context_len, scale=None, ws=None,
-                           stream=None):
-    """out, q: CUDA [Tq, Hq, D]; query_start_loc int32 [S+1]; context_lens int32 [S]."""
+                           stream=None, window=0):
+    """out, q: CUDA [Tq, Hq, D]; query_start_loc int32 [S+1]; context_lens int32 [S].
+    ``window`` > 0: sliding-window attention (paged_attention_varlen_window) over
+    logically ordered tables (BlockPool.window_tables)."""
     Tq = q.shape[0]
     S = context_lens.shape[0]
     dt = _TORCH_DTYPE[desc.dtype]
@@ -501,6 +537,13 @@ def paged_attention_varlen(out, q, k_cache, v_cache, desc, block_tables, query_s
     if ws is None:
         ws = workspace(varlen_workspace_bytes(desc, S, Tq, max_query_len, max_context_len),
                        q.device)
+    if window:
+        _check(lib().paged_attention_varlen_window(
+            _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc),
+            _ptr(block_tables), block_tables.shape[1], _ptr(query_start_loc), _ptr(context_lens),
+            S, Tq, max_query_len, max_context_len, int(window), scale, _ptr(ws), ws.numel(), st),
+            "paged_attention_varlen_window")
+        return out
     _check(lib().paged_attention_varlen(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                         ctypes.byref(desc), _ptr(block_tables),
                                         block_tables.shape[1], _ptr(query_start_loc),

@@ -160,14 +160,14 @@ extern "C" int paged_attention_decode(void* out, const void* q, const void* k_ca
     return launch_decode_merge(a);
 }
 
-extern "C" int paged_attention_varlen(void* out, const void* q, const void* k_cache,
-                                      const void* v_cache, const pkv_cache_desc* desc,
-                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                      const int32_t* query_start_loc, const int32_t* context_lens,
-                                      int32_t num_seqs, int32_t num_query_tokens,
-                                      int32_t max_query_len, int32_t max_context_len, float scale,
-                                      void* workspace, size_t workspace_bytes, void* stream) {
-    if (num_seqs < 0 || num_query_tokens < 0 || max_query_len < 0) return PKV_ERR_INVALID;
+static int varlen_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                       const pkv_cache_desc* desc, const int32_t* block_tables,
+                       int32_t max_blocks_per_seq, const int32_t* query_start_loc,
+                       const int32_t* context_lens, int32_t num_seqs, int32_t num_query_tokens,
+                       int32_t max_query_len, int32_t max_context_len, int32_t window,
+                       float scale, void* workspace, size_t workspace_bytes, void* stream) {
+    if (num_seqs < 0 || num_query_tokens < 0 || max_query_len < 0 || window < 0)
+        return PKV_ERR_INVALID;
     int st = check_attention_common(out, q, k_cache, v_cache, desc, block_tables,
                                     max_blocks_per_seq, context_lens, max_context_len, scale);
     if (st != PKV_OK) return st;
@@ -197,6 +197,7 @@ extern "C" int paged_attention_varlen(void* out, const void* q, const void* k_ca
     a.num_query_tokens = num_query_tokens;
     a.max_query_len = max_query_len;
     a.max_context_len = max_context_len;
+    a.window = window;
     a.scale = scale;
     a.stream = static_cast<cudaStream_t>(stream);
     if ((st = launch_plan(a)) != PKV_OK) return st;
@@ -208,6 +209,33 @@ extern "C" int paged_attention_varlen(void* out, const void* q, const void* k_ca
     }
     if ((st = launch_decode_split(a)) != PKV_OK) return st;
     return launch_decode_merge(a);
+}
+
+extern "C" int paged_attention_varlen(void* out, const void* q, const void* k_cache,
+                                      const void* v_cache, const pkv_cache_desc* desc,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* query_start_loc, const int32_t* context_lens,
+                                      int32_t num_seqs, int32_t num_query_tokens,
+                                      int32_t max_query_len, int32_t max_context_len, float scale,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+    return varlen_impl(out, q, k_cache, v_cache, desc, block_tables, max_blocks_per_seq,
+                       query_start_loc, context_lens, num_seqs, num_query_tokens, max_query_len,
+                       max_context_len, 0, scale, workspace, workspace_bytes, stream);
+}
+
+extern "C" int paged_attention_varlen_window(void* out, const void* q, const void* k_cache,
+                                             const void* v_cache, const pkv_cache_desc* desc,
+                                             const int32_t* block_tables,
+                                             int32_t max_blocks_per_seq,
+                                             const int32_t* query_start_loc,
+                                             const int32_t* context_lens, int32_t num_seqs,
+                                             int32_t num_query_tokens, int32_t max_query_len,
+                                             int32_t max_context_len, int32_t window, float scale,
+                                             void* workspace, size_t workspace_bytes,
+                                             void* stream) {
+    return varlen_impl(out, q, k_cache, v_cache, desc, block_tables, max_blocks_per_seq,
+                       query_start_loc, context_lens, num_seqs, num_query_tokens, max_query_len,
+                       max_context_len, window, scale, workspace, workspace_bytes, stream);
 }
 
 extern "C" int pkv_device_error(int32_t* code_out, int32_t clear) {

@@ -52,7 +52,8 @@ struct pkv_pool {
     int32_t block_size = 0;
     int32_t watermark = 0;
     bool caching = false;
-    int32_t ring = 0;                 // sliding window in blocks (0: off)
+    int32_t ring = 0;                 // ring of a sliding-window pool in blocks (0: off)
+    int32_t window = 0;               // the window in tokens (a multiple of block_size)
     std::vector<int32_t> free_stack;  // back() is handed out next
     std::vector<int32_t> refs;        // reference count per physical block
     struct Seq {
@@ -158,11 +159,11 @@ struct pkv_pool {
 
 extern "C" {
 
-int pkv_pool_create_ex(int32_t num_blocks, int32_t block_size, int32_t watermark_blocks,
+static int create_pool(int32_t num_blocks, int32_t block_size, int32_t watermark_blocks,
                        const int32_t* free_order, int32_t flags, int32_t sliding_window,
-                       pkv_pool** out) {
+                       int32_t max_chunk, pkv_pool** out) {
     if (!out || num_blocks < 1 || block_size < 1 || watermark_blocks < 0 || sliding_window < 0 ||
-        (flags & ~PKV_POOL_PREFIX_CACHING))
+        max_chunk < 1 || (flags & ~PKV_POOL_PREFIX_CACHING))
         return PKV_ERR_INVALID;
     *out = nullptr;
     if ((flags & PKV_POOL_PREFIX_CACHING) && sliding_window > 0) return PKV_ERR_UNSUPPORTED;
@@ -173,7 +174,12 @@ int pkv_pool_create_ex(int32_t num_blocks, int32_t block_size, int32_t watermark
     p->block_size = block_size;
     p->watermark = watermark_blocks;
     p->caching = (flags & PKV_POOL_PREFIX_CACHING) != 0;
-    p->ring = sliding_window / block_size;
+    p->window = sliding_window;
+    // the window's blocks, plus room for the keys a chunk of max_chunk queries
+    // needs beyond the window of its first query
+    p->ring = sliding_window > 0
+                  ? sliding_window / block_size + (max_chunk - 1 + block_size - 1) / block_size
+                  : 0;
     p->refs.assign(num_blocks, 0);
     if (p->caching) p->info.assign(num_blocks, pkv_pool::BlockInfo());
     p->free_stack.resize(num_blocks);
@@ -197,9 +203,24 @@ int pkv_pool_create_ex(int32_t num_blocks, int32_t block_size, int32_t watermark
     PKV_GUARD_END
 }
 
+int pkv_pool_create_ex(int32_t num_blocks, int32_t block_size, int32_t watermark_blocks,
+                       const int32_t* free_order, int32_t flags, int32_t sliding_window,
+                       pkv_pool** out) {
+    return create_pool(num_blocks, block_size, watermark_blocks, free_order, flags,
+                       sliding_window, 1, out);
+}
+
+int pkv_pool_create_window(int32_t num_blocks, int32_t block_size, int32_t watermark_blocks,
+                           const int32_t* free_order, int32_t sliding_window, int32_t max_chunk,
+                           pkv_pool** out) {
+    if (sliding_window < 1) return PKV_ERR_INVALID;
+    return create_pool(num_blocks, block_size, watermark_blocks, free_order, 0, sliding_window,
+                       max_chunk, out);
+}
+
 int pkv_pool_create(int32_t num_blocks, int32_t block_size, int32_t watermark_blocks,
                     const int32_t* free_order, pkv_pool** out) {
-    return pkv_pool_create_ex(num_blocks, block_size, watermark_blocks, free_order, 0, 0, out);
+    return create_pool(num_blocks, block_size, watermark_blocks, free_order, 0, 0, 1, out);
 }
 
 int pkv_pool_destroy(pkv_pool* pool) {
@@ -268,9 +289,10 @@ static int add_sequence(pkv_pool* pool, int64_t seq_id, const int32_t* token_ids
         s.table.push_back(b);
     }
     if (slots_out) {
-        const int64_t window = int64_t(pool->ring) * bs;
+        // a token whose ring slot a later token of the same prompt takes is skipped
+        const int64_t capacity = int64_t(pool->ring) * bs;
         for (int64_t p = 0; p < num_tokens; ++p)
-            slots_out[p] = (window && p + window < num_tokens) ? -1 : pool->slot(s, p);
+            slots_out[p] = (capacity && p + capacity < num_tokens) ? -1 : pool->slot(s, p);
     }
     if (num_cached_out) *num_cached_out = int32_t(leading * bs);
     entry = std::move(s);
@@ -414,6 +436,9 @@ int pkv_block_tables(const pkv_pool* pool, const int64_t* seq_ids, int32_t n, in
                      int32_t* tables_out, int32_t* ctx_lens_out) {
     if (!pool || n < 0 || max_blocks < 1 || (n > 0 && (!seq_ids || !tables_out)))
         return PKV_ERR_INVALID;
+    // the rotated export holds exactly the last `window` tokens only on a ring of
+    // exactly the window's blocks
+    if (pool->ring && pool->ring != pool->window / pool->block_size) return PKV_ERR_UNSUPPORTED;
     for (int32_t i = 0; i < n; ++i) {
         auto it = pool->seqs.find(seq_ids[i]);
         if (it == pool->seqs.end()) return PKV_ERR_INVALID;
@@ -435,6 +460,34 @@ int pkv_block_tables(const pkv_pool* pool, const int64_t* seq_ids, int32_t n, in
             std::copy(s.table.begin(), s.table.end(), row);
             if (ctx_lens_out) ctx_lens_out[i] = int32_t(s.len);
         }
+    }
+    return PKV_OK;
+}
+
+int pkv_window_tables(const pkv_pool* pool, const int64_t* seq_ids, const int32_t* query_lens,
+                      int32_t n, int32_t max_blocks, int32_t* tables_out, int32_t* ctx_lens_out) {
+    if (!pool || n < 0 || max_blocks < 1 ||
+        (n > 0 && (!seq_ids || !query_lens || !tables_out || !ctx_lens_out)))
+        return PKV_ERR_INVALID;
+    if (!pool->ring) return PKV_ERR_UNSUPPORTED;
+    const int64_t bs = pool->block_size, capacity = int64_t(pool->ring) * bs;
+    // validate everything before writing anything
+    for (int32_t i = 0; i < n; ++i) {
+        auto it = pool->seqs.find(seq_ids[i]);
+        if (it == pool->seqs.end()) return PKV_ERR_INVALID;
+        const int64_t len = it->second.len, q = query_lens[i];
+        if (q < 1 || q > len || q + pool->window - 1 > capacity) return PKV_ERR_INVALID;
+        const int64_t first = std::max<int64_t>(0, len - q - pool->window + 1) / bs;
+        if (pool->blocks_for(len) - first > max_blocks) return PKV_ERR_INVALID;
+    }
+    for (int32_t i = 0; i < n; ++i) {
+        const pkv_pool::Seq& s = pool->seqs.find(seq_ids[i])->second;
+        const int64_t first = std::max<int64_t>(0, s.len - query_lens[i] - pool->window + 1) / bs;
+        const int64_t nb = pool->blocks_for(s.len);
+        int32_t* row = tables_out + int64_t(i) * max_blocks;
+        std::fill(row, row + max_blocks, -1);
+        for (int64_t j = first; j < nb; ++j) row[j - first] = s.table[j % pool->ring];
+        ctx_lens_out[i] = int32_t(s.len - first * bs);
     }
     return PKV_OK;
 }

@@ -23,6 +23,12 @@
 //    the context length, so results do not depend on the batch.
 //  * Persistent grid (a multiple of the SM count) over a work list that a
 //    one-CTA planner kernel builds on the device, so no host round trip.
+//  * Sliding window of W keys ("大模型部署.md" §2.1 block_sliding_window, with
+//    the reading that a query sees its W most recent keys): a decode row
+//    attends keys max(0, ctx - W) .. ctx - 1 of a logically ordered table; the
+//    planner starts its splits at the one holding the window's first key, a
+//    split skips the blocks below it and masks the keys below it in its block,
+//    and the merge starts at that split.
 #include <algorithm>
 #include <atomic>
 #include <cfloat>
@@ -49,6 +55,7 @@ struct PlanParams {
     int32_t table_stride;
     int32_t tokens_per_tile;          // prefill tile height in tokens
     int32_t num_sms;
+    int32_t window;                   // sliding window in keys (0: none)
     double kv_bytes_per_token;        // K + V bytes of one token, all KV heads
     double flops_per_pair;            // QK^T + PV flops of one (query, key) pair, all query heads
     Workspace ws;
@@ -81,7 +88,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
     __syncthreads();
     for (int base = 0; base < p.num_seqs; base += 1024) {
         const int s = base + tid;
-        int nd = 0, np = 0;
+        int nd = 0, np = 0, first_split = 0;
         if (s < p.num_seqs && layout_ok) {
             const int ctx = p.context_lens[s];
             int qlen = 1;
@@ -94,13 +101,24 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
                 } else if ((ctx + kBlockTokens - 1) / kBlockTokens > p.table_stride) {
                     flag_error(p.err, PKV_DEV_TABLE_TOO_NARROW);
                 } else if (qlen == 1) {
-                    nd = (ctx + kSplitTokens - 1) / kSplitTokens;
-                    my_tok += (unsigned long long)ctx;
+                    // the splits from the one holding the window's first key
+                    const int lo = window_first_key(ctx - 1, p.window);
+                    first_split = lo / kSplitTokens;
+                    nd = (ctx - 1) / kSplitTokens - first_split + 1;
+                    my_tok += (unsigned long long)(ctx - lo);
                 } else {
                     np = (qlen + p.tokens_per_tile - 1) / p.tokens_per_tile;
-                    // causal (query, key) pairs of the chunk
+                    // causal (query, key) pairs of the chunk; with a window W, row i
+                    // sees min(ctx - qlen + 1 + i, W) keys
                     const unsigned long long q = qlen, c = ctx;
-                    my_pairs += q * (c - q) + q * (q + 1) / 2;
+                    if (p.window > 0) {
+                        const long long c0 = ctx - qlen + 1;
+                        const long long n1 = max(0LL, min((long long)qlen, p.window - c0));
+                        my_pairs += (unsigned long long)(n1 * c0 + n1 * (n1 - 1) / 2 +
+                                                         (qlen - n1) * (long long)p.window);
+                    } else {
+                        my_pairs += q * (c - q) + q * (q + 1) / 2;
+                    }
                 }
             }
         }
@@ -137,7 +155,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
         __syncthreads();
         const int before_d = carry_d + (warp ? warp_d[warp - 1] : 0) + xd - nd;
         const int before_p = carry_p + (warp ? warp_p[warp - 1] : 0) + xp - np;
-        for (int k = 0; k < nd; ++k) p.ws.items[before_d + k] = make_int2(s, k);
+        for (int k = 0; k < nd; ++k) p.ws.items[before_d + k] = make_int2(s, first_split + k);
         for (int k = 0; k < np; ++k) {
             if (before_p + k < p.ws.max_prefill_items) p.ws.prefill_items[before_p + k] = make_int2(s, k);
         }
@@ -196,8 +214,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
         const int q0 = p.query_start_loc[it.x], qlen = p.query_start_loc[it.x + 1] - q0;
         const int t0 = it.y * p.tokens_per_tile;
         const int nt = min(p.tokens_per_tile, qlen - t0);
-        const int n_keys = p.context_lens[it.x] - qlen + t0 + nt;
-        const int tiles = (n_keys + kPrefillKeys - 1) / kPrefillKeys;
+        const int ctx = p.context_lens[it.x];
+        const int n_keys = ctx - qlen + t0 + nt;
+        const int key0 = window_first_key(ctx - qlen + t0, p.window) / kPrefillKeys * kPrefillKeys;
+        const int tiles = (n_keys - key0 + kPrefillKeys - 1) / kPrefillKeys;
         const int b = kSortBuckets - 1 - min(tiles, kSortBuckets - 1);   // descending
         s_item[i] = it;
         s_bucket[i] = b;
@@ -239,6 +259,7 @@ int launch_plan(const AttnArgs& a) {
     p.table_stride = a.table_stride;
     p.tokens_per_tile = kPrefillRows / (a.desc->num_q_heads / a.desc->num_kv_heads);
     p.num_sms = num_sms();
+    p.window = a.window;
     p.kv_bytes_per_token =
         2.0 * a.desc->num_kv_heads * a.desc->head_dim * double(elem_bytes(a.desc->dtype));
     p.flops_per_pair = 4.0 * a.desc->head_dim * a.desc->num_q_heads;
@@ -270,6 +291,7 @@ struct SplitParams {
     int32_t num_q_heads;
     int32_t max_splits;
     int32_t wait_plan;   // launched right behind the planner: wait for its work list
+    int32_t window;      // sliding window in keys (0: none)
     float scale_log2;
     int* err;
 };
@@ -344,9 +366,9 @@ __global__ void __launch_bounds__(SplitCfg<T, D, G>::kThreads)
             if (u < 0) break;
             const int2 item = p.items[u / Hkv];
             const int kvh = u % Hkv;
-            const int ctx = p.context_lens[item.x];
-            const int b0 = item.y * (kSplitTokens / kBlockTokens);
-            const int nb = min(kSplitTokens / kBlockTokens, (ctx + kBlockTokens - 1) / kBlockTokens - b0);
+            const SplitSpan sp = split_span(p.context_lens[item.x], item.y, p.window);
+            const int b0 = sp.begin;
+            const int nb = max(0, sp.end - b0);
             int my_blk = 0;
             if (lane < nb) my_blk = p.block_tables[size_t(item.x) * p.table_stride + b0 + lane];
             for (int j = 0; j < nb; ++j, ++it) {
@@ -396,9 +418,9 @@ __global__ void __launch_bounds__(SplitCfg<T, D, G>::kThreads)
         const int seq = item.x, split = item.y;
         const int kvh = u % Hkv;
         const int ctx = p.context_lens[seq];
-        const int nblk_seq = (ctx + kBlockTokens - 1) / kBlockTokens;
-        const int b0 = split * (kSplitTokens / kBlockTokens);
-        const int nb = min(kSplitTokens / kBlockTokens, nblk_seq - b0);
+        const SplitSpan sp = split_span(ctx, split, p.window);
+        const int b0 = sp.begin;
+        const int nb = max(0, sp.end - b0);
         const int qrow = p.query_start_loc ? p.query_start_loc[seq] : seq;
 
         float qr[G][DPL];
@@ -424,6 +446,8 @@ __global__ void __launch_bounds__(SplitCfg<T, D, G>::kThreads)
             const T* kt = reinterpret_cast<const T*>(ring + size_t(st) * C::kStageBytes);
             const T* vt = kt + kBlockTokens * D;
             const int nvalid = min(kBlockTokens, ctx - (b0 + jb) * kBlockTokens);
+            // keys below the window's first key (its block only) are masked
+            const int fvalid = b0 + jb == sp.lo / kBlockTokens ? sp.lo % kBlockTokens : 0;
 
             // scores s = q . k for this lane's (head, token) in each chunk
             float s[NC];
@@ -443,7 +467,7 @@ __global__ void __launch_bounds__(SplitCfg<T, D, G>::kThreads)
                     }
                 }
                 s[c] = reduce_scatter<NV>(part, lane);
-                if (c * TC + my_tok >= nvalid) s[c] = -INFINITY;
+                if (c * TC + my_tok >= nvalid || c * TC + my_tok < fvalid) s[c] = -INFINITY;
             }
             // online softmax update over this block (column block of 16 keys)
             float mx = s[0];
@@ -471,7 +495,7 @@ __global__ void __launch_bounds__(SplitCfg<T, D, G>::kThreads)
 #pragma unroll
                 for (int d = 0; d < DPL; ++d) o[j][d] *= a;
             }
-            for (int t = 0; t < nvalid; ++t) {
+            for (int t = fvalid; t < nvalid; ++t) {
                 float vf[DPL];
                 Elem<T>::template load<DPL>(vt + t * D + lane * DPL, vf);
 #pragma unroll
@@ -497,7 +521,7 @@ __global__ void __launch_bounds__(SplitCfg<T, D, G>::kThreads)
             rec[G * D + G + my_head] = l;
         }
         consumer_sync(C::kWarps * 32);
-        const int nsplit = (ctx + kSplitTokens - 1) / kSplitTokens;
+        const int nsplit = sp.nsplit;
         for (int idx = threadIdx.x; idx < G * D; idx += C::kWarps * 32) {
             const int j = idx / D, d = idx % D;
             float M = -INFINITY;
@@ -549,6 +573,7 @@ struct MergeParams {
     int32_t num_q_heads;
     int32_t max_splits;
     int32_t max_context_len;
+    int32_t window;
 };
 
 template <typename T, int D>
@@ -568,10 +593,12 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(MergeParams p) {
     }
     const int ctx = p.context_lens[seq];
     if (ctx < 1 || ctx > p.max_context_len) return;          // flagged by the planner
-    const int n = (ctx + kSplitTokens - 1) / kSplitTokens;
+    // splits first .. first + n - 1 (first > 0 when a window starts past split 0)
+    const int first = window_first_key(ctx - 1, p.window) / kSplitTokens;
+    const int n = (ctx - 1) / kSplitTokens - first + 1;
     if (n <= 1) return;                                     // written by the split kernel
-    // slot of split k: base + k
-    const size_t base = (size_t(seq) * Hq + h) * p.max_splits;
+    // slot of split first + k: base + k
+    const size_t base = (size_t(seq) * Hq + h) * p.max_splits + first;
     float M = -INFINITY;
     for (int k = lane; k < n; k += 32) M = fmaxf(M, p.part_ml[base + k].x);
 #pragma unroll
@@ -668,6 +695,7 @@ int launch_split_t(const AttnArgs& a) {
     p.num_q_heads = a.desc->num_q_heads;
     p.max_splits = a.ws.max_splits;
     p.wait_plan = a.pdl ? 0 : 1;   // behind a prefill kernel, the plan is complete
+    p.window = a.window;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.err = a.err;
     cudaLaunchConfig_t cfg = {};
@@ -706,6 +734,7 @@ int launch_merge_d(const AttnArgs& a) {
     p.num_q_heads = a.desc->num_q_heads;
     p.max_splits = a.ws.max_splits;
     p.max_context_len = a.max_context_len;
+    p.window = a.window;
     const int64_t warps = int64_t(a.num_seqs) * a.desc->num_q_heads;   // one per (seq, head)
     const int64_t blocks = (warps + 3) / 4;
     if (blocks < 1) return PKV_OK;

@@ -48,6 +48,7 @@ struct MmaParams {
     int32_t num_q_heads;
     int32_t max_splits;
     int32_t wait_plan;   // launched right behind the planner: wait for its work list
+    int32_t window;      // sliding window in keys (0: none)
     float scale_log2;
     int* err;
 };
@@ -162,7 +163,6 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads, MmaCfg<D, G>::kMinBloc
 
     const int Hkv = p.num_kv_heads, Hq = p.num_q_heads;
     const int n_units = p.n_items[0] * Hkv;
-    constexpr int kSplitBlocks = kSplitTokens / kBlockTokens;
 
     if (warp == C::kWarps) {
         // ---------------- producer ----------------
@@ -175,8 +175,9 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads, MmaCfg<D, G>::kMinBloc
             const int2 item = p.items[u / Hkv];
             const int kvh = u % Hkv;
             const int ctx = p.context_lens[item.x];
-            const int b0 = item.y * kSplitBlocks;
-            const int nb = min(kSplitBlocks, (ctx + kBlockTokens - 1) / kBlockTokens - b0);
+            const SplitSpan sp = split_span(ctx, item.y, p.window);
+            const int b0 = sp.begin;
+            const int nb = max(0, sp.end - b0);
             int my_blk = 0;
             if (lane < nb) my_blk = p.block_tables[size_t(item.x) * p.table_stride + b0 + lane];
             // the unit's description and q, so the consumers start without global loads
@@ -237,8 +238,9 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads, MmaCfg<D, G>::kMinBloc
         const int4 mt = meta[2 * qs];
         const int seq = mt.x, split = mt.y, ctx = mt.z, kvh = mt.w;
         const int qrow = meta[2 * qs + 1].x;
-        const int b0 = split * kSplitBlocks;
-        const int nb = ok ? min(kSplitBlocks, (ctx + kBlockTokens - 1) / kBlockTokens - b0) : 0;
+        const SplitSpan sp = split_span(ctx, split, p.window);
+        const int b0 = sp.begin;
+        const int nb = ok ? max(0, sp.end - b0) : 0;
 
         // q fragments (A operand): row gid = query head gid of the group, rows >= G zero
         uint32_t qa0[D / 16], qa2[D / 16];
@@ -266,6 +268,8 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads, MmaCfg<D, G>::kMinBloc
             const uint32_t kt = base + st * C::kStageBytes;
             const uint32_t vt = kt + C::kTileBytes;
             const int nvalid = min(kBlockTokens, ctx - (b0 + jb) * kBlockTokens);
+            // keys below the window's first key (its block only) are masked
+            const int fvalid = b0 + jb == sp.lo / kBlockTokens ? sp.lo % kBlockTokens : 0;
 
             // ---- S = q K^T: two 8-key column tiles ----
             float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -286,7 +290,7 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads, MmaCfg<D, G>::kMinBloc
             float mx = -INFINITY;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                v[i] = key[i] < nvalid ? v[i] * p.scale_log2 : -INFINITY;
+                v[i] = key[i] < nvalid && key[i] >= fvalid ? v[i] * p.scale_log2 : -INFINITY;
                 mx = fmaxf(mx, v[i]);
             }
             mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 1));
@@ -306,11 +310,13 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads, MmaCfg<D, G>::kMinBloc
             }
             m_row = m_new;
 
-            // zero V rows past the context (partial last block) before PV reads them
-            if (nvalid < kBlockTokens) {
-                const int nz = (kBlockTokens - nvalid) * (D / 8);
+            // zero V rows past the context (partial last block) and below the
+            // window's first key before PV reads them
+            if (nvalid < kBlockTokens || fvalid > 0) {
+                const int nz = (kBlockTokens - nvalid + fvalid) * (D / 8);
                 for (int i = lane; i < nz; i += 32) {
-                    const int t = nvalid + i / (D / 8), c = i % (D / 8);
+                    const int z = i / (D / 8), c = i % (D / 8);
+                    const int t = z < fvalid ? z : nvalid + (z - fvalid);
                     const uint32_t a = tile_addr(vt, t, c);
                     asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0)
                                  : "memory");
@@ -331,7 +337,7 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads, MmaCfg<D, G>::kMinBloc
                     mma16816(o[2 * pr2 + 1], pa0, 0u, pa2, 0u, r2, r3);
                 }
             }
-            if (nvalid < kBlockTokens) fence_proxy_async_shared();
+            if (nvalid < kBlockTokens || fvalid > 0) fence_proxy_async_shared();
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
         }
@@ -354,7 +360,7 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads, MmaCfg<D, G>::kMinBloc
             }
         }
         asm volatile("bar.sync 1, %0;" ::"r"(C::kWarps * 32) : "memory");
-        const int nsplit = (ctx + kSplitTokens - 1) / kSplitTokens;
+        const int nsplit = sp.nsplit;
         // (a failed wait leaves the unit's description unknown: write nothing)
         for (int idx = threadIdx.x; ok && idx < G * D; idx += C::kWarps * 32) {
             const int j = idx / D, d = idx % D;
@@ -415,6 +421,7 @@ int launch_t(const AttnArgs& a) {
     p.num_q_heads = a.desc->num_q_heads;
     p.max_splits = a.ws.max_splits;
     p.wait_plan = a.pdl ? 0 : 1;   // behind a prefill kernel, the plan is complete
+    p.window = a.window;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.err = a.err;
     cudaLaunchConfig_t cfg = {};

@@ -6,6 +6,7 @@
 #include <cstdint>
 
 #include "pagedkv.h"
+#include "pkv_internal.h"
 
 namespace pkv {
 
@@ -17,6 +18,31 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: a pipeline wait this l
 // context stays usable and the host reads the code with pkv_device_error.
 __device__ __forceinline__ void flag_error(int* err, int code) {
     if (err) atomicCAS(err, 0, code);
+}
+
+// First key (table index) that a query whose last visible key is `last`
+// attends under a sliding window of `window` keys (0: no window): the query
+// sees keys max(0, last - window + 1) .. last.
+__device__ __forceinline__ int window_first_key(int last, int window) {
+    return window > 0 ? max(0, last - window + 1) : 0;
+}
+
+// The part of decode split `split` (kSplitTokens keys from split * kSplitTokens)
+// that a decode query over `ctx` keys attends under a sliding window: blocks
+// [begin, end) of its table, the first attended key `lo` (masked below within
+// block lo / kBlockTokens), and how many splits the query's keys span (the
+// planner's items start at split lo / kSplitTokens).
+struct SplitSpan {
+    int begin, end, lo, nsplit;
+};
+__device__ __forceinline__ SplitSpan split_span(int ctx, int split, int window) {
+    constexpr int per = kSplitTokens / kBlockTokens;
+    SplitSpan r;
+    r.lo = window_first_key(ctx - 1, window);
+    r.begin = max(split * per, r.lo / kBlockTokens);
+    r.end = min((split + 1) * per, (ctx + kBlockTokens - 1) / kBlockTokens);
+    r.nsplit = (ctx - 1) / kSplitTokens - r.lo / kSplitTokens + 1;
+    return r;
 }
 
 __device__ __forceinline__ uint64_t global_ns() {

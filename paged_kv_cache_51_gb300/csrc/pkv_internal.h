@@ -62,6 +62,7 @@ struct AttnArgs {
     cudaStream_t stream;
     int* err;
     bool pdl;            // decode kernels may start while the preceding prefill kernel runs
+    int32_t window;      // sliding window in keys (0: none); tables in logical order
 };
 
 // Planning rates for the split of SMs between prefill chunks and decode rows

@@ -7,6 +7,14 @@
 // accumulated tile by tile with the online recurrence of §15.1 算法详解
 // (running max m, running sum l, O rescaled by alpha), in base 2.
 //
+// With a sliding window of W keys ("大模型部署.md" §2.1 block_sliding_window;
+// the reading taken: a query sees its W most recent keys), query i sees keys
+// max(0, a - W + 1) .. a, a = ctx - qlen + i, over a logically ordered table:
+// a unit's key tiles start at the tile holding its first token's first key,
+// each row masks the keys below its own window, and V rows below the first
+// token's window in that tile are zeroed before P V (they belong to other
+// tokens of the ring, or were never written).
+//
 // Both products are dense contractions, so they run on the 5th-generation
 // tensor cores:
 //   S = Q K^T   M = 128 query rows, N = 128 keys, K = 128 dims
@@ -271,13 +279,18 @@ struct PrefillParams {
     int32_t num_q_heads;
     int32_t group;
     int32_t tokens_per_tile;
+    int32_t window;            // sliding window in keys (0: none); tables in logical order
     float scale_log2;
     int* err;
 };
 
-// Per-unit geometry shared by all roles.
+// Per-unit geometry shared by all roles.  Key tiles start at table index
+// kbase (0 without a window; with one, the 128-key tile holding the first key
+// of the unit's first token), so tile j holds keys kbase + 128 j ..; n_keys,
+// n_tiles and nblk count from kbase, and lo0 is the first token's first key
+// relative to kbase.
 struct Unit {
-    int seq, kvh, q0, qlen, ctx, t0, nt, n_keys, n_tiles, nblk;
+    int seq, kvh, q0, qlen, ctx, t0, nt, n_keys, n_tiles, nblk, kbase, lo0;
 };
 
 __device__ __forceinline__ Unit unit_of(const PrefillParams& p, int u) {
@@ -290,7 +303,10 @@ __device__ __forceinline__ Unit unit_of(const PrefillParams& p, int u) {
     x.ctx = p.context_lens[x.seq];
     x.t0 = item.y * p.tokens_per_tile;
     x.nt = min(p.tokens_per_tile, x.qlen - x.t0);
-    x.n_keys = x.ctx - x.qlen + x.t0 + x.nt;  // keys visible to the tile's last token
+    const int lo = window_first_key(x.ctx - x.qlen + x.t0, p.window);
+    x.kbase = lo / kKeys * kKeys;
+    x.lo0 = lo - x.kbase;
+    x.n_keys = x.ctx - x.qlen + x.t0 + x.nt - x.kbase;  // up to the tile's last token's key
     x.n_tiles = (x.n_keys + kKeys - 1) / kKeys;
     x.nblk = (x.n_keys + kBlockTokens - 1) / kBlockTokens;
     return x;
@@ -536,7 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             BlockIds ids;
-            ids.start(p.block_tables + size_t(x.seq) * p.table_stride, x.nblk, lane);
+            ids.start(p.block_tables + size_t(x.seq) * p.table_stride + x.kbase / kBlockTokens,
+                      x.nblk, lane);
             for (int j = 0; j < x.n_tiles && ok; ++j, ++kt) {
                 const int st = kt % kKStages;
                 const int nb = min(kBlkPerTile, x.nblk - j * kBlkPerTile);
@@ -591,7 +608,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&bars[B_U_EMPTY + k % kUnitSlots]);
             if (u < 0 || !ok) break;
             BlockIds ids;
-            ids.start(p.block_tables + size_t(x.seq) * p.table_stride, x.nblk, lane);
+            ids.start(p.block_tables + size_t(x.seq) * p.table_stride + x.kbase / kBlockTokens,
+                      x.nblk, lane);
             for (int j = 0; j < x.n_tiles && ok; ++j, ++kt) {
                 const int st = kt % kVStages;
                 const int nb = min(kBlkPerTile, x.nblk - j * kBlkPerTile);
@@ -759,7 +777,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tok = r / G, g_head = r % G;
             const bool row_valid = tok < x.nt;
             const int t = x.t0 + tok;
-            const int limit = row_valid ? x.ctx - x.qlen + t : x.ctx - 1;  // last visible key
+            // this row's visible keys, as indices from the unit's first key tile:
+            // lower .. limit (the window's first key .. the row's own position)
+            const int last = row_valid ? x.ctx - x.qlen + t : x.ctx - 1;
+            const int limit = last - x.kbase;
+            const int lower = row_valid ? window_first_key(last, p.window) - x.kbase : x.lo0;
 
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < x.n_tiles; ++j) {
@@ -784,11 +806,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
 
-                // mask keys beyond this row's causal limit; max on the raw scores
+                // mask keys beyond this row's causal limit and below its window;
+                // max on the raw scores
                 const int key0 = j * kKeys + h * 64;
-                if (key0 + 63 > limit) {
+                if (key0 + 63 > limit || key0 < lower) {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) s[c] = (key0 + c <= limit) ? s[c] : -INFINITY;
+                    for (int c = 0; c < 64; ++c)
+                        s[c] = (key0 + c <= limit && key0 + c >= lower) ? s[c] : -INFINITY;
                 }
                 // eight independent partial maxima instead of one 64-long chain
                 // (three-input maxima: half the instructions of a two-input tree)
@@ -855,25 +879,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // rows of the last staged block that lie beyond the context were
                 // never written: zero their V so 0 * (anything) cannot become NaN.
                 // The half whose keys hold that block does it before its P V.
-                const int rows_last = x.ctx - (x.nblk - 1) * kBlockTokens;  // valid rows, 1..16+
+                const int rows_last = x.ctx - x.kbase - (x.nblk - 1) * kBlockTokens;  // 1..16+
                 const int slot = (x.nblk - 1) - j * kBlkPerTile;
                 const bool zero_v = j == x.n_tiles - 1 && rows_last < kBlockTokens && (slot >> 2) == h;
-                if (zero_v) {
+                // in the unit's first tile, the rows below its first token's window
+                // hold other tokens of the ring (or were never written): zero their V
+                // too; this half's keys h * 64 .. h * 64 + z_lo - 1
+                const int z_lo = j == 0 ? max(0, min(x.lo0, h * 64 + 64) - h * 64) : 0;
+                if (zero_v || z_lo > 0) {
                     // the V tile must have landed before its rows are overwritten (its
                     // stage cannot be refilled before this tile's P V has been issued)
                     ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_V_FULL + g % kVStages],
                                                            (g / kVStages) & 1, p.err));
                     if (!ok) break;
-                    const int nz = (kBlockTokens - rows_last) * 2 * 8;  // rows x halves x chunks
                     unsigned char* vs = smem + kVOff + (g % kVStages) * kKBytes;
+                    const int nz = zero_v ? (kBlockTokens - rows_last) * 2 * 8 : 0;  // rows x halves x chunks
                     for (int i = r; i < nz; i += kRows) {
                         const int row = rows_last + i / 16, half = (i / 8) & 1, c = i & 7;
                         *reinterpret_cast<uint4*>(vs + half * (kKeys * 128) +
                                                   (slot * kBlockTokens + row) * 128 + c * 16) =
                             make_uint4(0, 0, 0, 0);
                     }
+                    for (int i = r; i < z_lo * 16; i += kRows) {
+                        const int key = h * 64 + i / 16, half = (i / 8) & 1, c = i & 7;
+                        *reinterpret_cast<uint4*>(vs + half * (kKeys * 128) + key * 128 + c * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_async_smem();   // the zeroed V rows, before the P V reads them
                 }
-                if (zero_v) fence_async_smem();   // the zeroed V rows, before the P V reads them
                 tmem_wait_st();
                 tc_before();
                 __syncwarp();
@@ -1000,6 +1033,7 @@ int launch_prefill(const AttnArgs& a) {
     p.num_q_heads = d->num_q_heads;
     p.group = group;
     p.tokens_per_tile = kPrefillRows / p.group;
+    p.window = a.window;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.err = a.err;
     if (kernel_occupancy<prefill_kernel>(kThreads, kSmemBytes) < 1) return PKV_ERR_CUDA;

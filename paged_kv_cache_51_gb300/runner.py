@@ -212,3 +212,52 @@ def prepare(w, device="cuda"):
     dc.run_setup()
     step = Step(dc, dc.plan_step())
     return dc, step
+
+
+def run_window_trace(tr, device="cuda"):
+    """Run a sliding-window trace (``workloads.WindowTrace``) through the library:
+    the C++ window pool with room for ``max_chunk`` queries, copy-on-write and
+    append of each step's tokens, then one windowed varlen call over the step's
+    prompt chunks and decode rows with the pool's logically ordered tables.
+    Returns (list of per-step outputs on the device, K cache, V cache)."""
+    dev = torch.device(device)
+    tdt = torch.float32 if tr.dtype == "f32" else torch.bfloat16
+    shape = (tr.num_blocks, tr.num_kv_heads, tr.block_size, tr.head_dim)
+    kc = torch.zeros(shape, dtype=tdt, device=dev)
+    vc = torch.zeros_like(kc)
+    desc = cache_desc(kc, tr.num_q_heads)
+    pool = BlockPool(tr.num_blocks, tr.block_size, 0, tr.free_order,
+                     sliding_window=tr.window, max_chunk=tr.max_chunk)
+    lens, outs = {}, []
+    for i, step in enumerate(tr.steps):
+        slots, rows, pairs = [], [], []
+        for seq, qlen in step:
+            n = lens.get(seq, 0)
+            if n == 0:
+                slots += pool.add(seq, qlen)
+            else:
+                for _ in range(qlen):
+                    slot, cow = pool.append_slot(seq)
+                    if cow is not None:
+                        pairs.append(cow)
+                    slots.append(slot)
+            rows += range(tr.row_offset[seq] + n, tr.row_offset[seq] + n + qlen)
+            lens[seq] = n + qlen
+        if pairs:
+            pkv_copy_blocks(torch.tensor(pairs, dtype=torch.int32).to(dev), kc, vc, desc)
+        r = np.asarray(rows)
+        paged_kv_append(_torch_rows(tr.k_rows[r], tr.dtype).to(dev),
+                        _torch_rows(tr.v_rows[r], tr.dtype).to(dev),
+                        torch.tensor(slots, dtype=torch.int64).to(dev), kc, vc, desc)
+        seqs = [seq for seq, _ in step]
+        qlens = [q for _, q in step]
+        width = max(math.ceil(lens[s] / tr.block_size) for s in seqs) + 1
+        tables, ctx = pool.window_tables(seqs, qlens, width)
+        qsl = torch.zeros(len(step) + 1, dtype=torch.int32)
+        qsl[1:] = torch.cumsum(torch.tensor(qlens, dtype=torch.int32), 0)
+        q = _torch_rows(tr.q_rows[tr.q_offset[i]:tr.q_offset[i + 1]], tr.dtype).to(dev)
+        out = torch.empty_like(q)
+        paged_attention_varlen(out, q, kc, vc, desc, tables.to(dev), qsl.to(dev), ctx.to(dev),
+                               max(qlens), int(ctx.max()), window=tr.window)
+        outs.append(out)
+    return outs, kc, vc
