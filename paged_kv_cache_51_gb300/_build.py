@@ -54,6 +54,25 @@ def _stamp(srcs, hdrs):
     return h.hexdigest()
 
 
+def build_variant(tag, defines, verbose=False):
+    """A separate copy of the library compiled with extra -D definitions, for
+    tests that need a behaviour the product build must not have (the
+    wait-timeout test: a 1 ms wait limit and one decode tile never copied).
+    It lands beside the product library as libpagedkv_<tag>.so, from its own
+    object directory, and is rebuilt only when sources or definitions change."""
+    import fcntl
+
+    lib = os.path.join(HERE, f"libpagedkv_{tag}.so")
+    flags = [f"-D{k}={v}" for k, v in sorted(defines.items())]
+    with open(lib + ".lock", "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            return _build_locked(False, verbose, lib=lib, build_dir=os.path.join(BUILD, tag),
+                                 extra=flags)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
 def build(force=False, verbose=False):
     """Compile and link the library; return its path.  Raises on compiler errors.
 
@@ -71,24 +90,25 @@ def build(force=False, verbose=False):
             fcntl.flock(lock, fcntl.LOCK_UN)
 
 
-def _build_locked(force, verbose):
+def _build_locked(force, verbose, lib=LIB, build_dir=BUILD, extra=()):
     srcs, hdrs = _sources()
-    stamp = _stamp(srcs, hdrs)
-    stamp_file = LIB + ".stamp"
-    if not force and os.path.exists(LIB) and os.path.exists(stamp_file):
+    stamp = _stamp(srcs, hdrs) + ("" if not extra else " " + " ".join(extra))
+    stamp_file = lib + ".stamp"
+    if not force and os.path.exists(lib) and os.path.exists(stamp_file):
         with open(stamp_file) as f:
             if f.read().strip() == stamp:
-                return LIB
-    os.makedirs(BUILD, exist_ok=True)
+                return lib
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src + ".o")
+        obj = os.path.join(build_dir, src + ".o")
         path = os.path.join(CSRC, src)
         if src.endswith(".cu"):
-            cmd = [nvcc] + NVCC_FLAGS + EXTRA_FLAGS.get(src, []) + ["-c", path, "-o", obj]
+            cmd = ([nvcc] + NVCC_FLAGS + EXTRA_FLAGS.get(src, []) + list(extra)
+                   + ["-c", path, "-o", obj])
         else:
-            cmd = ["g++"] + CXX_FLAGS + ["-c", path, "-o", obj]
+            cmd = ["g++"] + CXX_FLAGS + list(extra) + ["-c", path, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"compile failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
@@ -98,15 +118,15 @@ def _build_locked(force, verbose):
 
     with ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp_file, "w") as f:
         f.write(stamp)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

@@ -11,7 +11,12 @@
 namespace pkv {
 
 constexpr int kBlockTokens = 16;          // tokens per cache block the kernels implement
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: a pipeline wait this long is a fault
+// 2 s: a pipeline wait this long is a fault.  The wait-timeout test builds a
+// separate copy of the library with a 1 ms limit (PKV_WAIT_LIMIT_NS).
+#ifndef PKV_WAIT_LIMIT_NS
+#define PKV_WAIT_LIMIT_NS 2000000000ull
+#endif
+constexpr uint64_t kWaitLimitNs = PKV_WAIT_LIMIT_NS;
 
 // ---- device error word ------------------------------------------------------
 // First fault wins; kernels skip the offending access and carry on, so the
