@@ -302,9 +302,12 @@ def job_throughput(bytes_per_rank, world, ms):
 
 def time_steps(step, steps, warmup):
     """Device time of `steps` steps (one event pair around the whole loop), then
-    the mean time of the attention call alone, from a second loop of the same
-    steps with an event pair around each call (the events inside a step cost
-    about 2 us of it, so they stay out of the first loop)."""
+    the mean time of the attention call alone: the same number of attention
+    calls back to back between one event pair.  (The step's tokens are already
+    in the cache, so the calls repeat the step's attention exactly; every input
+    is larger than L2, so a call gains nothing from the one before.  An event
+    pair around each call would break the calls' launch chain and cost a few
+    microseconds of each.)"""
     import torch
 
     stream = torch.cuda.current_stream()
@@ -318,15 +321,13 @@ def time_steps(step, steps, warmup):
         step.run()
     ev1.record(stream)
     torch.cuda.synchronize()
-    a_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(steps)]
-    for i in range(steps):
-        step.write_kv()
-        a_ev[i][0].record(stream)
+    step_ms = ev0.elapsed_time(ev1) / steps
+    ev0.record(stream)
+    for _ in range(steps):
         step.attend()
-        a_ev[i][1].record(stream)
+    ev1.record(stream)
     torch.cuda.synchronize()
-    return ev0.elapsed_time(ev1) / steps, statistics.mean(a.elapsed_time(b) for a, b in a_ev)
+    return step_ms, ev0.elapsed_time(ev1) / steps
 
 
 def peaks():
@@ -588,16 +589,15 @@ def int8_decode_summary(w, dc, step, steps, warmup, bf16_attn_ms, full_size):
     for _ in range(warmup):
         call()
     torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
-    for a, b in evs:
-        a.record(stream)
-        call()
-        b.record(stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        call()                      # back to back, as the bf16 call is timed
+    e1.record(stream)
     torch.cuda.synchronize()
     if pkv.device_error() != 0:
         raise SystemExit("device error in the int8 decode")
-    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    ms = e0.elapsed_time(e1) / steps
     # the step's own tokens through the quantising append
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a0.record(stream)

@@ -15,6 +15,7 @@
 
 #include <algorithm>
 
+#include "launch_cache.h"
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -44,6 +45,10 @@ constexpr int kAppendUnroll = 4;
 
 template <typename Idx>
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
+    // launched programmatically behind the previous kernel: wait for it to
+    // complete before touching the inputs or the cache; let the next launch
+    pdl_wait_prerequisites();
+    pdl_launch_dependents();
     const Idx per_tok = Idx(p.num_kv_heads) * Idx(p.vec_per_row);
     const Idx total = Idx(p.num_tokens) * per_tok;
     const Idx vec = Idx(p.vec_per_row);
@@ -94,6 +99,8 @@ struct CopyParams {
 
 // blockIdx.y = pair; blockIdx.x strides over the block's vectors
 __global__ void __launch_bounds__(256) copy_blocks_kernel(CopyParams p) {
+    pdl_wait_prerequisites();   // as append_kernel
+    pdl_launch_dependents();
     const int pair = blockIdx.y;
     const int src = __ldg(p.pairs + 2 * pair), dst = __ldg(p.pairs + 2 * pair + 1);
     if (src < 0 || src >= p.num_blocks || dst < 0 || dst >= p.num_blocks) {
@@ -383,13 +390,13 @@ extern "C" int paged_kv_append(const void* k, const void* v, const int64_t* slot
     if (total < (int64_t(1) << 31)) {
         static const int per_sm = resident_blocks_per_sm(append_kernel<uint32_t>);
         const int64_t blocks = std::min<int64_t>(want, sms * per_sm);
-        append_kernel<uint32_t><<<unsigned(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
-    } else {
-        static const int per_sm = resident_blocks_per_sm(append_kernel<int64_t>);
-        const int64_t blocks = std::min<int64_t>(want, sms * per_sm);
-        append_kernel<int64_t><<<unsigned(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
+        return cuda_status(launch_pdl(append_kernel<uint32_t>, dim3(unsigned(blocks)), dim3(256), 0,
+                                      static_cast<cudaStream_t>(stream), p));
     }
-    return cuda_status(cudaGetLastError());
+    static const int per_sm = resident_blocks_per_sm(append_kernel<int64_t>);
+    const int64_t blocks = std::min<int64_t>(want, sms * per_sm);
+    return cuda_status(launch_pdl(append_kernel<int64_t>, dim3(unsigned(blocks)), dim3(256), 0,
+                                  static_cast<cudaStream_t>(stream), p));
 }
 
 extern "C" int pkv_copy_blocks(const int32_t* block_pairs, int32_t num_pairs, void* k_cache,
@@ -415,8 +422,8 @@ extern "C" int pkv_copy_blocks(const int32_t* block_pairs, int32_t num_pairs, vo
     p.num_blocks = desc->num_blocks;
     p.err = err;
     const unsigned gx = unsigned(std::min<int64_t>((p.vec_per_block + 255) / 256, 64));
-    copy_blocks_kernel<<<dim3(gx, unsigned(num_pairs)), 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
-    return cuda_status(cudaGetLastError());
+    return cuda_status(launch_pdl(copy_blocks_kernel, dim3(gx, unsigned(num_pairs)), dim3(256), 0,
+                                  static_cast<cudaStream_t>(stream), p));
 }
 
 extern "C" int pkv_copy_blocks_int8(const int32_t* block_pairs, int32_t num_pairs, void* k_pool,

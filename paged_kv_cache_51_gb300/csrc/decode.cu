@@ -67,31 +67,41 @@ constexpr int kSortBuckets = 256;   // key-tile counts (larger counts share the 
 
 __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
     __shared__ int warp_d[32], warp_p[32];
-    __shared__ int carry_d, carry_p, layout_ok;
+    __shared__ int carry_d, carry_p;
     __shared__ unsigned long long warp_tok[32], warp_pairs[32];
+    // prefill items and their sort buckets, recorded during the pass (when they
+    // fit) so the longest-first reorder needs no second round of global loads
+    __shared__ int2 s_item[kSortItems];
+    __shared__ int s_bucket[kSortItems];
+    __shared__ int hist[kSortBuckets], cursor[kSortBuckets];
     unsigned long long my_tok = 0, my_pairs = 0;   // this thread's work estimate
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // the kernels that consume the plan may launch now; each waits for this
-    // grid to complete before it reads the plan
+    const int sortable = min(kSortItems, p.ws.max_prefill_items);
+    // launched programmatically behind the previous kernel (the step's append,
+    // or the previous call's merge): the lengths and the workspace are read and
+    // written only after it completes.  The kernels that consume the plan may
+    // launch now; each waits for this grid to complete before it reads the plan.
+    pdl_wait_prerequisites();
     pdl_launch_dependents();
+    // the two ends of the query layout, loaded now and checked after the pass
+    // (a bad layout empties the plan), so their latency overlaps the pass
+    int q_first = 0, q_last = 0;
+    if (tid == 0 && p.query_start_loc) {
+        q_first = p.query_start_loc[0];
+        q_last = p.query_start_loc[p.num_seqs];
+    }
     if (tid == 0) {
         carry_d = 0;
         carry_p = 0;
-        layout_ok = 1;
-        if (p.query_start_loc) {
-            if (p.query_start_loc[0] != 0 || p.query_start_loc[p.num_seqs] != p.num_query_tokens) {
-                layout_ok = 0;
-                flag_error(p.err, PKV_DEV_BAD_QUERY_LAYOUT);
-            }
-        }
     }
+    for (int i = tid; i < kSortBuckets; i += 1024) hist[i] = 0;
     __syncthreads();
     for (int base = 0; base < p.num_seqs; base += 1024) {
         const int s = base + tid;
-        int nd = 0, np = 0, first_split = 0;
-        if (s < p.num_seqs && layout_ok) {
-            const int ctx = p.context_lens[s];
-            int qlen = 1;
+        int nd = 0, np = 0, first_split = 0, ctx = 0, qlen = 0;
+        if (s < p.num_seqs) {
+            ctx = p.context_lens[s];
+            qlen = 1;
             if (p.query_start_loc) qlen = p.query_start_loc[s + 1] - p.query_start_loc[s];
             if (qlen < 0 || qlen > p.num_query_tokens) {
                 flag_error(p.err, PKV_DEV_BAD_QUERY_LAYOUT);
@@ -157,7 +167,22 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
         const int before_p = carry_p + (warp ? warp_p[warp - 1] : 0) + xp - np;
         for (int k = 0; k < nd; ++k) p.ws.items[before_d + k] = make_int2(s, first_split + k);
         for (int k = 0; k < np; ++k) {
-            if (before_p + k < p.ws.max_prefill_items) p.ws.prefill_items[before_p + k] = make_int2(s, k);
+            const int idx = before_p + k;
+            if (idx < p.ws.max_prefill_items) p.ws.prefill_items[idx] = make_int2(s, k);
+            if (idx < sortable) {
+                // key tiles of the item: from the tile of its first token's first
+                // key to its last token's key
+                const int t0 = k * p.tokens_per_tile;
+                const int nt = min(p.tokens_per_tile, qlen - t0);
+                const int n_keys = ctx - qlen + t0 + nt;
+                const int key0 =
+                    window_first_key(ctx - qlen + t0, p.window) / kPrefillKeys * kPrefillKeys;
+                const int tiles = (n_keys - key0 + kPrefillKeys - 1) / kPrefillKeys;
+                const int b = kSortBuckets - 1 - min(tiles, kSortBuckets - 1);   // descending
+                s_item[idx] = make_int2(s, k);
+                s_bucket[idx] = b;
+                atomicAdd(&hist[b], 1);
+            }
         }
         __syncthreads();
         if (tid == 0) {
@@ -178,6 +203,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
     }
     __syncthreads();
     if (tid == 0) {
+        if (p.query_start_loc && (q_first != 0 || q_last != p.num_query_tokens)) {
+            flag_error(p.err, PKV_DEV_BAD_QUERY_LAYOUT);
+            carry_d = 0;
+            carry_p = 0;
+        }
         unsigned long long dec_tokens = 0, pre_pairs = 0;
         for (int w = 0; w < 32; ++w) {
             dec_tokens += warp_tok[w];
@@ -188,7 +218,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
         // SMs for the prefill chunks: their share of the estimated time, so that
         // tensor-bound chunks and HBM-bound decode rows finish together
         int sms_prefill = 0;
-        if (pre_pairs) {
+        if (pre_pairs && carry_p) {
             const double t_pre = double(pre_pairs) * p.flops_per_pair / kPrefillFlopsPerNs;
             const double t_dec = double(dec_tokens) * p.kv_bytes_per_token / kDecodeBytesPerNs;
             sms_prefill = int(ceil(p.num_sms * t_pre / (t_pre + t_dec)));
@@ -199,31 +229,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
         p.ws.counters[4] = 0;  // prefill unit ticket
     }
     // Longest first: prefill units are taken from a ticket in item order, so the
-    // items are reordered by descending key-tile count (a counting sort; items
-    // with equal counts in any order).  Large lists keep their order.
+    // items are reordered by descending key-tile count (a counting sort of the
+    // items recorded in shared memory; items with equal counts in any order).
+    // Lists longer than the recorded ones keep their order.
     __syncthreads();
     const int n_pre = min(carry_p, p.ws.max_prefill_items);
-    if (n_pre < 2 || n_pre > kSortItems) return;
-    __shared__ int2 s_item[kSortItems];
-    __shared__ int s_bucket[kSortItems];
-    __shared__ int hist[kSortBuckets], cursor[kSortBuckets];
-    for (int i = tid; i < kSortBuckets; i += 1024) hist[i] = 0;
-    __syncthreads();
-    for (int i = tid; i < n_pre; i += 1024) {
-        const int2 it = p.ws.prefill_items[i];
-        const int q0 = p.query_start_loc[it.x], qlen = p.query_start_loc[it.x + 1] - q0;
-        const int t0 = it.y * p.tokens_per_tile;
-        const int nt = min(p.tokens_per_tile, qlen - t0);
-        const int ctx = p.context_lens[it.x];
-        const int n_keys = ctx - qlen + t0 + nt;
-        const int key0 = window_first_key(ctx - qlen + t0, p.window) / kPrefillKeys * kPrefillKeys;
-        const int tiles = (n_keys - key0 + kPrefillKeys - 1) / kPrefillKeys;
-        const int b = kSortBuckets - 1 - min(tiles, kSortBuckets - 1);   // descending
-        s_item[i] = it;
-        s_bucket[i] = b;
-        atomicAdd(&hist[b], 1);
-    }
-    __syncthreads();
+    if (n_pre < 2 || n_pre > sortable) return;
     if (warp == 0) {
         // exclusive scan of the histogram, kSortBuckets / 32 buckets per lane
         constexpr int kPer = kSortBuckets / 32;
@@ -265,8 +276,7 @@ int launch_plan(const AttnArgs& a) {
     p.flops_per_pair = 4.0 * a.desc->head_dim * a.desc->num_q_heads;
     p.ws = a.ws;
     p.err = a.err;
-    plan_kernel<<<1, 1024, 0, a.stream>>>(p);
-    return cuda_status(cudaGetLastError());
+    return cuda_status(launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, a.stream, p));
 }
 
 // ---------------------------------------------------------------------------
@@ -585,6 +595,7 @@ struct MergeParams {
 template <typename T, int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(MergeParams p) {
     pdl_wait_prerequisites();   // the split kernel's partials
+    pdl_launch_dependents();    // the next call's first kernel may become resident
     constexpr int DPL = D / 32;
     constexpr int kBatch = 8;   // splits whose O rows are requested together
     const int lane = threadIdx.x & 31;

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <utility>
 
 namespace pkv {
 
@@ -32,6 +33,28 @@ int kernel_occupancy(int threads, int smem) {
         return 0;
     cached[dev].store(v, std::memory_order_relaxed);
     return v;
+}
+
+// Launch `kern` with programmatic dependent launch allowed: it may become
+// resident while the kernel before it on the stream is still running (once that
+// kernel triggers its dependents), so the launch latency hides behind that
+// kernel's tail.  Every kernel launched this way waits for its prerequisites
+// (griddepcontrol.wait) before it reads or writes anything the work ahead of it
+// could touch, so stream order holds.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 }  // namespace pkv

@@ -224,3 +224,24 @@ def test_never_written_rows_may_hold_nan_decode(rt, lib, hq, hkv, dtype):
     assert np.isfinite(out_f64(out)).all()
     mx, mean = errors(out, ref)
     assert mx <= TOL[dtype][0] and mean <= TOL[dtype][1]
+
+
+def test_bad_query_layout_is_flagged_and_nothing_runs(rt, lib):
+    """query_start_loc must run from 0 to num_query_tokens: otherwise the planner
+    flags PKV_DEV_BAD_QUERY_LAYOUT and plans no work (the output is not written)."""
+    from paged_kv_cache_51_gb300 import paged_attention_varlen
+
+    w = workloads.random_varlen(61, "bf16", 16, 8, 128, 16, [(30, 2), (9, 1)], scale=0.5)
+    dc, step = rt.prepare(w)
+    step.write_kv()
+    lib.device_error(clear=True)
+    bad_qsl = torch.tensor([0, 2, 2], dtype=torch.int32, device="cuda")   # ends at 2, not 3
+    out = torch.full_like(step.q, 7.0)
+    paged_attention_varlen(out, step.q, dc.k_cache, dc.v_cache, dc.desc, step.tables, bad_qsl,
+                           step.ctx, step.max_qlen, step.max_ctx)
+    assert lib.device_error() == 5                                   # PKV_DEV_BAD_QUERY_LAYOUT
+    assert bool((out == 7.0).all())
+    # the same call with the right layout is unaffected
+    step.attend()
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0

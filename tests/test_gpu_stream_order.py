@@ -1,13 +1,16 @@
 """GPU: every attention call sees the device work queued before it on its stream.
 
-The attention entry points chain their kernels with programmatic dependent
-launch: the planner is an ordinary launch, and the kernels behind it (prefill,
-decode split, merge, 8-bit split) start early and wait for their predecessor
-before reading its output.  Here q is rewritten on the device (an exact sign
+The library's kernels are chained with programmatic dependent launch: the
+planner, the append and the block copies start while the kernel before them on
+the stream finishes, and the kernels behind the planner (prefill, decode split,
+merge, 8-bit split) start early too; each waits for its predecessor before it
+reads or writes anything.  Here q is rewritten on the device (an exact sign
 flip) right before each of several calls, with no host synchronisation in
 between, and every call's result is checked against the float64 oracle for the
-q it must have read.  A kernel that read q (or the plan) before the writes
-ahead of it had finished would fail this.
+q it must have read; and the step's new K/V rows are rewritten by the
+library's own append between calls, so nothing but its kernels separates one
+call from the next.  A kernel that read q, the cache or the plan before the
+writes ahead of it had finished would fail this.
 """
 
 import numpy as np
@@ -111,3 +114,37 @@ def test_int8_decode_sees_each_new_q(rt, lib):
         sign = -1 if i % 2 == 0 else +1
         mx, mean = errors(o, ref[sign])
         assert mx <= tmax and mean <= tmean, (i, sign, mx, mean)
+
+
+def test_attention_sees_each_append_before_it(rt, lib):
+    """append (variant i) -> attention -> append (variant i + 1) -> ..., queued
+    back to back: each call must see its own append's rows."""
+    from oracle import cache as ocache
+    from paged_kv_cache_51_gb300 import paged_attention_decode, paged_kv_append
+
+    w = workloads.config3(batch=8)
+    ost, _, dc, step, _ = run_both(w, rt)
+    rng = np.random.default_rng(71)
+    variants = [workloads._values(rng, tuple(step.k_new.shape), "bf16", 0.5) for _ in range(4)]
+    dev = [torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).view(torch.bfloat16).cuda()
+           for v in variants]
+    slots = step.slot_mapping.cpu().numpy()
+    outs = [torch.empty_like(step.q) for _ in variants]
+    torch.cuda.synchronize()
+    for i in range(len(variants)):
+        # K takes variant i, V variant i + 1 (mod n): a stale row of either shows
+        paged_kv_append(dev[i], dev[(i + 1) % len(dev)], step.slot_mapping, dc.k_cache,
+                        dc.v_cache, dc.desc)
+        paged_attention_decode(outs[i], step.q, dc.k_cache, dc.v_cache, dc.desc, step.tables,
+                               step.ctx, step.max_ctx, ws=step.ws)
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0
+    tmax, tmean = TOL["bf16"]
+    bt, ctx, _ = ost.batch_metadata()
+    for i in range(len(variants)):
+        kc, vc = ost.k_cache.copy(), ost.v_cache.copy()
+        ocache.append(kc, vc, variants[i], variants[(i + 1) % len(variants)], slots,
+                      w.block_size)
+        ref = oatt.decode(w.q, kc, vc, bt, ctx, w.block_size, "bf16")
+        mx, mean = errors(outs[i], ref)
+        assert mx <= tmax and mean <= tmean, (i, mx, mean)
