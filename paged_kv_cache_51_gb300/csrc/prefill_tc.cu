@@ -514,16 +514,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             out_staged[qb] = false;
         };
+        // The next unit's ticket is taken when this unit's last K tile is issued,
+        // not when the unit starts: the units come longest first, and a CTA that
+        // reserved its next unit at the start of a long one would take a long or
+        // medium unit that a CTA finishing sooner should get (measured on the
+        // SplitFuse chunks: CTAs ending at 33 and at 44 us).  The atomic's latency
+        // still hides behind the unit's last products and epilogue.
         int next = lane == 0 ? atomicAdd(p.ticket, 1) : 0;
         for (;; ++k) {
             const int slot = k % kUnitSlots;
             ok = ok && __all_sync(0xffffffffu, mbar_wait(&bars[B_U_EMPTY + slot],
                                                          ((k / kUnitSlots) & 1) ^ 1, p.err));
             int u = -1;
-            if (lane == 0 && ok && !*abort_flag && next < n_units) {
-                u = next;
-                next = atomicAdd(p.ticket, 1);
-            }
+            if (lane == 0 && ok && !*abort_flag && next < n_units) u = next;
             u = __shfl_sync(0xffffffffu, u, 0);
             Unit x = {};
             if (u >= 0) x = unit_of(p, u);
@@ -558,6 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int st = kt % kKStages;
                 const int nb = min(kBlkPerTile, x.nblk - j * kBlkPerTile);
                 const int blk = ids.tile(j, lane);
+                if (j == x.n_tiles - 1 && lane == 0) next = atomicAdd(p.ticket, 1);
                 ok = __all_sync(0xffffffffu,
                                 mbar_wait(&bars[B_S_FULL + st], ((kt / kKStages) & 1) ^ 1, p.err));
                 if (!ok || *abort_flag) {
