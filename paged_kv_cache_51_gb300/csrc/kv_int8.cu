@@ -443,15 +443,22 @@ __global__ void __launch_bounds__(I8Cfg<D, G>::kThreads, I8Cfg<D, G>::kMinBlocks
             // head g, tokens 4t .. 4t + 3 (the PV product's k index, permuted as on the V side)
             const uint2 bp = *reinterpret_cast<const uint2*>(pb + g * kBlockTokens + 4 * t);
 
-            // O^T = diag-scaled O^T + V^T P': rows dims 16 mb + g, + 8; columns heads 2t, 2t + 1
+            // O^T = diag-scaled O^T + V^T P': rows dims 16 mb + g, + 8; columns heads 2t, 2t + 1.
+            // The rescale is skipped when every lane's factors are exactly 1 (the
+            // running max and the V-scale exponent unchanged): the same bits.
+            if (__any_sync(kFullWarp, ao.x != 1.f || ao.y != 1.f)) {
+#pragma unroll
+                for (int mb = 0; mb < KB; ++mb) {
+                    const float2 lo = __fmul2_rn(make_float2(o[mb][0], o[mb][1]), ao);
+                    const float2 hi = __fmul2_rn(make_float2(o[mb][2], o[mb][3]), ao);
+                    o[mb][0] = lo.x;
+                    o[mb][1] = lo.y;
+                    o[mb][2] = hi.x;
+                    o[mb][3] = hi.y;
+                }
+            }
 #pragma unroll
             for (int mb = 0; mb < KB; ++mb) {
-                const float2 lo = __fmul2_rn(make_float2(o[mb][0], o[mb][1]), ao);
-                const float2 hi = __fmul2_rn(make_float2(o[mb][2], o[mb][3]), ao);
-                o[mb][0] = lo.x;
-                o[mb][1] = lo.y;
-                o[mb][2] = hi.x;
-                o[mb][3] = hi.y;
                 const uint32_t u0 =
                     *reinterpret_cast<const uint32_t*>(vt + (16 * mb + g) * kBlockTokens + 4 * t);
                 const uint32_t u1 = *reinterpret_cast<const uint32_t*>(
