@@ -333,7 +333,8 @@ PKV_API size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t nu
  * Long contexts are split into fixed spans of 512 tokens whose partial
  * (max, sum, output) states are merged in a second kernel; the split depends
  * only on the context length, so a sequence's result does not depend on the
- * rest of the batch. */
+ * rest of the batch.  num_seqs == 0 is a no-op: the descriptor and the sizes
+ * are checked, the pointers are not (zero-sized tensors may be null). */
 PKV_API int paged_attention_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
                            const pkv_cache_desc* desc, const int32_t* block_tables,
                            int32_t max_blocks_per_seq, const int32_t* context_lens,
@@ -386,6 +387,7 @@ PKV_API size_t pkv_varlen_workspace_bytes(const pkv_cache_desc* desc, int32_t nu
  *   query_start_loc:  device int32 [num_seqs + 1], 0 .. num_query_tokens
  *   context_lens:     device int32 [num_seqs], >= qlen_s, <= max_context_len
  *   max_query_len:    host upper bound of qlen_s
+ * num_seqs == 0 or num_query_tokens == 0 is a no-op (pointers unchecked).
  * Other arguments as for paged_attention_decode. */
 PKV_API int paged_attention_varlen(void* out, const void* q, const void* k_cache, const void* v_cache,
                            const pkv_cache_desc* desc, const int32_t* block_tables,

@@ -85,19 +85,24 @@ namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-int check_attention_common(void* out, const void* q, const void* k_cache, const void* v_cache,
-                           const pkv_cache_desc* desc, const int32_t* block_tables,
-                           int32_t max_blocks_per_seq, const int32_t* context_lens,
-                           int32_t max_context_len, float scale) {
+// Checks that do not look at the pointers (run first: an empty batch is a
+// no-op whatever its pointers hold, as zero-sized tensors often give null).
+int check_attention_scalars(const pkv_cache_desc* desc, int32_t max_blocks_per_seq,
+                            int32_t max_context_len, float scale) {
     int st = check_desc(desc, true);
     if (st != PKV_OK) return st;
+    if (max_blocks_per_seq < 1 || max_context_len < 1) return PKV_ERR_INVALID;
+    if (!std::isfinite(scale)) return PKV_ERR_INVALID;
+    return PKV_OK;
+}
+
+int check_attention_pointers(void* out, const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, const int32_t* context_lens) {
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
         return PKV_ERR_INVALID;
     if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
         !aligned(block_tables, 4) || !aligned(context_lens, 4))
         return PKV_ERR_INVALID;
-    if (max_blocks_per_seq < 1 || max_context_len < 1) return PKV_ERR_INVALID;
-    if (!std::isfinite(scale)) return PKV_ERR_INVALID;
     return PKV_OK;
 }
 
@@ -130,10 +135,11 @@ extern "C" int paged_attention_decode(void* out, const void* q, const void* k_ca
                                       int32_t max_context_len, float scale, void* workspace,
                                       size_t workspace_bytes, void* stream) {
     if (num_seqs < 0) return PKV_ERR_INVALID;
-    int st = check_attention_common(out, q, k_cache, v_cache, desc, block_tables,
-                                    max_blocks_per_seq, context_lens, max_context_len, scale);
+    int st = check_attention_scalars(desc, max_blocks_per_seq, max_context_len, scale);
     if (st != PKV_OK) return st;
     if (num_seqs == 0) return PKV_OK;
+    st = check_attention_pointers(out, q, k_cache, v_cache, block_tables, context_lens);
+    if (st != PKV_OK) return st;
     const size_t need = pkv_decode_workspace_bytes(desc, num_seqs, max_context_len);
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return PKV_ERR_WORKSPACE;
     AttnArgs a{};
@@ -168,11 +174,12 @@ static int varlen_impl(void* out, const void* q, const void* k_cache, const void
                        float scale, void* workspace, size_t workspace_bytes, void* stream) {
     if (num_seqs < 0 || num_query_tokens < 0 || max_query_len < 0 || window < 0)
         return PKV_ERR_INVALID;
-    int st = check_attention_common(out, q, k_cache, v_cache, desc, block_tables,
-                                    max_blocks_per_seq, context_lens, max_context_len, scale);
+    int st = check_attention_scalars(desc, max_blocks_per_seq, max_context_len, scale);
+    if (st != PKV_OK) return st;
+    if (num_seqs == 0 || num_query_tokens == 0) return PKV_OK;
+    st = check_attention_pointers(out, q, k_cache, v_cache, block_tables, context_lens);
     if (st != PKV_OK) return st;
     if (!query_start_loc || !aligned(query_start_loc, 4)) return PKV_ERR_INVALID;
-    if (num_seqs == 0 || num_query_tokens == 0) return PKV_OK;
     if (max_query_len > max_context_len) return PKV_ERR_INVALID;
     if (max_query_len > 1 && !prefill_supported(desc)) return PKV_ERR_UNSUPPORTED;
     const size_t need = pkv_varlen_workspace_bytes(desc, num_seqs, num_query_tokens,

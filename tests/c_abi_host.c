@@ -1,6 +1,7 @@
 /* A C99 client of libpagedkv.so that uses only host entry points (no GPU):
- * the block pool with fork and copy-on-write, block-table export, the
- * SplitFuse composer, workspace sizing and status strings.  It checks each
+ * the block pool with fork and copy-on-write, block-table export, a
+ * sliding-window pool with room for prefill chunks and its logically ordered
+ * tables, the SplitFuse composer, workspace sizing and status strings.  It checks each
  * result against values worked out by hand from the rules in pagedkv.h and
  * prints "ok" when all hold.  Built and run by tests/test_c_abi.py. */
 #include <stdio.h>
@@ -77,6 +78,31 @@ int main(void) {
     CHECK(pkv_status_string(PKV_ERR_NO_BLOCKS) != NULL &&
           strlen(pkv_status_string(PKV_ERR_NO_BLOCKS)) > 0);
     CHECK(pkv_status_string(12345) != NULL);
+
+    /* a sliding-window pool with room for chunks of up to 6 queries: window 8
+     * (2 blocks of 4) + ceil(5 / 4) = 4 ring blocks, handed out 0, 1, 2, 3 */
+    {
+        pkv_pool* wp = NULL;
+        int64_t wid = 7, wslots[6], wslot = -1;
+        int32_t q6 = 6, q1 = 1, q10 = 10, wt[5], wctx = 0;
+        CHECK(pkv_pool_create_window(32, 4, 0, NULL, 8, 6, &wp) == PKV_OK && wp != NULL);
+        CHECK(pkv_seq_add(wp, wid, 6, wslots) == PKV_OK && wslots[5] == 1 * 4 + 1);
+        for (i = 0; i < 15; ++i)
+            CHECK(pkv_seq_append_slot(wp, wid, &wslot, &src, &dst) == PKV_OK && src == -1);
+        /* 21 tokens: logical blocks 4 and 5 reuse ring entries 0 and 1 */
+        CHECK(wslot == 1 * 4 + 0);
+        /* the last 6 tokens as queries: first key 21 - 6 - 8 + 1 = 8, block 2;
+         * logical blocks 2..5 are ring entries 2, 3, 0, 1; context 21 - 8 */
+        CHECK(pkv_window_tables(wp, &wid, &q6, 1, 5, wt, &wctx) == PKV_OK);
+        CHECK(wt[0] == 2 && wt[1] == 3 && wt[2] == 0 && wt[3] == 1 && wt[4] == -1 && wctx == 13);
+        /* one decode query: first key 13, block 3; context 21 - 12 */
+        CHECK(pkv_window_tables(wp, &wid, &q1, 1, 5, wt, &wctx) == PKV_OK);
+        CHECK(wt[0] == 3 && wt[1] == 0 && wt[2] == 1 && wt[3] == -1 && wctx == 9);
+        /* 10 + 8 - 1 keys do not fit the ring's 16 tokens */
+        CHECK(pkv_window_tables(wp, &wid, &q10, 1, 5, wt, &wctx) == PKV_ERR_INVALID);
+        CHECK(pkv_block_tables(wp, &wid, 1, 5, wt, &wctx) == PKV_ERR_UNSUPPORTED);
+        CHECK(pkv_pool_destroy(wp) == PKV_OK);
+    }
 
     if (failures) return 1;
     printf("ok\n");

@@ -171,6 +171,16 @@ def test_device_calls_reject_bad_arguments_before_launch(lib):
     # zero-sized work is a no-op
     assert L.paged_kv_append(None, None, None, 0, None, None, ref(desc), None) == 0
     assert L.pkv_copy_blocks(None, 0, None, None, ref(desc), None) == 0
+    # an empty attention batch is a no-op whatever its pointers hold (zero-sized
+    # tensors often have a null data pointer); its descriptor is still checked
+    assert L.paged_attention_decode(None, None, None, None, ref(desc), None, 4, None, 0, 16,
+                                    0.1, None, 0, None) == 0
+    assert L.paged_attention_decode(None, None, None, None, ref(odd), None, 4, None, 0, 16,
+                                    0.1, None, 0, None) == lib.PKV_ERR_UNSUPPORTED
+    assert L.paged_attention_varlen(None, None, None, None, ref(desc), None, 4, None, None, 2, 0,
+                                    0, 16, 0.1, None, 0, None) == 0
+    assert L.paged_attention_varlen(None, None, None, None, ref(desc), None, 4, None, None, 0, 0,
+                                    0, 16, 0.1, None, 0, None) == 0
 
 
 def test_int8_entry_points_validate_on_the_host(lib):

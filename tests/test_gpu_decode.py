@@ -245,3 +245,41 @@ def test_bad_query_layout_is_flagged_and_nothing_runs(rt, lib):
     step.attend()
     torch.cuda.synchronize()
     assert lib.device_error() == 0
+
+
+def test_empty_inputs_are_no_ops(rt, lib):
+    """No sequences, no query tokens, no new tokens, no copy pairs: each call
+    returns at once, touches no output and records no device error."""
+    from paged_kv_cache_51_gb300 import (paged_attention_decode, paged_attention_varlen,
+                                         paged_kv_append, pkv_copy_blocks)
+
+    w = workloads.random_decode(71, "bf16", 16, 8, 128, 16, [40, 7], scale=0.5)
+    dc, step = rt.prepare(w)
+    step.write_kv()
+    lib.device_error(clear=True)
+    k_before, v_before = dc.k_cache.clone(), dc.v_cache.clone()
+    q0 = step.q[:0]
+    out0 = torch.empty_like(q0)
+    paged_attention_decode(out0, q0, dc.k_cache, dc.v_cache, dc.desc, step.tables[:0],
+                           step.ctx[:0], step.max_ctx)
+    # varlen with sequences that have no query rows: nothing is written
+    sentinel = torch.full_like(step.q, 3.0)
+    qsl_empty = torch.zeros(len(w.batch) + 1, dtype=torch.int32, device="cuda")
+    paged_attention_varlen(sentinel[:0], q0, dc.k_cache, dc.v_cache, dc.desc, step.tables,
+                           qsl_empty, step.ctx, 0, step.max_ctx)
+    rows = torch.empty((0, 8, 128), dtype=torch.bfloat16, device="cuda")
+    paged_kv_append(rows, rows, torch.empty(0, dtype=torch.int64, device="cuda"), dc.k_cache,
+                    dc.v_cache, dc.desc)
+    pkv_copy_blocks(torch.empty((0, 2), dtype=torch.int32, device="cuda"), dc.k_cache,
+                    dc.v_cache, dc.desc)
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0
+    assert torch.equal(dc.k_cache, k_before) and torch.equal(dc.v_cache, v_before)
+    assert bool((sentinel == 3.0).all())
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (64, 8)])
+def test_longest_context_many_split_passes(rt, lib, hq, hkv):
+    """131072 keys: 256 splits, so the merge folds eight passes of 32 splits."""
+    w = workloads.random_decode(72, "bf16", hq, hkv, 128, 16, [131072, 1000], scale=0.5)
+    _check(w, rt, lib)
