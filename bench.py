@@ -476,13 +476,18 @@ def next_rows_summary(reps=20, warmup=3):
     bw, _, _, _ = peaks()
     dev = torch.device("cuda")
     g = torch.Generator(device="cpu").manual_seed(7)
-    T, hq, hkv, d, bs, maxpos = 16384, 32, 8, 128, 16, 4096
-    nb = T // bs + 64
-    k = (torch.randn((T, hkv, d), generator=g) * 0.5).to(torch.bfloat16).to(dev)
-    v = (torch.randn((T, hkv, d), generator=g) * 0.5).to(torch.bfloat16).to(dev)
-    q = (torch.randn((T, hq, d), generator=g) * 0.5).to(torch.bfloat16).to(dev)
-    q_out = torch.empty_like(q)
-    slots = torch.randperm(nb * bs, generator=g)[:T].to(torch.int64).to(dev)
+    T, hq, hkv, d, bs, maxpos, sets = 16384, 32, 8, 128, 16, 4096, 4
+    nb = sets * (T // bs)          # each input set writes its own quarter of the pool
+
+    def rows(h):
+        return (torch.randn((T, h, d), generator=g) * 0.5).to(torch.bfloat16).to(dev)
+
+    ks = [rows(hkv) for _ in range(sets)]
+    vs = [rows(hkv) for _ in range(sets)]
+    qs = [rows(hq) for _ in range(sets)]
+    q_outs = [torch.empty_like(qs[0]) for _ in range(sets)]
+    slot_sets = [(torch.randperm(T, generator=g) + j * T).to(torch.int64).to(dev)
+                 for j in range(sets)]
     pos = (torch.arange(T, dtype=torch.int32) % maxpos).to(dev)
     cos_sin = (torch.rand((maxpos, d), generator=g) * 2 - 1).to(dev)
     kc = torch.zeros((nb, hkv, bs, d), dtype=torch.bfloat16, device=dev)
@@ -491,28 +496,40 @@ def next_rows_summary(reps=20, warmup=3):
     stream = torch.cuda.current_stream()
 
     def timed(fn):
-        for _ in range(warmup):
-            fn()
+        """(ms per call with `reps` calls back to back between one event pair,
+        median ms of one call between its own event pair).  Calls rotate over
+        the input sets, so a call's inputs and cache rows were last touched
+        three calls (about 0.4 GB of traffic) earlier: not in L2."""
+        for j in range(max(warmup, sets)):
+            fn(j % sets)
         torch.cuda.synchronize()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(reps)]
-        for a, b in ev:
+        for i, (a, b) in enumerate(ev):
             a.record(stream)
-            fn()
+            fn(i % sets)
             b.record(stream)
         torch.cuda.synchronize()
-        return statistics.median(a.elapsed_time(b) for a, b in ev)
+        single = statistics.median(a.elapsed_time(b) for a, b in ev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(reps):
+            fn(i % sets)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps, single
 
-    rope_ms = timed(lambda: pkv.paged_kv_append_rope(k, v, slots, pos, cos_sin, kc, vc, desc,
-                                                     q=q, q_out=q_out))
-    plain_ms = timed(lambda: pkv.paged_kv_append(k, v, slots, kc, vc, desc))
+    rope_ms, rope_single = timed(lambda j: pkv.paged_kv_append_rope(
+        ks[j], vs[j], slot_sets[j], pos, cos_sin, kc, vc, desc, q=qs[j], q_out=q_outs[j]))
+    plain_ms, plain_single = timed(lambda j: pkv.paged_kv_append(ks[j], vs[j], slot_sets[j], kc,
+                                                                 vc, desc))
     if pkv.device_error() != 0:
         raise SystemExit("device error in the append measurements")
     kv_bytes = T * hkv * d * 2 * 2
     q_bytes = T * hq * d * 2
     rope_bytes = 2 * kv_bytes + 2 * q_bytes + T * (8 + 4) + min(T, maxpos) * d * 4
     plain_bytes = 2 * kv_bytes + T * 8
-    del k, v, q, q_out, kc, vc
+    del ks, vs, qs, q_outs, kc, vc
     torch.cuda.empty_cache()
 
     # SplitFuse composer (host)
@@ -553,7 +570,10 @@ def next_rows_summary(reps=20, warmup=3):
             "bytes": rope_bytes, "achieved_gbs": rope_bytes / (rope_ms * 1e-3) / 1e9,
             "frac": rope_bytes / (rope_ms * 1e-3) / 1e9 / bw,
             "plain_append_ms": plain_ms,
-            "plain_append_frac": plain_bytes / (plain_ms * 1e-3) / 1e9 / bw},
+            "plain_append_frac": plain_bytes / (plain_ms * 1e-3) / 1e9 / bw,
+            "timing": "calls back to back over 4 input sets and 4 disjoint quarters of the "
+                      "pool (nothing in L2); *_single_ms: one call between its own events",
+            "ms_single": rope_single, "plain_append_ms_single": plain_single},
         "compose": {"us_per_step": compose_us, "budget": 2048, "decodes": 512,
                     "waiting_prompts": len(prompts)},
         "prefix_pool": {"us_per_add_tokens_3000": add_us, "us_per_append_token": append_us,
