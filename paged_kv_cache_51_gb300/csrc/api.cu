@@ -161,6 +161,7 @@ extern "C" int paged_attention_decode(void* out, const void* q, const void* k_ca
     a.max_context_len = max_context_len;
     a.scale = scale;
     a.stream = static_cast<cudaStream_t>(stream);
+    a.group_splits = true;
     if ((st = launch_plan(a)) != PKV_OK) return st;
     if ((st = launch_decode_split(a)) != PKV_OK) return st;
     return launch_decode_merge(a);

@@ -56,14 +56,65 @@ struct PlanParams {
     int32_t tokens_per_tile;          // prefill tile height in tokens
     int32_t num_sms;
     int32_t window;                   // sliding window in keys (0: none)
+    int32_t group;                    // group sequences that share complete splits
+    const int32_t* block_tables;      // read only when grouping
     double kv_bytes_per_token;        // K + V bytes of one token, all KV heads
     double flops_per_pair;            // QK^T + PV flops of one (query, key) pair, all query heads
     Workspace ws;
     int* err;
 };
 
+constexpr int kGroupSeqs = 4096;    // batches up to this size are grouped (shared memory)
 constexpr int kSortItems = 2048;    // prefill items reordered longest first (at most)
 constexpr int kSortBuckets = 256;   // key-tile counts (larger counts share the last bucket)
+
+// Complete 512-token splits of a decode row over `ctx` keys, or 0 when the row
+// fails the planner's checks (it is then flagged and gets no work).
+__device__ __forceinline__ int complete_splits(const PlanParams& p, int ctx) {
+    const bool valid = ctx >= 1 && ctx <= p.max_context_len &&
+                       (ctx + kBlockTokens - 1) / kBlockTokens <= p.table_stride;
+    return valid ? ctx / kSplitTokens : 0;
+}
+
+// Decode items of sequence s when sequences that share complete splits are
+// grouped (paged_attention_decode, groups of 8 query heads, no window).
+// sh[s] = n means s reads the same 32 blocks as sequence s - 1 in each of its
+// first n splits (s "follows" s - 1 there).  For each split j a run of
+// sequences reads the same blocks: one that does not follow, then the
+// followers after it.  A run is cut into chunks at batch positions that are
+// multiples of kMaxGroup; each chunk is one item, owned by its first sequence
+// (a grouped item when the chunk holds two or more sequences, else a plain
+// one).  So s owns split j when it starts a run there, or follows and sits at
+// a multiple of kMaxGroup.  Writes s's items when `out` is given; returns
+// their number.
+__device__ __forceinline__ int grouped_items(const PlanParams& p, const int* sh, int s, int ctx,
+                                             int2* out) {
+    const int nsplit = (ctx - 1) / kSplitTokens + 1;
+    const int own = sh[s];
+    // how far the chunk may reach: up to the next multiple of kMaxGroup
+    const int cap = min(kMaxGroup - s % kMaxGroup, p.num_seqs - s);
+    int f[kMaxGroup - 1];                     // shares of the sequences after s in the chunk
+#pragma unroll
+    for (int k = 0; k < kMaxGroup - 1; ++k) f[k] = k + 1 < cap ? sh[s + 1 + k] : 0;
+    if (own == 0 && f[0] == 0) {
+        // shares nothing with its neighbours: one item per split
+        if (out)
+            for (int j = 0; j < nsplit; ++j) out[j] = make_int2(s, j);
+        return nsplit;
+    }
+    const bool aligned = s % kMaxGroup == 0;
+    int n = 0;
+    for (int j = 0; j < nsplit; ++j) {
+        if (j < own && !aligned) continue;    // inside a chunk another sequence owns
+        int m = 1;                            // sequences s .. s + m - 1 read split j
+#pragma unroll
+        for (int k = 0; k < kMaxGroup - 1; ++k)
+            if (m == k + 1 && f[k] > j) m = k + 2;
+        if (out) out[n] = make_int2(s, j | (m >= 2 ? m << kItemSplitBits : 0));
+        ++n;
+    }
+    return n;
+}
 
 __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
     __shared__ int warp_d[32], warp_p[32];
@@ -74,6 +125,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
     __shared__ int2 s_item[kSortItems];
     __shared__ int s_bucket[kSortItems];
     __shared__ int hist[kSortBuckets], cursor[kSortBuckets];
+    __shared__ int s_shared[kGroupSeqs];   // shared_splits of each sequence
+    const bool group = p.group && p.num_seqs <= kGroupSeqs;
     unsigned long long my_tok = 0, my_pairs = 0;   // this thread's work estimate
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int sortable = min(kSortItems, p.ws.max_prefill_items);
@@ -95,6 +148,48 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
         carry_p = 0;
     }
     for (int i = tid; i < kSortBuckets; i += 1024) hist[i] = 0;
+    if (group) {
+        // How many leading complete splits each sequence shares, block for
+        // block, with the one before it.  First every thread checks its
+        // sequences' first block ids (one round of loads for the batch); then a
+        // warp per remaining candidate compares the ids of up to 8 splits at a
+        // time, a lane per block.
+        constexpr int kPer = kSplitTokens / kBlockTokens;
+        constexpr int kBatch = 8;
+        static_assert(kPer == 32, "one block id per lane");
+        for (int s = tid; s < p.num_seqs; s += 1024) {
+            int cand = 0;                        // -(splits to compare) for a candidate
+            if (s > 0) {
+                const int c1 = p.context_lens[s], c0 = p.context_lens[s - 1];
+                const int32_t* t1 = p.block_tables + size_t(s) * p.table_stride;
+                const int32_t f1 = t1[0], f0 = t1[-p.table_stride];
+                const int n = min(complete_splits(p, c1), complete_splits(p, c0));
+                if (n > 0 && f1 == f0) cand = -n;
+            }
+            s_shared[s] = cand;
+        }
+        __syncthreads();
+        for (int s = warp; s < p.num_seqs; s += 32) {
+            const int n = -s_shared[s];
+            if (n <= 0) continue;
+            const int32_t* t1 = p.block_tables + size_t(s) * p.table_stride + lane;
+            const int32_t* t0 = t1 - p.table_stride;
+            int shared = 0;
+            for (int j0 = 0; j0 < n && shared == j0; j0 += kBatch) {
+                int a[kBatch], b[kBatch];
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    a[u] = j0 + u < n ? t1[(j0 + u) * kPer] : 0;
+                    b[u] = j0 + u < n ? t0[(j0 + u) * kPer] : 1;
+                }
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u)
+                    if (shared == j0 + u && __all_sync(kFull, a[u] == b[u])) shared = j0 + u + 1;
+            }
+            __syncwarp();
+            if (lane == 0) s_shared[s] = shared;
+        }
+    }
     __syncthreads();
     for (int base = 0; base < p.num_seqs; base += 1024) {
         const int s = base + tid;
@@ -114,7 +209,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
                     // the splits from the one holding the window's first key
                     const int lo = window_first_key(ctx - 1, p.window);
                     first_split = lo / kSplitTokens;
-                    nd = (ctx - 1) / kSplitTokens - first_split + 1;
+                    nd = group ? grouped_items(p, s_shared, s, ctx, nullptr)
+                               : (ctx - 1) / kSplitTokens - first_split + 1;
                     my_tok += (unsigned long long)(ctx - lo);
                 } else {
                     np = (qlen + p.tokens_per_tile - 1) / p.tokens_per_tile;
@@ -165,7 +261,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
         __syncthreads();
         const int before_d = carry_d + (warp ? warp_d[warp - 1] : 0) + xd - nd;
         const int before_p = carry_p + (warp ? warp_p[warp - 1] : 0) + xp - np;
-        for (int k = 0; k < nd; ++k) p.ws.items[before_d + k] = make_int2(s, first_split + k);
+        if (group) {
+            if (nd) grouped_items(p, s_shared, s, ctx, p.ws.items + before_d);
+        } else {
+            for (int k = 0; k < nd; ++k) p.ws.items[before_d + k] = make_int2(s, first_split + k);
+        }
         for (int k = 0; k < np; ++k) {
             const int idx = before_p + k;
             if (idx < p.ws.max_prefill_items) p.ws.prefill_items[idx] = make_int2(s, k);
@@ -271,6 +371,10 @@ int launch_plan(const AttnArgs& a) {
     p.tokens_per_tile = kPrefillRows / (a.desc->num_q_heads / a.desc->num_kv_heads);
     p.num_sms = num_sms();
     p.window = a.window;
+    // grouped items are read only by the tensor-core kernel for groups of 8
+    p.group = a.group_splits && a.window == 0 && !a.query_start_loc &&
+              decode_mma_eligible(a.desc) && a.desc->num_q_heads == 8 * a.desc->num_kv_heads;
+    p.block_tables = a.block_tables;
     p.kv_bytes_per_token =
         2.0 * a.desc->num_kv_heads * a.desc->head_dim * double(elem_bytes(a.desc->dtype));
     p.flops_per_pair = 4.0 * a.desc->head_dim * a.desc->num_q_heads;
@@ -597,7 +701,9 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(MergeParams p) {
     pdl_wait_prerequisites();   // the split kernel's partials
     pdl_launch_dependents();    // the next call's first kernel may become resident
     constexpr int DPL = D / 32;
-    constexpr int kBatch = 8;   // splits whose O rows are requested together
+    // splits whose O rows are requested together (16 and 32 measured no faster
+    // overall: the registers they take cost the short rows' occupancy)
+    constexpr int kBatch = 8;
     const int lane = threadIdx.x & 31;
     const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int Hq = p.num_q_heads;
@@ -616,8 +722,12 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(MergeParams p) {
     if (n <= 1) return;                                     // written by the split kernel
     // slot of split first + k: base + k
     const size_t base = (size_t(seq) * Hq + h) * p.max_splits + first;
-    float M = -INFINITY;
-    for (int k = lane; k < n; k += 32) M = fmaxf(M, p.part_ml[base + k].x);
+    // (m, l) of splits lane and lane + 32 stay in registers for the second pass
+    const float2 none = make_float2(-INFINITY, 0.f);
+    const float2 ml_a = lane < n ? p.part_ml[base + lane] : none;
+    const float2 ml_b = lane + 32 < n ? p.part_ml[base + lane + 32] : none;
+    float M = fmaxf(ml_a.x, ml_b.x);
+    for (int k = lane + 64; k < n; k += 32) M = fmaxf(M, p.part_ml[base + k].x);
 #pragma unroll
     for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
     float L = 0.f, acc[DPL];
@@ -626,7 +736,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(MergeParams p) {
     for (int k0 = 0; k0 < n; k0 += 32) {
         float w = 0.f;
         if (k0 + lane < n) {
-            const float2 ml = __ldcs(p.part_ml + base + k0 + lane);
+            const float2 ml = k0 == 0 ? ml_a : k0 == 32 ? ml_b : __ldcs(p.part_ml + base + k0 + lane);
             w = exp2f(ml.x - M);
             L = fmaf(ml.y, w, L);
         }

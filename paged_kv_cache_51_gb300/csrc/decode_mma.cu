@@ -60,17 +60,18 @@ struct MmaCfg {
     static constexpr int kHalves = D / 64;                 // 64-dim boxes per tile
     static constexpr int kTileBytes = kBlockTokens * D * 2;
     static constexpr int kStageBytes = 2 * kTileBytes;
-    // g = 8 runs 3 CTAs per SM on a 4-stage ring (measured faster on the
-    // prefix-sharing batch); smaller groups run 12 stages at 2 CTAs per SM
-    // (192 KB of tiles in flight per SM; measured 0.5 % faster than 8 stages)
-    static constexpr int kStages = G == 8 ? 4 : 12;
-    static constexpr int kMinBlocks = G == 8 ? 3 : 1;
+    // 12 stages at 2 CTAs per SM: 192 KB of tiles in flight per SM (measured
+    // 0.5 % faster than 8 stages for g = 4).  For g = 8 the consumer warps
+    // combine through two records instead of four to make room.
+    static constexpr int kStages = 12;
+    static constexpr int kMinBlocks = G == 8 ? 2 : 1;
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kComb = G * (D + 2);
+    static constexpr int kCombRecords = G == 8 ? 2 : kWarps;
     static constexpr int kCombOff = kRingBytes;
     static constexpr int kQBytes = G * D * 2;               // q of one unit (bf16)
     static constexpr int kQSlots = 2;                       // units whose q is in flight
-    static constexpr int kQOff = kCombOff + kWarps * kComb * 4;
+    static constexpr int kQOff = kCombOff + kCombRecords * kComb * 4;
     static constexpr int kMetaOff = kQOff + kQSlots * kQBytes;
     static constexpr int kBarOff = kMetaOff + kQSlots * 32;
     // full[kStages], empty[kStages], q_full[kQSlots], q_empty[kQSlots]
@@ -124,6 +125,230 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t tile, int t, int c) {
     return tile + uint32_t((c >> 3) * (kBlockTokens * 128) + t * 128 + (((c & 7) ^ (t & 7)) << 4));
 }
 
+// Combine of a plain unit's four consumer-warp states for groups of 8 (every
+// row of the tile's top half is a query head, so each lane holds the whole
+// state of its row for its columns): warps 2 and 3 hand their states to warps
+// 0 and 1 through two records, warp 1 hands the merged state to warp 0, and
+// warp 0 writes the unit's split partials or outputs.  Two records instead of
+// four leave shared memory for a deeper tile ring.
+template <int D>
+__device__ __forceinline__ void combine_pairwise(const MmaParams& p, float* comb,
+                                                 float (&o)[D / 8][4], float& m_row,
+                                                 float& l_row, bool ok, int nsplit, int seq,
+                                                 int qrow, int split, int kvh) {
+    using C = MmaCfg<D, 8>;
+    constexpr int G = 8;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gid = lane >> 2, tig = lane & 3;
+    auto put = [&](float* rec) {
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n)
+            *reinterpret_cast<float2*>(rec + gid * D + n * 8 + 2 * tig) =
+                make_float2(o[n][0], o[n][1]);
+        if (tig == 0) {
+            rec[G * D + gid] = m_row;
+            rec[G * D + G + gid] = l_row;
+        }
+    };
+    auto merge = [&](const float* rec) {
+        const float m2 = rec[G * D + gid], l2 = rec[G * D + G + gid];
+        const float M = fmaxf(m_row, m2);
+        const float Mx = M == -INFINITY ? 0.f : M;    // both states empty: stay empty
+        const float s1 = exp2f(m_row - Mx), s2 = exp2f(m2 - Mx);
+        l_row = fmaf(l2, s2, l_row * s1);
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n) {
+            const float2 v = *reinterpret_cast<const float2*>(rec + gid * D + n * 8 + 2 * tig);
+            o[n][0] = fmaf(v.x, s2, o[n][0] * s1);
+            o[n][1] = fmaf(v.y, s2, o[n][1] * s1);
+        }
+        m_row = M;
+    };
+    if (warp >= 2) put(comb + (warp - 2) * C::kComb);
+    asm volatile("bar.sync 1, %0;" ::"r"(C::kWarps * 32) : "memory");
+    if (warp < 2) merge(comb + warp * C::kComb);
+    asm volatile("bar.sync 1, %0;" ::"r"(C::kWarps * 32) : "memory");
+    if (warp == 1) put(comb);
+    asm volatile("bar.sync 1, %0;" ::"r"(C::kWarps * 32) : "memory");
+    if (warp != 0) return;
+    merge(comb);
+    // (a failed wait leaves the unit's description unknown: write nothing)
+    if (!ok) return;
+    const int Hq = p.num_q_heads;
+    const int h = kvh * G + gid;
+    if (nsplit == 1) {
+        __nv_bfloat16* dst = p.out + (size_t(qrow) * Hq + h) * D + 2 * tig;
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n)
+            *reinterpret_cast<__nv_bfloat162*>(dst + n * 8) =
+                __floats2bfloat162_rn(o[n][0] / l_row, o[n][1] / l_row);
+    } else {
+        const uint64_t keep = l2_evict_last_policy();
+        const size_t slot = (size_t(seq) * Hq + h) * p.max_splits + split;
+        float* dst = p.part_o + slot * D + 2 * tig;
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n)
+            st_keep(reinterpret_cast<float2*>(dst + n * 8), make_float2(o[n][0], o[n][1]), keep);
+        if (tig == 0) st_keep(p.part_ml + slot, make_float2(m_row, l_row), keep);
+    }
+}
+
+// Rows gid (R = 0) or gid + 8 (R = 1) of a grouped split's accumulators: query
+// head h of sequence s, as its split partial, or as its output when the split
+// is the sequence's only one.
+template <int D, int R>
+__device__ __forceinline__ void grouped_write(const MmaParams& p, const float (&o)[D / 8][4], int s,
+                                              int h, int split, float m_row, float l_row) {
+    const int tig = threadIdx.x & 3;
+    const int Hq = p.num_q_heads;
+    const int nsplit = (p.context_lens[s] - 1) / kSplitTokens + 1;
+    if (nsplit == 1) {
+        __nv_bfloat16* dst = p.out + (size_t(s) * Hq + h) * D + 2 * tig;
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n)
+            *reinterpret_cast<__nv_bfloat162*>(dst + n * 8) =
+                __floats2bfloat162_rn(o[n][2 * R] / l_row, o[n][2 * R + 1] / l_row);
+    } else {
+        const uint64_t keep = l2_evict_last_policy();
+        const size_t slot = (size_t(s) * Hq + h) * p.max_splits + split;
+        float* dst = p.part_o + slot * D + 2 * tig;
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n)
+            st_keep(reinterpret_cast<float2*>(dst + n * 8),
+                    make_float2(o[n][2 * R], o[n][2 * R + 1]), keep);
+        if (tig == 0) st_keep(p.part_ml + slot, make_float2(m_row, l_row), keep);
+    }
+}
+
+// One complete 512-token split that `count` consecutive sequences from `first`
+// read block for block (groups of 8 query heads).  Every tile of the split is
+// loaded once and read by all four consumer warps; warp w takes sequences
+// first + 2w (tile rows 0..7, its eight query heads) and first + 2w + 1 (rows
+// 8..15, the rows a single sequence leaves empty), with a running max and sum
+// per row over all the split's tiles in order, and writes their split
+// partials, or their outputs when the split is a sequence's only one.
+template <int D>
+__device__ __forceinline__ void grouped_split(const MmaParams& p, uint32_t base, uint64_t* full,
+                                              uint64_t* empty, uint32_t it_base, int nb,
+                                              int first, int count, int split, int kvh,
+                                              bool& ok) {
+    using C = MmaCfg<D, 8>;
+    constexpr int G = 8;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int Hq = p.num_q_heads;
+    const int active = (count + 1) / 2;                // warps with members
+    const bool act = warp < active, has_b = 2 * warp + 1 < count;
+    const int sa = first + 2 * warp, sb = has_b ? sa + 1 : sa;
+    if (!act) return;   // warp 0 releases each tile for the warps without members
+
+    // q fragments (A operand): rows gid from sequence sa, rows gid + 8 from sb
+    uint32_t qa0[D / 16], qa1[D / 16], qa2[D / 16], qa3[D / 16];
+    {
+        const uint32_t* q32 = reinterpret_cast<const uint32_t*>(p.q);
+        const uint32_t* ra = q32 + (size_t(sa) * Hq + kvh * G + gid) * (D / 2);
+        const uint32_t* rb = q32 + (size_t(sb) * Hq + kvh * G + gid) * (D / 2);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            qa0[ks] = ra[ks * 8 + tig];
+            qa2[ks] = ra[ks * 8 + 4 + tig];
+            qa1[ks] = has_b ? rb[ks * 8 + tig] : 0u;
+            qa3[ks] = has_b ? rb[ks * 8 + 4 + tig] : 0u;
+        }
+    }
+    float o[D / 8][4];
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float ma = -INFINITY, mb = -INFINITY, la = 0.f, lb = 0.f;
+    const uint32_t release = warp == 0 ? 1 + C::kWarps - active : 1;
+
+    for (int jb = 0; jb < nb; ++jb) {
+        const uint32_t it = it_base + jb;
+        const int st = it % C::kStages;
+        if (ok) ok = __all_sync(kFullMask, mbar_wait(&full[st], (it / C::kStages) & 1, p.err));
+        if (!ok) continue;
+        const uint32_t kt = base + st * C::kStageBytes;
+        const uint32_t vt = kt + C::kTileBytes;
+
+        // S = q K^T for both sequences' rows: two 8-key column tiles
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const int mi = lane >> 3;
+            const int t = ((mi >> 1) << 3) + (lane & 7);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4(tile_addr(kt, t, ks * 2 + (mi & 1)), r0, r1, r2, r3);
+                mma16816(s0, qa0[ks], qa1[ks], qa2[ks], qa3[ks], r0, r1);
+                mma16816(s1, qa0[ks], qa1[ks], qa2[ks], qa3[ks], r2, r3);
+            }
+        }
+        // row gid (sa): keys 2tig, 2tig+1 (s0[0..1]) and 8+2tig, 9+2tig (s1[0..1]);
+        // row gid + 8 (sb): the same keys in s0[2..3], s1[2..3].  Every key is valid.
+        float va[4] = {s0[0], s0[1], s1[0], s1[1]};
+        float vb[4] = {s0[2], s0[3], s1[2], s1[3]};
+        float xa = -INFINITY, xb = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            va[i] *= p.scale_log2;
+            vb[i] *= p.scale_log2;
+            xa = fmaxf(xa, va[i]);
+            xb = fmaxf(xb, vb[i]);
+        }
+        xa = fmaxf(xa, __shfl_xor_sync(kFullMask, xa, 1));
+        xb = fmaxf(xb, __shfl_xor_sync(kFullMask, xb, 1));
+        xa = fmaxf(xa, __shfl_xor_sync(kFullMask, xa, 2));
+        xb = fmaxf(xb, __shfl_xor_sync(kFullMask, xb, 2));
+        const float na = fmaxf(ma, xa), nb2 = fmaxf(mb, xb);
+        const float aa = exp2f(ma - na), ab = exp2f(mb - nb2);
+        float pa[4], pb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            pa[i] = exp2f(va[i] - na);
+            pb[i] = exp2f(vb[i] - nb2);
+        }
+        la = la * aa + (pa[0] + pa[1]) + (pa[2] + pa[3]);
+        lb = lb * ab + (pb[0] + pb[1]) + (pb[2] + pb[3]);
+        if (__any_sync(kFullMask, aa != 1.f || ab != 1.f)) {
+#pragma unroll
+            for (int n = 0; n < D / 8; ++n) {
+                o[n][0] *= aa;
+                o[n][1] *= aa;
+                o[n][2] *= ab;
+                o[n][3] *= ab;
+            }
+        }
+        ma = na;
+        mb = nb2;
+
+        // O += P V with both sequences' rows of P as the A operand
+        const uint32_t p0 = pack2(pa[0], pa[1]), p1 = pack2(pb[0], pb[1]);
+        const uint32_t p2 = pack2(pa[2], pa[3]), p3 = pack2(pb[2], pb[3]);
+        {
+            const int mi = lane >> 3;
+            const int t = ((mi & 1) << 3) + (lane & 7);
+#pragma unroll
+            for (int pr2 = 0; pr2 < D / 16; ++pr2) {
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4_t(tile_addr(vt, t, pr2 * 2 + (mi >> 1)), r0, r1, r2, r3);
+                mma16816(o[2 * pr2], p0, p1, p2, p3, r0, r1);
+                mma16816(o[2 * pr2 + 1], p0, p1, p2, p3, r2, r3);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cnt(&empty[st], release);
+    }
+    if (!ok) return;
+
+    // per-row sums over the quad, then each sequence's partial (or output)
+    la += __shfl_xor_sync(kFullMask, la, 1);
+    lb += __shfl_xor_sync(kFullMask, lb, 1);
+    la += __shfl_xor_sync(kFullMask, la, 2);
+    lb += __shfl_xor_sync(kFullMask, lb, 2);
+    grouped_write<D, 0>(p, o, sa, kvh * G + gid, split, ma, la);
+    if (has_b) grouped_write<D, 1>(p, o, sb, kvh * G + gid, split, mb, lb);
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads, MmaCfg<D, G>::kMinBlocks)
     decode_split_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -146,7 +371,9 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads, MmaCfg<D, G>::kMinBloc
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            // a tile is released by its consumer warp, which arrives for all of
+            // them, or (grouped units) by every consumer warp once
+            mbar_init(&empty[s], C::kWarps);
         }
         for (int s = 0; s < C::kQSlots; ++s) {
             mbar_init(&q_full[s], 1);
@@ -175,7 +402,9 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads, MmaCfg<D, G>::kMinBloc
             const int2 item = p.items[u / Hkv];
             const int kvh = u % Hkv;
             const int ctx = p.context_lens[item.x];
-            const SplitSpan sp = split_span(ctx, item.y, p.window);
+            const int grouped = item.y >> kItemSplitBits;   // sequences reading this split
+            // (a grouped split is complete for every member: the first one's table serves all)
+            const SplitSpan sp = split_span(ctx, item.y & kItemSplitMask, p.window);
             const int b0 = sp.begin;
             const int nb = max(0, sp.end - b0);
             int my_blk = 0;
@@ -188,9 +417,13 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads, MmaCfg<D, G>::kMinBloc
                 const int qrow = p.query_start_loc ? p.query_start_loc[item.x] : item.x;
                 meta[2 * qs] = make_int4(item.x, item.y, ctx, kvh);
                 meta[2 * qs + 1] = make_int4(qrow, 0, 0, 0);
-                mbar_arrive_expect_tx(&q_full[qs], C::kQBytes);
-                bulk_g2s(qbuf + qs * C::kQBytes, p.q + (size_t(qrow) * Hq + kvh * G) * D, C::kQBytes,
-                         &q_full[qs]);
+                if (grouped) {
+                    mbar_arrive(&q_full[qs]);   // each consumer warp loads its members' q
+                } else {
+                    mbar_arrive_expect_tx(&q_full[qs], C::kQBytes);
+                    bulk_g2s(qbuf + qs * C::kQBytes, p.q + (size_t(qrow) * Hq + kvh * G) * D,
+                             C::kQBytes, &q_full[qs]);
+                }
             }
             __syncwarp();
             for (int j = 0; j < nb; ++j, ++it) {
@@ -236,11 +469,21 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads, MmaCfg<D, G>::kMinBloc
         const int qs = k % C::kQSlots;
         if (ok) ok = __all_sync(kFullMask, mbar_wait(&q_full[qs], (k / C::kQSlots) & 1, p.err));
         const int4 mt = meta[2 * qs];
-        const int seq = mt.x, split = mt.y, ctx = mt.z, kvh = mt.w;
+        const int seq = mt.x, split = mt.y & kItemSplitMask, ctx = mt.z, kvh = mt.w;
         const int qrow = meta[2 * qs + 1].x;
         const SplitSpan sp = split_span(ctx, split, p.window);
         const int b0 = sp.begin;
         const int nb = ok ? max(0, sp.end - b0) : 0;
+        if constexpr (G == 8) {
+            const int grouped = mt.y >> kItemSplitBits;
+            if (grouped) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&q_empty[qs]);
+                grouped_split<D>(p, base, full, empty, it_base, nb, seq, grouped, split, kvh, ok);
+                it_base += nb;
+                continue;
+            }
+        }
 
         // q fragments (A operand): row gid = query head gid of the group, rows >= G zero
         uint32_t qa0[D / 16], qa2[D / 16];
@@ -339,7 +582,7 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads, MmaCfg<D, G>::kMinBloc
             }
             if (nvalid < kBlockTokens || fvalid > 0) fence_proxy_async_shared();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[st]);
+            if (lane == 0) mbar_arrive_cnt(&empty[st], C::kWarps);
         }
         it_base += nb;
 
@@ -347,6 +590,10 @@ __global__ void __launch_bounds__(MmaCfg<D, G>::kThreads, MmaCfg<D, G>::kMinBloc
         float l_row = l_part;
         l_row += __shfl_xor_sync(kFullMask, l_row, 1);
         l_row += __shfl_xor_sync(kFullMask, l_row, 2);
+        if constexpr (G == 8) {
+            combine_pairwise<D>(p, comb, o, m_row, l_row, ok, sp.nsplit, seq, qrow, split, kvh);
+            continue;
+        }
         float* rec = comb + warp * C::kComb;
         if (gid < G) {
 #pragma unroll

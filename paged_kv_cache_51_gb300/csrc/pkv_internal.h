@@ -63,7 +63,16 @@ struct AttnArgs {
     int* err;
     bool pdl;            // decode kernels may start while the preceding prefill kernel runs
     int32_t window;      // sliding window in keys (0: none); tables in logical order
+    bool group_splits;   // decode call: group sequences that share a complete split
 };
+
+// Decode work items are int2 (seq, split word).  The split word holds the split
+// index in its low kItemSplitBits bits and, for a grouped item, the number of
+// consecutive sequences from `seq` (2 .. kMaxGroup) that read the split's 32
+// blocks block for block, above them (0: the item is one sequence's split).
+constexpr int kItemSplitBits = 26;
+constexpr int kItemSplitMask = (1 << kItemSplitBits) - 1;
+constexpr int kMaxGroup = 8;
 
 // Planning rates for the split of SMs between prefill chunks and decode rows
 // of one mixed batch (what this library's kernels sustain on GB300).
