@@ -742,9 +742,10 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(MergeParams p) {
         }
         const int cnt = min(32, n - k0);                    // the same in every lane
         const float* src = p.part_o + (base + k0) * D + lane * DPL;
-        for (int i = 0; i < cnt; i += kBatch) {
-            // all of the batch's rows in flight, then summed in split order
-            float ov[kBatch][DPL];
+        // the rows of a batch of splits are requested together; the next
+        // batch's requests go out before this one is summed (in split order)
+        float ov[2][kBatch][DPL];
+        auto fetch = [&](float(&dst)[kBatch][DPL], int i) {
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
                 if (i + u < cnt) {
@@ -752,20 +753,31 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(MergeParams p) {
                     const float* r = src + size_t(i + u) * D;
                     if constexpr (DPL == 4) {
                         const float4 v = __ldcs(reinterpret_cast<const float4*>(r));
-                        ov[u][0] = v.x; ov[u][1] = v.y; ov[u][2] = v.z; ov[u][3] = v.w;
+                        dst[u][0] = v.x; dst[u][1] = v.y; dst[u][2] = v.z; dst[u][3] = v.w;
                     } else {
                         const float2 v = __ldcs(reinterpret_cast<const float2*>(r));
-                        ov[u][0] = v.x; ov[u][1] = v.y;
+                        dst[u][0] = v.x; dst[u][1] = v.y;
                     }
                 }
             }
+        };
+        auto sum = [&](const float(&rows)[kBatch][DPL], int i) {
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
                 if (i + u < cnt) {
                     const float wi = __shfl_sync(kFull, w, i + u);
 #pragma unroll
-                    for (int d = 0; d < DPL; ++d) acc[d] = fmaf(wi, ov[u][d], acc[d]);
+                    for (int d = 0; d < DPL; ++d) acc[d] = fmaf(wi, rows[u][d], acc[d]);
                 }
+            }
+        };
+        fetch(ov[0], 0);
+        for (int i = 0; i < cnt; i += 2 * kBatch) {
+            if (i + kBatch < cnt) fetch(ov[1], i + kBatch);
+            sum(ov[0], i);
+            if (i + kBatch < cnt) {
+                if (i + 2 * kBatch < cnt) fetch(ov[0], i + 2 * kBatch);
+                sum(ov[1], i + kBatch);
             }
         }
     }
