@@ -333,7 +333,12 @@ PKV_API size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t nu
  * Long contexts are split into fixed spans of 512 tokens whose partial
  * (max, sum, output) states are merged in a second kernel; the split depends
  * only on the context length, so a sequence's result does not depend on the
- * rest of the batch.  num_seqs == 0 is a no-op: the descriptor and the sizes
+ * rest of the batch, with one exception: for groups of 8 query heads, a
+ * complete split whose 32 block ids a sequence shares with its neighbours in
+ * the batch (parallel-sampling branches of one prompt [Deploy §2.1 4.
+ * PageAttention: shared blocks]) is computed once for up to 8 of them, each
+ * tile read once per KV head, and rounds differently (within the same error
+ * bound) from the same split computed alone.  num_seqs == 0 is a no-op: the descriptor and the sizes
  * are checked, the pointers are not (zero-sized tensors may be null). */
 PKV_API int paged_attention_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
                            const pkv_cache_desc* desc, const int32_t* block_tables,

@@ -20,7 +20,12 @@
 //    decoding): a sequence's context is cut into fixed 512-token splits; each
 //    (split, kv head) is one work unit; partial (m, l, O) states are merged by
 //    a second kernel with the same alpha rescaling.  The split depends only on
-//    the context length, so results do not depend on the batch.
+//    the context length, so results do not depend on the batch (except where
+//    the planner groups sequences that read the same blocks, below).
+//  * Shared prompt blocks ("大模型部署.md" §2.1 4. PageAttention: parallel
+//    sampling shares a prompt's blocks by reference count): for groups of 8
+//    query heads, consecutive sequences whose complete split reads the same
+//    32 blocks get one work unit, so each shared tile is read once per KV head.
 //  * Persistent grid (a multiple of the SM count) over a work list that a
 //    one-CTA planner kernel builds on the device, so no host round trip.
 //  * Sliding window of W keys ("大模型部署.md" §2.1 block_sliding_window, with
