@@ -428,16 +428,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmap_v,
                    const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_o, PrefillParams p) {
-    // Launched right behind the planner (programmatic launch): wait for the plan.
-    // The planner gives the prefill chunks only as many SMs as their share of
-    // the batch's work; the other CTAs leave at once, and the decode kernel that
-    // follows in the stream may start right away on the SMs they free (it reads
-    // the plan without waiting, so the trigger comes after this grid's wait).
-    pdl_wait_prerequisites();
-    pdl_launch_dependents();
-    const int active = min(p.counters[2], int(gridDim.x));
-    if (int(blockIdx.x) >= active) return;
-
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;           // 1 KiB aligned for the swizzle
@@ -449,9 +439,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     float2* stat = reinterpret_cast<float2*>(smem + kStatOff);  // [set][half][row]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_units = p.n_items[0] * p.num_kv_heads;
 
-    // zero the operand area once so no stale bit pattern can be NaN
+    // Shared-memory set-up needs nothing from the plan, so it runs while the
+    // planner still works.  Zero the operand area once so no stale bit pattern
+    // can be NaN.
     for (int i = threadIdx.x; i < kStatOff / 16; i += kThreads)
         reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
@@ -480,6 +471,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
+
+    // Launched right behind the planner (programmatic launch): wait for the plan.
+    // The planner gives the prefill chunks only as many SMs as their share of
+    // the batch's work; the other CTAs leave at once, and the decode kernel that
+    // follows in the stream may start right away on the SMs they free (it reads
+    // the plan without waiting, so the trigger comes after this grid's wait).
+    pdl_wait_prerequisites();
+    pdl_launch_dependents();
+    const int active = min(p.counters[2], int(gridDim.x));
+    if (int(blockIdx.x) >= active) return;
+    const int n_units = p.n_items[0] * p.num_kv_heads;
+
     if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_slot)),
