@@ -517,13 +517,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             out_staged[qb] = false;
         };
-        // The next unit's ticket is taken when this unit's last K tile is issued,
-        // not when the unit starts: the units come longest first, and a CTA that
+        // A CTA's first unit is its own index (units come longest first, one for
+        // each active CTA, with no atomic before the first copies); later units
+        // come from the ticket, after them.  The next unit's ticket is taken when
+        // this unit's last K tile is issued, not when the unit starts: a CTA that
         // reserved its next unit at the start of a long one would take a long or
         // medium unit that a CTA finishing sooner should get (measured on the
         // SplitFuse chunks: CTAs ending at 33 and at 44 us).  The atomic's latency
         // still hides behind the unit's last products and epilogue.
-        int next = lane == 0 ? atomicAdd(p.ticket, 1) : 0;
+        int next = int(blockIdx.x);
         for (;; ++k) {
             const int slot = k % kUnitSlots;
             ok = ok && __all_sync(0xffffffffu, mbar_wait(&bars[B_U_EMPTY + slot],
@@ -564,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int st = kt % kKStages;
                 const int nb = min(kBlkPerTile, x.nblk - j * kBlkPerTile);
                 const int blk = ids.tile(j, lane);
-                if (j == x.n_tiles - 1 && lane == 0) next = atomicAdd(p.ticket, 1);
+                if (j == x.n_tiles - 1 && lane == 0) next = active + atomicAdd(p.ticket, 1);
                 ok = __all_sync(0xffffffffu,
                                 mbar_wait(&bars[B_S_FULL + st], ((kt / kKStages) & 1) ^ 1, p.err));
                 if (!ok || *abort_flag) {
