@@ -63,8 +63,9 @@ struct PlanParams {
     int32_t window;                   // sliding window in keys (0: none)
     int32_t group;                    // group sequences that share complete splits
     const int32_t* block_tables;      // read only when grouping
-    double kv_bytes_per_token;        // K + V bytes of one token, all KV heads
-    double flops_per_pair;            // QK^T + PV flops of one (query, key) pair, all query heads
+    float ns_per_token;               // decode: K + V bytes of a token (all KV heads) at the planning rate
+    float ns_per_pair;                // prefill: QK^T + PV flops of a (query, key) pair (all
+                                      // query heads) at the planning rate
     Workspace ws;
     int* err;
 };
@@ -307,31 +308,36 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
         warp_pairs[warp] = my_pairs;
     }
     __syncthreads();
-    if (tid == 0) {
-        if (p.query_start_loc && (q_first != 0 || q_last != p.num_query_tokens)) {
-            flag_error(p.err, PKV_DEV_BAD_QUERY_LAYOUT);
-            carry_d = 0;
-            carry_p = 0;
+    if (warp == 0) {
+        unsigned long long dec_tokens = warp_tok[lane], pre_pairs = warp_pairs[lane];
+#pragma unroll
+        for (int off = 16; off; off >>= 1) {
+            dec_tokens += __shfl_xor_sync(kFull, dec_tokens, off);
+            pre_pairs += __shfl_xor_sync(kFull, pre_pairs, off);
         }
-        unsigned long long dec_tokens = 0, pre_pairs = 0;
-        for (int w = 0; w < 32; ++w) {
-            dec_tokens += warp_tok[w];
-            pre_pairs += warp_pairs[w];
+        if (lane == 0) {
+            if (p.query_start_loc && (q_first != 0 || q_last != p.num_query_tokens)) {
+                flag_error(p.err, PKV_DEV_BAD_QUERY_LAYOUT);
+                carry_d = 0;
+                carry_p = 0;
+            }
+            p.ws.counters[0] = carry_d;
+            p.ws.counters[1] = min(carry_p, p.ws.max_prefill_items);
+            // SMs for the prefill chunks: their share of the estimated time, so
+            // that tensor-bound chunks and HBM-bound decode rows finish together
+            // (an estimate: single precision is plenty, and double precision
+            // arithmetic is slow on this GPU)
+            int sms_prefill = 0;
+            if (pre_pairs && carry_p) {
+                const float t_pre = float(pre_pairs) * p.ns_per_pair;
+                const float t_dec = float(dec_tokens) * p.ns_per_token;
+                sms_prefill = int(ceilf(float(p.num_sms) * (t_pre / (t_pre + t_dec))));
+                sms_prefill = max(1, min(p.num_sms, sms_prefill));
+            }
+            p.ws.counters[2] = sms_prefill;
+            p.ws.counters[3] = 0;  // decode unit ticket
+            p.ws.counters[4] = 0;  // prefill unit ticket
         }
-        p.ws.counters[0] = carry_d;
-        p.ws.counters[1] = min(carry_p, p.ws.max_prefill_items);
-        // SMs for the prefill chunks: their share of the estimated time, so that
-        // tensor-bound chunks and HBM-bound decode rows finish together
-        int sms_prefill = 0;
-        if (pre_pairs && carry_p) {
-            const double t_pre = double(pre_pairs) * p.flops_per_pair / kPrefillFlopsPerNs;
-            const double t_dec = double(dec_tokens) * p.kv_bytes_per_token / kDecodeBytesPerNs;
-            sms_prefill = int(ceil(p.num_sms * t_pre / (t_pre + t_dec)));
-            sms_prefill = max(1, min(p.num_sms, sms_prefill));
-        }
-        p.ws.counters[2] = sms_prefill;
-        p.ws.counters[3] = 0;  // decode unit ticket
-        p.ws.counters[4] = 0;  // prefill unit ticket
     }
     // Longest first: prefill units are taken from a ticket in item order, so the
     // items are reordered by descending key-tile count (a counting sort of the
@@ -380,9 +386,9 @@ int launch_plan(const AttnArgs& a) {
     p.group = a.group_splits && a.window == 0 && !a.query_start_loc &&
               decode_mma_eligible(a.desc) && a.desc->num_q_heads == 8 * a.desc->num_kv_heads;
     p.block_tables = a.block_tables;
-    p.kv_bytes_per_token =
-        2.0 * a.desc->num_kv_heads * a.desc->head_dim * double(elem_bytes(a.desc->dtype));
-    p.flops_per_pair = 4.0 * a.desc->head_dim * a.desc->num_q_heads;
+    p.ns_per_token = float(2.0 * a.desc->num_kv_heads * a.desc->head_dim *
+                           double(elem_bytes(a.desc->dtype)) / kDecodeBytesPerNs);
+    p.ns_per_pair = float(4.0 * a.desc->head_dim * a.desc->num_q_heads / kPrefillFlopsPerNs);
     p.ws = a.ws;
     p.err = a.err;
     return cuda_status(launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, a.stream, p));
