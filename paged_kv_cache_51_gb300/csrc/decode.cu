@@ -131,8 +131,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
     __shared__ int2 s_item[kSortItems];
     __shared__ int s_bucket[kSortItems];
     __shared__ int hist[kSortBuckets], cursor[kSortBuckets];
-    __shared__ int s_shared[kGroupSeqs];   // shared_splits of each sequence
+    __shared__ int s_shared[kGroupSeqs];   // shared_splits of each sequence (grouped
+                                           // decode batches) or the prefill rows' first
+                                           // items, lengths and contexts (one_pass)
     const bool group = p.group && p.num_seqs <= kGroupSeqs;
+    const bool one_pass = !group && p.num_seqs <= 1024;
+    static_assert(kGroupSeqs >= 3 * 1024, "three per-row arrays for one_pass");
     unsigned long long my_tok = 0, my_pairs = 0;   // this thread's work estimate
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int sortable = min(kSortItems, p.ws.max_prefill_items);
@@ -272,23 +276,49 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
         } else {
             for (int k = 0; k < nd; ++k) p.ws.items[before_d + k] = make_int2(s, first_split + k);
         }
-        for (int k = 0; k < np; ++k) {
-            const int idx = before_p + k;
-            if (idx < p.ws.max_prefill_items) p.ws.prefill_items[idx] = make_int2(s, k);
+        // Prefill item k of sequence s: recorded for the longest-first reorder
+        // (its bucket: the item's key tiles, from the tile of its first token's
+        // first key to its last token's key) and written in batch order.
+        auto prefill_item = [&](int idx, int s_, int k, int qlen_, int ctx_) {
+            if (idx < p.ws.max_prefill_items) p.ws.prefill_items[idx] = make_int2(s_, k);
             if (idx < sortable) {
-                // key tiles of the item: from the tile of its first token's first
-                // key to its last token's key
                 const int t0 = k * p.tokens_per_tile;
-                const int nt = min(p.tokens_per_tile, qlen - t0);
-                const int n_keys = ctx - qlen + t0 + nt;
+                const int nt = min(p.tokens_per_tile, qlen_ - t0);
+                const int n_keys = ctx_ - qlen_ + t0 + nt;
                 const int key0 =
-                    window_first_key(ctx - qlen + t0, p.window) / kPrefillKeys * kPrefillKeys;
+                    window_first_key(ctx_ - qlen_ + t0, p.window) / kPrefillKeys * kPrefillKeys;
                 const int tiles = (n_keys - key0 + kPrefillKeys - 1) / kPrefillKeys;
                 const int b = kSortBuckets - 1 - min(tiles, kSortBuckets - 1);   // descending
-                s_item[idx] = make_int2(s, k);
+                s_item[idx] = make_int2(s_, k);
                 s_bucket[idx] = b;
                 atomicAdd(&hist[b], 1);
             }
+        };
+        if (one_pass) {
+            // a batch of up to 1024 rows: the items are spread over all threads
+            // (a chunk's items would otherwise be one thread's serial loop); the
+            // owner of item idx is the last row whose first item is <= idx
+            int* s_first = s_shared;                  // free: no grouping with prefill rows
+            int* s_qlen = s_shared + 1024;
+            int* s_ctx = s_shared + 2048;
+            if (s < p.num_seqs) {
+                s_first[s] = before_p;
+                s_qlen[s] = qlen;
+                s_ctx[s] = ctx;
+            }
+            __syncthreads();
+            const int total_p = warp_p[31];
+            for (int idx = tid; idx < total_p; idx += 1024) {
+                int lo = 0, hi = p.num_seqs - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (s_first[mid] <= idx) lo = mid;
+                    else hi = mid - 1;
+                }
+                prefill_item(idx, lo, idx - s_first[lo], s_qlen[lo], s_ctx[lo]);
+            }
+        } else {
+            for (int k = 0; k < np; ++k) prefill_item(before_p + k, s, k, qlen, ctx);
         }
         __syncthreads();
         if (tid == 0) {
