@@ -722,35 +722,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (pv) {
-                    // P of both key halves, V, and (first tile of a unit) the previous
-                    // unit's epilogue has read O
+                    // P of both key halves (which the softmax warps publish only once
+                    // the tile's V has landed, so this one check covers V too), and
+                    // (first tile of a unit) the previous unit's epilogue has read O
                     ok = mbar_wait(&bars[B_P_FULL + (t & 1)], (t >> 1) & 1, p.err) &&
-                         mbar_wait(&bars[B_V_FULL + t % kVStages], (t / kVStages) & 1, p.err) &&
                          (!t0 || mbar_wait(&bars[B_O_EMPTY], ((unit_par_bits >> (t & 3)) & 1u) ^ 1u,
                                            p.err));
                     if (!ok) break;
                 }
-                bool pv_out = !pv;
-                if (qk) {
-                    const bool ready = (!q_first || mbar_test(&bars[B_Q_FULL + qb], (cur_unit >> 1) & 1)) &&
-                                       mbar_test(&bars[B_K_FULL + q % kKStages], (q / kKStages) & 1);
-                    if (!ready) {
-                        if (!pv_out) {
-                            tc_after();
-                            umma_ts8(tmem + kOCol, tmem + (t & 1) * kKeys, vd, kIdescPV, t0 ? 0u : 1u);
-                            umma_commit(&bars[B_O_DONE + (t & 1)]);
-                            pv_out = true;
-                        }
-                        ok = (!q_first ||
-                              mbar_wait(&bars[B_Q_FULL + qb], (cur_unit >> 1) & 1, p.err)) &&
-                             mbar_wait(&bars[B_K_FULL + q % kKStages], (q / kKStages) & 1, p.err);
-                        if (!ok) break;
-                    }
-                }
-                tc_after();
-                if (!pv_out) {
+                // P V first (its inputs are checked above), then the Q K^T side's
+                // inputs, whose check overlaps the queued P V products
+                if (pv) {
+                    tc_after();
                     umma_ts8(tmem + kOCol, tmem + (t & 1) * kKeys, vd, kIdescPV, t0 ? 0u : 1u);
                     umma_commit(&bars[B_O_DONE + (t & 1)]);
+                }
+                if (qk) {
+                    ok = (!q_first ||
+                          mbar_wait(&bars[B_Q_FULL + qb], (cur_unit >> 1) & 1, p.err)) &&
+                         mbar_wait(&bars[B_K_FULL + q % kKStages], (q / kKStages) & 1, p.err);
+                    if (!ok) break;
+                    tc_after();
                 }
                 if (pv) ++n_pv;
                 if (qk) {
@@ -916,9 +908,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     fence_async_smem();   // the zeroed V rows, before the P V reads them
                 }
+                // the tile's V has landed before P is published (the issuer checks
+                // P alone; the softmax warps have time to spare for this check)
+                if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_V_FULL + g % kVStages],
+                                                               (g / kVStages) & 1, p.err));
                 tmem_wait_st();
                 tc_before();
                 __syncwarp();
+                if (!ok) break;
                 if (lane == 0) mbar_arrive(&bars[B_P_FULL + (g & 1)]);
             }
             if (!ok) break;
