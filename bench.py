@@ -445,6 +445,8 @@ def configs_summary(steps, warmup, with_int8=True):
                 "logical bytes: every branch's reads of its shared prompt blocks count")
             r["attention"]["dram_bytes_ncu"] = dram
             r["attention"]["dram_gbs"] = (dram / (attn_ms * 1e-3) / 1e9) if dram else None
+            # the bar for this batch is stated on DRAM bytes (ncu), not logical ones
+            r["attention"]["dram_frac"] = (dram / (attn_ms * 1e-3) / 1e9 / bw) if dram else None
         if with_int8:
             step.run()
             r["int8"] = int8_decode_summary(w, dc, step, steps, warmup, attn_ms, False)
