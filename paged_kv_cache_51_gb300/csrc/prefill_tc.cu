@@ -28,18 +28,21 @@
 // swizzled MN-major layout (V); TMA tensor copies write K and V blocks straight
 // into that layout, one (block, 64-dim half) box of 16 x 128 B per copy.
 //
-// Warp roles (352 threads, one CTA per SM, persistent over work units):
+// Warp roles (384 threads, one CTA per SM, persistent over work units):
 //   warps 0-7  softmax: two threads per query row, one per 64-key half of each
-//              key tile.  Each half keeps its own running max and sum and its
-//              own O accumulator in TMEM (O = O_0 + O_1 after rescaling, like a
-//              split over keys), so the two never exchange data inside the
-//              loop.  A thread reads its 64 scores from TMEM, masks, computes P
-//              (bf16) and writes it back into TMEM over its own scores; the
-//              P V product reads P from there.  S is double-buffered, so P is
-//              too: the softmax of the next key tile runs while the previous
-//              P V product is still executing.  O is rescaled only when the
-//              running max grows by more than 2^8 (the one case that waits for
-//              the previous P V).  The epilogue merges the halves; a full
+//              key tile (warps w and w + 4 hold the same rows).  A thread reads
+//              its 64 scores from TMEM, masks them, exchanges its tile maximum
+//              with the other half's thread through shared memory (both then
+//              hold the same running max) and with that frees the S buffer for
+//              the Q K^T two tiles on; it computes P (bf16) into a P buffer of
+//              its own in TMEM and keeps a partial row sum.  The P V product reads
+//              P from there and accumulates both halves into one O.  S and P
+//              are double-buffered, so a Q K^T waits only until the softmax has
+//              loaded the scores it overwrites, not until their P V has run,
+//              and the softmax of the next key tile overlaps the previous
+//              products.  O is rescaled (each thread its 64 dims) only when the
+//              running max grows by more than 2^8, the one case that waits for
+//              the previous P V.  The epilogue adds the halves' sums; a full
 //              unit's bf16 output tile is staged in the unit's Q buffer (the
 //              TMA box layout) and leaves by two TMA tensor stores, so the warps
 //              go on to the next unit at once (128 rows of scattered 16-byte
@@ -52,10 +55,24 @@
 //              tile into a 2-stage K ring; a K stage is released as soon as its
 //              Q K^T product is done; sends staged output tiles out by TMA
 //   warp 9     TMA producer for V: a 2-stage V ring released by the P V product
-//   warp 10    TMEM owner and MMA issuer (one thread issues tcgen05.mma): a step
-//              issues P V of key tile q - 2 and Q K^T of key tile q as bursts
-//              behind one group of waits, so the tensor pipe works on those
-//              while the softmax runs on tile q - 1 (across units as well)
+//   warp 10    TMEM owner and Q K^T issuer (one thread issues tcgen05.mma)
+//   warp 11    P V issuer (one thread)
+//              A thread issuing tcgen05.mma is held for the length of each
+//              product, and every instruction that another warp of its SM
+//              sub-partition (warp index mod 4) issues meanwhile delays the
+//              next product: measured with one issuing thread and busy warps
+//              beside it, a 128 x 128 x 16 product takes 64 cycles alone, 79
+//              beside two warps of TMEM loads and stores, 126 beside two warps
+//              of FMAs, and 64 whatever runs on the other three
+//              sub-partitions.  Each sub-partition holds two softmax warps (a
+//              warp reads only its own quarter of TMEM's lanes), so the two
+//              products go out from two sub-partitions (2 and 3), each carrying
+//              half the issue work.  Tensor-core instructions of one thread run
+//              in issue order, but two threads' need not: a Q K^T into an S
+//              buffer waits until the scores it replaces (two tiles
+//              earlier) has been loaded by the softmax.  The pipe works on
+//              Q K^T of tile q + 1 and P V of tile q - 1 while the softmax runs
+//              on tile q (across units as well).
 // Every wait is bounded; on a timeout the kernel records an error, stops
 // issuing work, drains its copies and MMAs and frees TMEM before it returns.
 #include <cuda.h>
@@ -83,23 +100,26 @@ constexpr int kKStages = 2;
 constexpr int kVStages = 2;
 constexpr int kQBufs = 2;
 static_assert(kKStages == 2 && kVStages == 2,
-              "the rings are released through the two S/P buffers' barriers");
+              "the rings are released through the two S and P buffers' barriers");
 constexpr int kSub = kRows * 128;            // one 64-column half of a 128-row operand (16 KiB)
 constexpr int kQBytes = 2 * kSub;            // one Q tile: 2 halves (dims 0-63, 64-127)
 constexpr int kKBytes = 2 * kKeys * 128;     // one K or V tile (2 halves of 128 key rows x 128 B)
 constexpr int kQOff = 0;
 constexpr int kKOff = kQOff + kQBufs * kQBytes;
 constexpr int kVOff = kKOff + kKStages * kKBytes;
-constexpr int kStatOff = kVOff + kVStages * kKBytes;  // (m, l) per half and row, 2 sets
-constexpr int kBarOff = kStatOff + 2 * 2 * kRows * 8;
+constexpr int kStatOff = kVOff + kVStages * kKBytes;  // l per half and row, 2 sets
+constexpr int kXmOff = kStatOff + 2 * 2 * kRows * 4;  // tile maxima per half and row, 2 sets
+constexpr int kBarOff = kXmOff + 2 * 2 * kRows * 4;
 constexpr int kSmemBytes = kBarOff + 1024 + 1024;  // barriers, unit ring + 1 KiB alignment slack
 constexpr int kSoftWarps = 8;
 constexpr int kKProducerWarp = 8;
 constexpr int kVProducerWarp = 9;
-constexpr int kMmaWarp = 10;
-constexpr int kThreads = 352;
-constexpr uint32_t kTmemCols = 512;          // S/P double buffer (2 x 128) + O halves (2 x 128)
-constexpr uint32_t kOCol = 256;              // O half h at kOCol + 128 h
+constexpr int kMmaWarp = 10;                 // TMEM owner, Q K^T issuer
+constexpr int kPvWarp = 11;                  // P V issuer
+constexpr int kThreads = 384;
+constexpr uint32_t kTmemCols = 512;          // S (2 x 128) + P (2 x 64) + O (128)
+constexpr uint32_t kPCol = 256;              // P buffer b at kPCol + 64 b (bf16 pairs)
+constexpr uint32_t kOCol = 384;              // O: 128 columns (fp32, one per dim)
 constexpr float kRescaleThreshold = 8.0f;    // log2 units: rescale O only when max grows > 2^8
 constexpr int kBoxBytes = kBlockTokens * 128;  // one TMA box: 16 rows x 64 bf16
 
@@ -107,22 +127,25 @@ constexpr int kBoxBytes = kBlockTokens * 128;  // one TMA box: 16 rows x 64 bf16
 enum {
     B_K_FULL = 0,
     // A K stage is free once the Q K^T that read it has completed, and a V stage
-    // once its P V has: with two K stages, two V stages and two S/P buffers,
-    // stage i of each ring belongs to the tiles of S/P buffer i, so the
+    // once its P V has: with two K stages, two V stages and two S and two P
+    // buffers, stage i of each ring belongs to the tiles of buffer i, so the
     // producers wait on B_S_FULL and B_O_DONE (the next phase of either needs a
     // tile the waiting producer has not loaded yet, so a wait cannot alias).
     B_V_FULL = B_K_FULL + kKStages,
     B_S_FULL = B_V_FULL + kVStages,
-    B_P_FULL = B_S_FULL + 2,        // [S/P buffer]: every softmax warp has written its P
-    B_O_DONE = B_P_FULL + 2,        // [S/P buffer]: that buffer's P V has completed
+    B_S_EMPTY = B_S_FULL + 2,       // [S buffer]: every softmax warp has loaded its scores
+    B_P_FULL = B_S_EMPTY + 2,       // [P buffer]: every softmax warp has written its P
+    B_O_DONE = B_P_FULL + 2,        // [P buffer]: that buffer's P V has completed
     B_Q_FULL = B_O_DONE + 2,        // [Q buffer]
     B_Q_EMPTY = B_Q_FULL + kQBufs,  // [Q buffer]: every softmax warp has finished its unit's
                                     // epilogue (output staged there or written directly)
     B_U_READY = B_Q_EMPTY + kQBufs, // [unit slot]
     B_U_EMPTY = B_U_READY + 4,      // [unit slot]
     B_O_EMPTY = B_U_EMPTY + 4,
-    B_STAT,                         // both halves' (m, l) of the current unit are published
-    B_DRAIN,
+    B_STAT,                         // both halves' l of the current unit are published
+    B_XM,                           // [lane quarter]: both halves' tile maxima are published
+    B_DRAIN = B_XM + 4,             // the Q K^T issuer's products have completed
+    B_DRAIN_PV,                     // the P V issuer's products have completed
     B_COUNT
 };
 
@@ -188,19 +211,21 @@ __device__ __forceinline__ void umma_ss8(uint32_t d, const uint64_t (&a)[8], con
 // b[4 h + kk].  The first step of each half accumulates only if `acc` is set.
 __device__ __forceinline__ void umma_ts8(uint32_t d, uint32_t a, const uint64_t (&b)[8],
                                          uint32_t idesc, uint32_t acc) {
+    // eight K = 16 steps over 128 keys (A from TMEM, 8 columns of bf16 pairs per
+    // step) into one accumulator; the first overwrites it when acc == 0
     asm volatile(
-        "{\n .reg .pred pf, pa;\n .reg .b32 d1, a1, a2, a3, a4, a5, a6, a7;\n"
+        "{\n .reg .pred pf, pa;\n .reg .b32 a1, a2, a3, a4, a5, a6, a7;\n"
         " setp.ne.b32 pf, %10, 0;\n setp.eq.b32 pa, %10, %10;\n"
-        " add.u32 d1, %0, 128;\n add.u32 a1, %1, 8;\n add.u32 a2, %1, 16;\n add.u32 a3, %1, 24;\n"
-        " add.u32 a4, %1, 64;\n add.u32 a5, %1, 72;\n add.u32 a6, %1, 80;\n add.u32 a7, %1, 88;\n"
+        " add.u32 a1, %1, 8;\n add.u32 a2, %1, 16;\n add.u32 a3, %1, 24;\n add.u32 a4, %1, 32;\n"
+        " add.u32 a5, %1, 40;\n add.u32 a6, %1, 48;\n add.u32 a7, %1, 56;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %11, pf;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], %3, %11, pa;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], %4, %11, pa;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], %5, %11, pa;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [d1], [a4], %6, %11, pf;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [d1], [a5], %7, %11, pa;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [d1], [a6], %8, %11, pa;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [d1], [a7], %9, %11, pa;\n}\n" ::"r"(d),
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], %6, %11, pa;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], %7, %11, pa;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], %8, %11, pa;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], %9, %11, pa;\n}\n" ::"r"(d),
         "r"(a), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]),
         "l"(b[7]), "r"(acc), "r"(idesc)
         : "memory");
@@ -360,7 +385,8 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
     return r;
 }
 
-// Whether the phase with the given parity has completed, without waiting.
+// Whether the phase with the given parity has completed, without waiting (a
+// test issued early, whose latency overlaps the work before its result is used).
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -398,10 +424,10 @@ struct BlockIds {
 };
 
 // Unit ring: the K producer takes units from the ticket (the planner ordered
-// the items longest first) and publishes them; the V producer, the MMA issuer
-// and the 8 softmax warps read each one and release its slot.
+// the items longest first) and publishes them; the V producer, the two MMA
+// issuers and the 8 softmax warps read each one and release its slot.
 constexpr int kUnitSlots = 4;
-constexpr int kUnitReaders = 1 + 1 + kSoftWarps;
+constexpr int kUnitReaders = 1 + 2 + kSoftWarps;
 
 // A published unit: its id (-1: no more work) and geometry, computed once by
 // the K producer so the other roles start a unit without global loads.
@@ -409,6 +435,8 @@ struct UnitSlot {
     int u;
     Unit x;
 };
+// barriers, TMEM address, abort flag and unit ring share the 1 KiB after kBarOff
+static_assert(B_COUNT * 8 + 16 + kUnitSlots * sizeof(UnitSlot) <= 1024, "barrier area");
 
 __device__ __forceinline__ int unit_read(uint64_t* bars, const UnitSlot* ring, uint32_t k,
                                          int* err, bool& ok, Unit& x) {
@@ -436,7 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + B_COUNT * 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + B_COUNT * 8 + 4);
     UnitSlot* unit_ring = reinterpret_cast<UnitSlot*>(smem + kBarOff + B_COUNT * 8 + 16);
-    float2* stat = reinterpret_cast<float2*>(smem + kStatOff);  // [set][half][row]
+    float* stat = reinterpret_cast<float*>(smem + kStatOff);  // [set][half][row]
+    float* xm = reinterpret_cast<float*>(smem + kXmOff);      // [tile parity][half][row]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -456,7 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars[B_Q_FULL + s], 1);
             mbar_init(&bars[B_Q_EMPTY + s], kSoftWarps);
         }
-        for (int s = 0; s < 2; ++s) mbar_init(&bars[B_S_FULL + s], 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars[B_S_FULL + s], 1);
+            mbar_init(&bars[B_S_EMPTY + s], kSoftWarps);
+        }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars[B_P_FULL + s], kSoftWarps);
             mbar_init(&bars[B_O_DONE + s], 1);
@@ -467,7 +499,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&bars[B_O_EMPTY], kSoftWarps);
         mbar_init(&bars[B_STAT], kSoftWarps);
+        for (int s = 0; s < 4; ++s) mbar_init(&bars[B_XM + s], 2);
         mbar_init(&bars[B_DRAIN], 1);
+        mbar_init(&bars[B_DRAIN_PV], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -651,20 +685,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == kMmaWarp) {
-        // ------------------------------ MMA issuer ------------------------------
-        // Key tiles are numbered over the CTA's whole sequence of units.  A step
-        // issues P V of tile q - 2 and Q K^T of tile q: S/P buffer q & 1 held
-        // P(q - 2), which the P V reads before the Q K^T overwrites it
-        // (tensor-core instructions run in issue order), while the softmax works
-        // on S(q - 1); after the last Q K^T the remaining P V go out alone.  The pipe idles for every instruction this thread runs
-        // between two products, so the step's waits come first, then one fence
-        // and the products as bursts of eight; descriptors come from per-CTA
-        // bases plus constant offsets (shared-memory addresses stay below
-        // 256 KiB: adding to the 14-bit start field never carries).  When the
-        // Q K^T side is not ready yet, the P V goes out first: the next unit's Q
-        // may be waiting for the epilogue that this P V completes.  The abort
-        // flag is read once per unit; a wait that can no longer be satisfied
-        // ends on its time limit.
+        // ---------------------------- Q K^T issuer ----------------------------
+        // Key tiles are numbered over the CTA's whole sequence of units.  Q K^T
+        // of tile q writes S buffer q & 1, which held S(q - 2): it waits until
+        // every softmax warp has loaded those scores, then for its K stage and
+        // (first tile of a unit) its Q buffer.  The pipe
+        // idles for every instruction this thread runs between two products,
+        // so the waits come first, then one fence and the eight products in one
+        // burst; descriptors come from per-CTA bases plus constant offsets
+        // (shared-memory addresses stay below 256 KiB: adding to the 14-bit
+        // start field never carries).  The abort flag is read once per unit; a
+        // wait that can no longer be satisfied ends on its time limit.
         if (lane == 0) {
             bool ok = true;
             uint64_t qd[8];  // Q buffer 0: K-major, 128-byte swizzle
@@ -675,90 +706,72 @@ __global__ void __launch_bounds__(kThreads, 1)
                     qd[kk] = q0 + uint64_t(((kk >> 2) * kSub + (kk & 3) * 32) >> 4);
             }
             const uint64_t kd_base = sdesc(base + kKOff, 16, 1024);
-            const uint64_t vd_base = sdesc(base + kVOff, kKeys * 128, 1024);
-            // per tile, bit (tile & 3) (a P V trails its Q K^T by two steps):
-            // whether it is its unit's first tile, and its unit's parity
-            uint32_t first_bits = 0, unit_par_bits = 0;
-            uint32_t k_next = 0;                 // next unit to read
-            uint32_t cur_unit = 0;               // unit of the Q K^T cursor
-            int cur_j = 0, cur_n = 0;            // its next tile, and its tile count
-            bool more = true;                    // units may remain
-            uint32_t n_qk = 0;                   // Q K^T products issued (tiles 0 .. n_qk - 1)
-            uint32_t n_pv = 0;                   // P V products issued
-            for (;;) {
-                if (ok && more && cur_j == cur_n) {
-                    Unit x;
-                    const int u = unit_read(bars, unit_ring, k_next, p.err, ok, x);
-                    mbar_arrive(&bars[B_U_EMPTY + k_next % kUnitSlots]);
-                    if (u < 0 || !ok || *abort_flag) {
-                        more = false;
-                    } else {
-                        cur_unit = k_next++;
-                        cur_j = 0;
-                        cur_n = x.n_tiles;
-                    }
-                }
-                const bool qk = ok && more && cur_j < cur_n;
-                // P V trails Q K^T by two tiles while products flow; once the
-                // units run out, the remaining ones go out in the next steps
-                const bool pv = ok && n_pv < n_qk && (!qk || n_qk >= n_pv + 2);
-                if (!qk && !pv) break;
-                const uint32_t t = n_pv;         // the P V tile
-                const uint32_t q = n_qk;         // the Q K^T tile
-                const bool t0 = pv && ((first_bits >> (t & 3)) & 1u);
-                const bool q_first = qk && cur_j == 0;
-                const uint32_t qb = cur_unit & 1;
-                // descriptors of both bursts, before any wait
-                uint64_t vd[8], qa[8], kd[8];
-                {
-                    const uint64_t v0 = vd_base + uint64_t((t % kVStages) * (kKBytes >> 4));
+            uint32_t q = 0;                      // Q K^T tiles issued
+            for (uint32_t k = 0;; ++k) {
+                Unit x;
+                const int u = unit_read(bars, unit_ring, k, p.err, ok, x);
+                mbar_arrive(&bars[B_U_EMPTY + k % kUnitSlots]);
+                if (u < 0 || !ok || *abort_flag) break;
+                const uint32_t qb = k & 1;
+                const uint64_t qoff = uint64_t(qb) * (kQBytes >> 4);
+                for (int j = 0; j < x.n_tiles; ++j, ++q) {
+                    uint64_t qa[8], kd[8];
                     const uint64_t k0 = kd_base + uint64_t((q % kKStages) * (kKBytes >> 4));
-                    const uint64_t qoff = uint64_t(qb) * (kQBytes >> 4);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        vd[i] = v0 + uint64_t((i * 16 * 128) >> 4);
                         qa[i] = qd[i] + qoff;
                         kd[i] = k0 + uint64_t(((i >> 2) * (kKeys * 128) + (i & 3) * 32) >> 4);
                     }
-                }
-                if (pv) {
-                    // P of both key halves (which the softmax warps publish only once
-                    // the tile's V has landed, so this one check covers V too), and
-                    // (first tile of a unit) the previous unit's epilogue has read O
-                    ok = mbar_wait(&bars[B_P_FULL + (t & 1)], (t >> 1) & 1, p.err) &&
-                         (!t0 || mbar_wait(&bars[B_O_EMPTY], ((unit_par_bits >> (t & 3)) & 1u) ^ 1u,
-                                           p.err));
-                    if (!ok) break;
-                }
-                // P V first (its inputs are checked above), then the Q K^T side's
-                // inputs, whose check overlaps the queued P V products
-                if (pv) {
-                    tc_after();
-                    umma_ts8(tmem + kOCol, tmem + (t & 1) * kKeys, vd, kIdescPV, t0 ? 0u : 1u);
-                    umma_commit(&bars[B_O_DONE + (t & 1)]);
-                }
-                if (qk) {
-                    ok = (!q_first ||
-                          mbar_wait(&bars[B_Q_FULL + qb], (cur_unit >> 1) & 1, p.err)) &&
+                    ok = (q < 2 || mbar_wait(&bars[B_S_EMPTY + (q & 1)], ((q - 2) >> 1) & 1, p.err)) &&
+                         (j != 0 || mbar_wait(&bars[B_Q_FULL + qb], (k >> 1) & 1, p.err)) &&
                          mbar_wait(&bars[B_K_FULL + q % kKStages], (q / kKStages) & 1, p.err);
                     if (!ok) break;
                     tc_after();
-                }
-                if (pv) ++n_pv;
-                if (qk) {
                     umma_ss8(tmem + (q & 1) * kKeys, qa, kd, kIdescQK);
                     umma_commit(&bars[B_S_FULL + (q & 1)]);
-                    const uint32_t bit = 1u << (q & 3);
-                    first_bits = q_first ? (first_bits | bit) : (first_bits & ~bit);
-                    unit_par_bits = (cur_unit & 1) ? (unit_par_bits | bit) : (unit_par_bits & ~bit);
-                    ++n_qk;
-                    ++cur_j;
                 }
+                if (!ok) break;
             }
             if (!ok) *abort_flag = 1;
             // wait until every MMA issued here has completed before TMEM is freed
             umma_commit(&bars[B_DRAIN]);
             mbar_wait(&bars[B_DRAIN], 0, p.err);
+        }
+        __syncwarp();
+    } else if (warp == kPvWarp) {
+        // ----------------------------- P V issuer -----------------------------
+        // P V of tile t (both 64-key halves into the one O accumulator) once the
+        // softmax warps have published P(t), the tile's V has landed and, for a
+        // unit's first tile, the previous unit's epilogue has read O (its first
+        // products overwrite O).  Products of this thread run in order, so a
+        // completed O_DONE of tile t also covers every earlier P V.
+        if (lane == 0) {
+            bool ok = true;
+            const uint64_t vd_base = sdesc(base + kVOff, kKeys * 128, 1024);
+            uint32_t t = 0;                      // P V tiles issued
+            for (uint32_t k = 0;; ++k) {
+                Unit x;
+                const int u = unit_read(bars, unit_ring, k, p.err, ok, x);
+                mbar_arrive(&bars[B_U_EMPTY + k % kUnitSlots]);
+                if (u < 0 || !ok || *abort_flag) break;
+                for (int j = 0; j < x.n_tiles; ++j, ++t) {
+                    uint64_t vd[8];
+                    const uint64_t v0 = vd_base + uint64_t((t % kVStages) * (kKBytes >> 4));
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) vd[i] = v0 + uint64_t((i * 16 * 128) >> 4);
+                    ok = mbar_wait(&bars[B_P_FULL + (t & 1)], (t >> 1) & 1, p.err) &&
+                         mbar_wait(&bars[B_V_FULL + t % kVStages], (t / kVStages) & 1, p.err) &&
+                         (j != 0 || mbar_wait(&bars[B_O_EMPTY], (k & 1) ^ 1u, p.err));
+                    if (!ok) break;
+                    tc_after();
+                    umma_ts8(tmem + kOCol, tmem + kPCol + (t & 1) * 64, vd, kIdescPV, j == 0 ? 0u : 1u);
+                    umma_commit(&bars[B_O_DONE + (t & 1)]);
+                }
+                if (!ok) break;
+            }
+            if (!ok) *abort_flag = 1;
+            umma_commit(&bars[B_DRAIN_PV]);
+            mbar_wait(&bars[B_DRAIN_PV], 0, p.err);
         }
         __syncwarp();
     } else {
@@ -774,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int u = unit_read(bars, unit_ring, k, p.err, ok, x);
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_U_EMPTY + k % kUnitSlots]);
-            if (u < 0 || !ok) break;
+            if (u < 0 || !ok || *abort_flag) break;
             const int tok = r / G, g_head = r % G;
             const bool row_valid = tok < x.nt;
             const int t = x.t0 + tok;
@@ -787,12 +800,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < x.n_tiles; ++j) {
                 const uint32_t g = kt + j;
-                if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_S_FULL + (g & 1)],
-                                                               (g >> 1) & 1, p.err));
-                if (!ok || *abort_flag) {
-                    ok = false;
-                    break;
-                }
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_S_FULL + (g & 1)], (g >> 1) & 1, p.err));
+                if (!ok) break;
                 tc_after();
                 float s[64];
                 {
@@ -806,6 +815,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         s[32 + i] = __uint_as_float(v1[i]);
                     }
                 }
+                // whether the P V of tile g - 2 (the last reader of P buffer g & 1)
+                // has completed, tested without waiting (it nearly always has); the
+                // bounded wait runs before P is stored only if it has not
+                const bool p_free = g < 2 || mbar_test(&bars[B_O_DONE + (g & 1)], ((g - 2) >> 1) & 1);
 
                 // mask keys beyond this row's causal limit and below its window;
                 // max on the raw scores
@@ -827,8 +840,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[i + 56]);
                 const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]),
-                                       fmaxf(mx8[6], mx8[7]));
-                const float m_new = fmaxf(m, mx * p.scale_log2);
+                                       fmaxf(mx8[6], mx8[7])) * p.scale_log2;
+                // the row's two halves share one O, so they share the running max:
+                // exchange this tile's maxima with the other half's thread (warp
+                // warp ^ 4, same TMEM lanes) through shared memory, a slot per tile
+                // parity; both then take identical decisions from identical values
+                float* xslot = xm + (g & 1) * 2 * kRows;
+                xslot[h * kRows + r] = mx;
+                // the scores are in registers: Q K^T of tile g + 2 may overwrite them
+                tc_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bars[B_XM + (warp & 3)]);
+                    mbar_arrive(&bars[B_S_EMPTY + (g & 1)]);
+                }
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_XM + (warp & 3)], g & 1, p.err));
+                if (!ok) break;
+                const float m_new = fmaxf(m, fmaxf(mx, xslot[(h ^ 1) * kRows + r]));
                 const bool need = m_new > m + kRescaleThreshold;  // first visible keys included
                 float alpha = 1.f;
                 if (need) {
@@ -855,18 +883,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                      ((sum4[2].x + sum4[2].y) + (sum4[3].x + sum4[3].y));
                 const bool warp_need = __any_sync(0xffffffffu, need);
                 if (j > 0 && warp_need) {
-                    // rescale O_h: wait for the previous P V of this half (buffer
-                    // (g - 1) & 1; that buffer's older products have completed,
-                    // since S(g) is full and was issued after them)
+                    // rescale O_h: wait for the previous P V (buffer (g - 1) & 1;
+                    // the P V products run in issue order on one thread, so every
+                    // older one has completed too)
                     const uint32_t gp = g - 1;
                     ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE + (gp & 1)],
                                                            (gp >> 1) & 1, p.err));
                     if (!ok) break;
                     tc_after();
+                    // this thread's 64 dims of the row's O (the other half's thread
+                    // takes the other 64, with the same alpha)
 #pragma unroll 1
-                    for (int c4 = 0; c4 < 4; ++c4) {
+                    for (int c2 = 0; c2 < 2; ++c2) {
                         uint32_t v[32];
-                        const uint32_t ta = tmem + lane_base + kOCol + h * 128 + c4 * 32;
+                        const uint32_t ta = tmem + lane_base + kOCol + h * 64 + c2 * 32;
                         tmem_ld32(ta, v);
                         tmem_wait_ld();
 #pragma unroll
@@ -875,8 +905,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_st32(ta, v);
                     }
                 }
-                // P (bf16 pairs) over the first 32 columns of this half's scores
-                tmem_st32(tmem + lane_base + (g & 1) * kKeys + h * 64, w);
+                // P (bf16 pairs) into P buffer g & 1, columns 32 h .. 32 h + 31, once
+                // the P V of tile g - 2 (the buffer's last reader) has completed
+                if (!__all_sync(0xffffffffu, p_free)) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE + (g & 1)],
+                                                           ((g - 2) >> 1) & 1, p.err));
+                    if (!ok) break;
+                }
+                tc_after();
+                tmem_st32(tmem + lane_base + kPCol + (g & 1) * 64 + h * 32, w);
                 // rows of the last staged block that lie beyond the context were
                 // never written: zero their V so 0 * (anything) cannot become NaN.
                 // The half whose keys hold that block does it before its P V.
@@ -908,10 +945,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     fence_async_smem();   // the zeroed V rows, before the P V reads them
                 }
-                // the tile's V has landed before P is published (the issuer checks
-                // P alone; the softmax warps have time to spare for this check)
-                if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_V_FULL + g % kVStages],
-                                                               (g / kVStages) & 1, p.err));
                 tmem_wait_st();
                 tc_before();
                 __syncwarp();
@@ -919,44 +952,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&bars[B_P_FULL + (g & 1)]);
             }
             if (!ok) break;
-            // ---- epilogue: merge the halves, O / l -> out (this thread: dims 64h..64h+63) ----
+            // ---- epilogue: O / l -> out (this thread: dims 64h..64h+63; l is the sum
+            // of both halves' partial sums, taken against the shared running max) ----
             const uint32_t glast = kt + x.n_tiles - 1;
             ok = __all_sync(0xffffffffu,
                             mbar_wait(&bars[B_O_DONE + (glast & 1)], (glast >> 1) & 1, p.err));
             if (!ok) break;
             tc_after();
             // A full unit (every row a query) leaves through its own Q buffer, which
-            // its last Q K^T has finished with (that product was issued before
-            // the P V awaited above), and TMA stores; a partial one writes its
-            // valid rows directly.  Either way the buffer is handed back to the Q
-            // producer at the end.
+            // its last Q K^T has finished with (these warps read that product's
+            // scores), and TMA stores; a partial one writes its valid rows
+            // directly.  Either way the buffer is handed back to the Q producer at
+            // the end.
             const bool staged = x.nt == p.tokens_per_tile;
             const uint32_t qbuf = k % kQBufs;
-            float2* st_set = stat + (k & 1) * 2 * kRows;
-            st_set[h * kRows + r] = make_float2(m, l);
+            float* st_set = stat + (k & 1) * 2 * kRows;
+            st_set[h * kRows + r] = l;
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_STAT]);
             ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_STAT], k & 1, p.err));
             if (!ok) break;
-            const float2 o0 = st_set[r], o1 = st_set[kRows + r];
-            const float M = fmaxf(o0.x, o1.x);
-            const float a0 = ex2_approx(o0.x - M), a1 = ex2_approx(o1.x - M);
-            const float inv = 1.f / (o0.y * a0 + o1.y * a1);
-            const float w0 = a0 * inv, w1 = a1 * inv;
+            const float inv = 1.f / (st_set[r] + st_set[kRows + r]);
             // this thread's 64 output dims (bf16 pairs): chunk c = dims 8c .. 8c + 7
             uint32_t packed[32];
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) {
-                uint32_t v0[32], v1[32];
-                tmem_ld32(tmem + lane_base + kOCol + h * 64 + c2 * 32, v0);
-                tmem_ld32(tmem + lane_base + kOCol + 128 + h * 64 + c2 * 32, v1);
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + kOCol + h * 64 + c2 * 32, v);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
-                    packed[c2 * 16 + i] =
-                        pack_bf16(__uint_as_float(v0[2 * i]) * w0 + __uint_as_float(v1[2 * i]) * w1,
-                                  __uint_as_float(v0[2 * i + 1]) * w0 +
-                                      __uint_as_float(v1[2 * i + 1]) * w1);
+                    packed[c2 * 16 + i] = pack_bf16(__uint_as_float(v[2 * i]) * inv,
+                                                    __uint_as_float(v[2 * i + 1]) * inv);
             }
             // O has been read: the next unit's first P V may overwrite it
             tc_before();
