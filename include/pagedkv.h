@@ -433,13 +433,16 @@ PKV_API int paged_attention_varlen_window(void* out, const void* q, const void* 
  *   code[d] = clamp(rint(x[d] / scale), -127, 127)     (code = 0 when amax = 0)
  * with both divisions rounded once in fp32 (ties to even), so the stored codes
  * and scales are reproducible bit for bit.  A value reads back as code * scale.
- * Pools (desc->dtype = PKV_INT8; block_size 16; head_dim 64 or 128):
- *   k_pool, v_pool: device bytes, 16-byte aligned, one tile of
- *                   PKV_INT8_TILE_BYTES(head_dim) = 16 * head_dim + 64 bytes
- *                   per (block, kv head), tiles ordered [num_blocks][num_kv_heads]
+ * Pool (desc->dtype = PKV_INT8; block_size 16; head_dim 64 or 128):
+ *   kv_pool: device bytes, 16-byte aligned, owned by the caller, ordered
+ *            [num_blocks][num_kv_heads][2][PKV_INT8_TILE_BYTES(head_dim)]:
+ *            per (block, kv head) its K tile and then its V tile, each of
+ *            PKV_INT8_TILE_BYTES(head_dim) = 16 * head_dim + 64 bytes
+ *            (PKV_INT8_POOL_BYTES(num_blocks, num_kv_heads, head_dim) in all)
  * A tile holds the codes of its 16 token rows (bytes 0 .. 16 * head_dim - 1)
  * and then their 16 fp32 scales (scale of row r at byte 16 * head_dim + 4 r),
- * so the decode reads a (block, kv head) in one contiguous run.  Inside the
+ * so the decode reads a (block, kv head)'s K and V in one contiguous run of
+ * 2 * PKV_INT8_TILE_BYTES(head_dim) bytes.  Inside the
  * codes, the code of token row r (slot % 16) and dimension d is stored at
  *   K: r * head_dim + 16 * ((d / 16) ^ sw(r)) + d % 16,
  *      sw(r) = r & 7 (head_dim 128) or (r >> 1) & 3 (head_dim 64)
@@ -451,27 +454,30 @@ PKV_API int paged_attention_varlen_window(void* out, const void* q, const void* 
  * written through slot_mapping as paged_kv_append writes (negative slot skips;
  * slot >= num_blocks * block_size sets PKV_DEV_BAD_SLOT and is skipped). */
 #define PKV_INT8_TILE_BYTES(head_dim) (16 * (head_dim) + 64)
+#define PKV_INT8_POOL_BYTES(num_blocks, num_kv_heads, head_dim) \
+    ((size_t)(num_blocks) * (size_t)(num_kv_heads) * 2u * (size_t)PKV_INT8_TILE_BYTES(head_dim))
 
 PKV_API int paged_kv_append_int8(const void* k, const void* v, const int64_t* slot_mapping,
-                                 int32_t num_tokens, void* k_pool, void* v_pool,
-                                 const pkv_cache_desc* desc, void* stream);
+                                 int32_t num_tokens, void* kv_pool, const pkv_cache_desc* desc,
+                                 void* stream);
 
 /* Copy-on-write for an 8-bit cache: for each (src, dst) pair, the tiles of
- * block src (every kv head: codes and scales) are copied to block dst, as
- * pkv_copy_blocks does for the other caches.  block_pairs: device int32
+ * block src (every kv head's K and V tiles, codes and scales: one contiguous
+ * run per block) are copied to block dst, as pkv_copy_blocks does for the
+ * other caches.  block_pairs: device int32
  * [num_pairs][2]; an id outside [0, num_blocks) sets PKV_DEV_BAD_COPY_PAIR and
  * that pair is skipped.  desc->block_size must be 16 (the tile has 16 rows;
  * PKV_ERR_UNSUPPORTED otherwise). */
-PKV_API int pkv_copy_blocks_int8(const int32_t* block_pairs, int32_t num_pairs, void* k_pool,
-                                 void* v_pool, const pkv_cache_desc* desc, void* stream);
+PKV_API int pkv_copy_blocks_int8(const int32_t* block_pairs, int32_t num_pairs, void* kv_pool,
+                                 const pkv_cache_desc* desc, void* stream);
 
 /* Decode attention over the 8-bit cache: exactly the attention of
  * paged_attention_decode over the dequantised keys and values (code * scale),
  * computed with the same splits and merge.  q, out: device bf16
  * [num_seqs][num_q_heads][head_dim].  workspace: >= pkv_decode_workspace_bytes
  * of the same desc.  Other arguments and errors as for paged_attention_decode. */
-PKV_API int paged_attention_decode_int8(void* out, const void* q, const void* k_pool,
-                                        const void* v_pool, const pkv_cache_desc* desc,
+PKV_API int paged_attention_decode_int8(void* out, const void* q, const void* kv_pool,
+                                        const pkv_cache_desc* desc,
                                         const int32_t* block_tables, int32_t max_blocks_per_seq,
                                         const int32_t* context_lens, int32_t num_seqs,
                                         int32_t max_context_len, float scale, void* workspace,

@@ -119,10 +119,10 @@ def lib():
         "pkv_device_error": (ctypes.c_int, [P(i32), i32]),
         "pkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "pkv_splitfuse_compose": (ctypes.c_int, [i32, i32, i32, p, p, P(i32), P(i32)]),
-        "paged_kv_append_int8": (ctypes.c_int, [p, p, p, i32, p, p, P(CacheDesc), p]),
-        "pkv_copy_blocks_int8": (ctypes.c_int, [p, i32, p, p, P(CacheDesc), p]),
-        "paged_attention_decode_int8": (ctypes.c_int, [p, p, p, p, P(CacheDesc), p, i32, p,
-                                                       i32, i32, ctypes.c_float, p, sz, p]),
+        "paged_kv_append_int8": (ctypes.c_int, [p, p, p, i32, p, P(CacheDesc), p]),
+        "pkv_copy_blocks_int8": (ctypes.c_int, [p, i32, p, P(CacheDesc), p]),
+        "paged_attention_decode_int8": (ctypes.c_int, [p, p, p, P(CacheDesc), p, i32, p, i32,
+                                                       i32, ctypes.c_float, p, sz, p]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -559,19 +559,21 @@ def int8_tile_bytes(head_dim, block_size=16):
 
 
 class Int8Cache:
-    """The two pools of an 8-bit KV cache, K and V: uint8 [NB, Hkv, tile], one
-    tile per (block, KV head) holding its bs x D codes and then their bs fp32
-    scales (see paged_kv_append_int8 in include/pagedkv.h for the format).
-    k_codes / v_codes (int8 [NB, Hkv, bs, D]) and k_scales / v_scales (fp32
-    [NB, Hkv, bs]) are views into the pools."""
+    """The pool of an 8-bit KV cache: uint8 [NB, Hkv, 2, tile], per (block, KV
+    head) a K tile and then a V tile, each holding its bs x D codes and then
+    their bs fp32 scales (see paged_kv_append_int8 in include/pagedkv.h for the
+    format).  k_pool / v_pool (uint8 [NB, Hkv, tile]), k_codes / v_codes (int8
+    [NB, Hkv, bs, D]) and k_scales / v_scales (fp32 [NB, Hkv, bs]) are views
+    into it."""
 
     def __init__(self, num_blocks, num_kv_heads, block_size, head_dim, num_q_heads,
                  device="cuda"):
         tile = int8_tile_bytes(head_dim, block_size)
         ncode = block_size * head_dim
-        self.k_pool = torch.zeros((num_blocks, num_kv_heads, tile), dtype=torch.uint8,
-                                  device=device)
-        self.v_pool = torch.zeros_like(self.k_pool)
+        self.kv_pool = torch.zeros((num_blocks, num_kv_heads, 2, tile), dtype=torch.uint8,
+                                   device=device)
+        self.k_pool = self.kv_pool[:, :, 0]
+        self.v_pool = self.kv_pool[:, :, 1]
         self.k_codes, self.k_scales = self._views(self.k_pool, ncode, block_size, head_dim)
         self.v_codes, self.v_scales = self._views(self.v_pool, ncode, block_size, head_dim)
         self.desc = CacheDesc(PKV_INT8, num_blocks, block_size, num_kv_heads, num_q_heads,
@@ -584,16 +586,15 @@ class Int8Cache:
         return codes, scales
 
     def tensors(self):
-        return self.k_pool, self.v_pool
+        return (self.kv_pool,)
 
 
 def _need_int8_cache(c):
     d = c.desc
-    shape = (d.num_blocks, d.num_kv_heads, int8_tile_bytes(d.head_dim, d.block_size))
-    for t, nm in ((c.k_pool, "k_pool"), (c.v_pool, "v_pool")):
-        _need(t, torch.uint8, nm)
-        if tuple(t.shape) != shape:
-            raise ValueError(f"{nm}: shape {tuple(t.shape)}, expected {shape}")
+    shape = (d.num_blocks, d.num_kv_heads, 2, int8_tile_bytes(d.head_dim, d.block_size))
+    _need(c.kv_pool, torch.uint8, "kv_pool")
+    if tuple(c.kv_pool.shape) != shape:
+        raise ValueError(f"kv_pool: shape {tuple(c.kv_pool.shape)}, expected {shape}")
 
 
 def paged_kv_append_int8(k, v, slot_mapping, cache, stream=None):
@@ -604,10 +605,9 @@ def paged_kv_append_int8(k, v, slot_mapping, cache, stream=None):
     _need(slot_mapping, torch.int64, "slot_mapping")
     _need_int8_cache(cache)
     st = _stream_on_device(stream, ("k", k), ("v", v), ("slot_mapping", slot_mapping),
-                           ("k_pool", cache.k_pool), ("v_pool", cache.v_pool))
+                           ("kv_pool", cache.kv_pool))
     _check(lib().paged_kv_append_int8(_ptr(k), _ptr(v), _ptr(slot_mapping), k.shape[0],
-                                      _ptr(cache.k_pool), _ptr(cache.v_pool),
-                                      ctypes.byref(cache.desc), st),
+                                      _ptr(cache.kv_pool), ctypes.byref(cache.desc), st),
            "paged_kv_append_int8")
 
 
@@ -618,11 +618,9 @@ def pkv_copy_blocks_int8(block_pairs, cache, stream=None):
         return
     _need(block_pairs, torch.int32, "block_pairs")
     _need_int8_cache(cache)
-    st = _stream_on_device(stream, ("block_pairs", block_pairs), ("k_pool", cache.k_pool),
-                           ("v_pool", cache.v_pool))
-    _check(lib().pkv_copy_blocks_int8(_ptr(block_pairs), n, _ptr(cache.k_pool),
-                                      _ptr(cache.v_pool), ctypes.byref(cache.desc),
-                                      st), "pkv_copy_blocks_int8")
+    st = _stream_on_device(stream, ("block_pairs", block_pairs), ("kv_pool", cache.kv_pool))
+    _check(lib().pkv_copy_blocks_int8(_ptr(block_pairs), n, _ptr(cache.kv_pool),
+                                      ctypes.byref(cache.desc), st), "pkv_copy_blocks_int8")
 
 
 def paged_attention_decode_int8(out, q, cache, block_tables, context_lens, max_context_len,
@@ -637,13 +635,13 @@ def paged_attention_decode_int8(out, q, cache, block_tables, context_lens, max_c
     desc = cache.desc
     if scale is None:
         scale = 1.0 / math.sqrt(desc.head_dim)
-    st = _stream_on_device(stream, ("out", out), ("q", q), ("k_pool", cache.k_pool),
-                           ("v_pool", cache.v_pool), ("block_tables", block_tables),
-                           ("context_lens", context_lens), ("ws", ws))
+    st = _stream_on_device(stream, ("out", out), ("q", q), ("kv_pool", cache.kv_pool),
+                           ("block_tables", block_tables), ("context_lens", context_lens),
+                           ("ws", ws))
     if ws is None:
         ws = workspace(decode_workspace_bytes(desc, S, max_context_len), q.device)
-    _check(lib().paged_attention_decode_int8(_ptr(out), _ptr(q), _ptr(cache.k_pool),
-                                             _ptr(cache.v_pool), ctypes.byref(desc),
+    _check(lib().paged_attention_decode_int8(_ptr(out), _ptr(q), _ptr(cache.kv_pool),
+                                             ctypes.byref(desc),
                                              _ptr(block_tables), block_tables.shape[1],
                                              _ptr(context_lens), S, max_context_len, scale,
                                              _ptr(ws), ws.numel(), st),

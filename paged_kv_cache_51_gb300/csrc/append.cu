@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
 struct CopyParams {
     const int32_t* pairs;
     uint4* k_cache;
-    uint4* v_cache;
+    uint4* v_cache;           // null: k_cache is one pool holding both
     int64_t vec_per_block;    // 16-byte vectors per physical block (all heads)
     int32_t num_blocks;
     int* err;
@@ -108,13 +108,19 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(CopyParams p) {
         return;
     }
     const uint4* ks = p.k_cache + int64_t(src) * p.vec_per_block;
-    const uint4* vs = p.v_cache + int64_t(src) * p.vec_per_block;
     uint4* kd = p.k_cache + int64_t(dst) * p.vec_per_block;
-    uint4* vd = p.v_cache + int64_t(dst) * p.vec_per_block;
-    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < p.vec_per_block;
-         i += int64_t(gridDim.x) * blockDim.x) {
-        kd[i] = ks[i];
-        vd[i] = vs[i];
+    if (p.v_cache) {
+        const uint4* vs = p.v_cache + int64_t(src) * p.vec_per_block;
+        uint4* vd = p.v_cache + int64_t(dst) * p.vec_per_block;
+        for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < p.vec_per_block;
+             i += int64_t(gridDim.x) * blockDim.x) {
+            kd[i] = ks[i];
+            vd[i] = vs[i];
+        }
+    } else {   // one pool (the 8-bit cache: K and V tiles of a block side by side)
+        for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < p.vec_per_block;
+             i += int64_t(gridDim.x) * blockDim.x)
+            kd[i] = ks[i];
     }
 }
 
@@ -426,8 +432,8 @@ extern "C" int pkv_copy_blocks(const int32_t* block_pairs, int32_t num_pairs, vo
                                   static_cast<cudaStream_t>(stream), p));
 }
 
-extern "C" int pkv_copy_blocks_int8(const int32_t* block_pairs, int32_t num_pairs, void* k_pool,
-                                    void* v_pool, const pkv_cache_desc* desc, void* stream) {
+extern "C" int pkv_copy_blocks_int8(const int32_t* block_pairs, int32_t num_pairs, void* kv_pool,
+                                    const pkv_cache_desc* desc, void* stream) {
     if (!desc) return PKV_ERR_INVALID;
     if (desc->dtype != PKV_INT8) return PKV_ERR_UNSUPPORTED;
     pkv_cache_desc bd = *desc;
@@ -438,19 +444,19 @@ extern "C" int pkv_copy_blocks_int8(const int32_t* block_pairs, int32_t num_pair
     if (num_pairs < 0) return PKV_ERR_INVALID;
     if (num_pairs == 0) return PKV_OK;
     if (num_pairs > 65535) return PKV_ERR_UNSUPPORTED;
-    if (!block_pairs || !k_pool || !v_pool || !aligned16(k_pool) || !aligned16(v_pool) ||
+    if (!block_pairs || !kv_pool || !aligned16(kv_pool) ||
         (reinterpret_cast<uintptr_t>(block_pairs) & 3u))
         return PKV_ERR_INVALID;
-    // whole blocks as bytes: every KV head's tile of codes and scales
+    // whole blocks as bytes: every KV head's K and V tiles of codes and scales
     const int64_t tile_bytes = int64_t(desc->block_size) * desc->head_dim + desc->block_size * 4;
-    const int64_t block_bytes = int64_t(desc->num_kv_heads) * tile_bytes;
+    const int64_t block_bytes = int64_t(desc->num_kv_heads) * 2 * tile_bytes;
     if (block_bytes % 16) return PKV_ERR_UNSUPPORTED;
     int* err = device_error_ptr(&st);
     if (st != PKV_OK) return st;
     CopyParams p;
     p.pairs = block_pairs;
-    p.k_cache = static_cast<uint4*>(k_pool);
-    p.v_cache = static_cast<uint4*>(v_pool);
+    p.k_cache = static_cast<uint4*>(kv_pool);
+    p.v_cache = nullptr;
     p.vec_per_block = block_bytes / 16;
     p.num_blocks = desc->num_blocks;
     p.err = err;

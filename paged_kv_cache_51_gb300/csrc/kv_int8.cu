@@ -7,10 +7,13 @@
 // (code = 0, scale = 0 for an all-zero row), each division rounded once in
 // fp32, so the stored codes are reproducible exactly.
 //
-// Tile layout.  One (block, KV head) tile holds 16 tokens: their 16 * D codes,
-// then their 16 fp32 scales, in one contiguous run of 16 * D + 64 bytes, so a
-// decode stage is one bulk copy for K and one for V (the scales as separate
-// 64-byte copies cost 13 % of the call).  K codes are row-major [token][D] with
+// Pool layout.  One tile holds 16 tokens of one KV head: their 16 * D codes,
+// then their 16 fp32 scales (16 * D + 64 bytes).  The pool holds, per (block,
+// KV head), the K tile and then the V tile, so a decode stage is one bulk copy
+// of 2 * (16 * D + 64) contiguous bytes: the scales as separate 64-byte copies
+// cost 13 % of the call, and K and V as two 2112-byte copies from separate
+// pools 6 % more than one 4224-byte run (scattered reads of 2 KB runs keep
+// the DRAM less busy than reads of 4 KB).  K codes are row-major [token][D] with
 // the 16-byte chunks of row r XOR-swizzled (chunk c stored at c ^ sw(r),
 // sw(r) = r & 7 for D = 128 and (r >> 1) & 3 for D = 64); V codes are
 // dim-major [D][token].  Both code layouts let a warp load its tensor-core
@@ -64,8 +67,7 @@ struct AppendI8Params {
     const __nv_bfloat16* k;
     const __nv_bfloat16* v;
     const int64_t* slots;
-    unsigned char* k_pool;
-    unsigned char* v_pool;
+    unsigned char* kv_pool;
     int64_t num_tokens;
     int32_t num_kv_heads;
     int32_t block_size;
@@ -118,7 +120,7 @@ __global__ void __launch_bounds__(256) append_int8_kernel(AppendI8Params p) {
         const int64_t blk = slot / p.block_size;
         const int rr = int(slot - blk * p.block_size);           // token row within the tile
         unsigned char* tile =
-            (is_v ? p.v_pool : p.k_pool) + (blk * p.num_kv_heads + h) * i8_tile_bytes<D>();
+            p.kv_pool + ((blk * p.num_kv_heads + h) * 2 + (is_v ? 1 : 0)) * i8_tile_bytes<D>();
         if (!is_v) {
             // row-major, 16-byte chunk (lane * DPL) / 16 swizzled by the row
             const int d0 = lane * DPL;
@@ -148,8 +150,7 @@ __global__ void __launch_bounds__(256) append_int8_kernel(AppendI8Params p) {
 struct SplitI8Params {
     const __nv_bfloat16* q;
     __nv_bfloat16* out;
-    const unsigned char* k_pool;
-    const unsigned char* v_pool;
+    const unsigned char* kv_pool;
     const int32_t* block_tables;
     const int32_t* context_lens;
     const int2* items;
@@ -304,9 +305,8 @@ __global__ void __launch_bounds__(I8Cfg<D, G>::kThreads, I8Cfg<D, G>::kMinBlocks
                         mbar_arrive_expect_tx(&full[st], C::kStageBytes);
                         const size_t row = size_t(blk) * Hkv + kvh;
                         unsigned char* dst = smem + size_t(st) * C::kStageBytes;
-                        bulk_g2s(dst, p.k_pool + row * C::kTileBytes, C::kTileBytes, &full[st]);
-                        bulk_g2s(dst + C::kTileBytes, p.v_pool + row * C::kTileBytes,
-                                 C::kTileBytes, &full[st]);
+                        // the (block, head) unit: K tile then V tile, one run
+                        bulk_g2s(dst, p.kv_pool + row * C::kStageBytes, C::kStageBytes, &full[st]);
                     }
                 }
                 __syncwarp();
@@ -536,7 +536,7 @@ __global__ void __launch_bounds__(I8Cfg<D, G>::kThreads, I8Cfg<D, G>::kMinBlocks
 bool aligned(const void* q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) & (a - 1)) == 0; }
 
 template <int D, int G>
-int launch_i8(const AttnArgs& a, const unsigned char* kp, const unsigned char* vp) {
+int launch_i8(const AttnArgs& a, const unsigned char* kvp) {
     using C = I8Cfg<D, G>;
     auto kern = decode_split_int8_kernel<D, G>;
     const int per_sm = kernel_occupancy<decode_split_int8_kernel<D, G>>(C::kThreads, C::kSmem);
@@ -547,8 +547,7 @@ int launch_i8(const AttnArgs& a, const unsigned char* kp, const unsigned char* v
     SplitI8Params p;
     p.q = static_cast<const __nv_bfloat16*>(a.q);
     p.out = static_cast<__nv_bfloat16*>(a.out);
-    p.k_pool = kp;
-    p.v_pool = vp;
+    p.kv_pool = kvp;
     p.block_tables = a.block_tables;
     p.context_lens = a.context_lens;
     p.items = a.ws.items;
@@ -577,12 +576,12 @@ int launch_i8(const AttnArgs& a, const unsigned char* kp, const unsigned char* v
 }
 
 template <int D>
-int launch_i8_d(const AttnArgs& a, int g, const unsigned char* kp, const unsigned char* vp) {
+int launch_i8_d(const AttnArgs& a, int g, const unsigned char* kvp) {
     switch (g) {
-        case 1: return launch_i8<D, 1>(a, kp, vp);
-        case 2: return launch_i8<D, 2>(a, kp, vp);
-        case 4: return launch_i8<D, 4>(a, kp, vp);
-        case 8: return launch_i8<D, 8>(a, kp, vp);
+        case 1: return launch_i8<D, 1>(a, kvp);
+        case 2: return launch_i8<D, 2>(a, kvp);
+        case 4: return launch_i8<D, 4>(a, kvp);
+        case 8: return launch_i8<D, 8>(a, kvp);
         default: return PKV_ERR_UNSUPPORTED;
     }
 }
@@ -593,7 +592,7 @@ int launch_i8_d(const AttnArgs& a, int g, const unsigned char* kp, const unsigne
 using namespace pkv;
 
 extern "C" int paged_kv_append_int8(const void* k, const void* v, const int64_t* slot_mapping,
-                                    int32_t num_tokens, void* k_pool, void* v_pool,
+                                    int32_t num_tokens, void* kv_pool,
                                     const pkv_cache_desc* desc, void* stream) {
     if (!desc) return PKV_ERR_INVALID;
     if (desc->dtype != PKV_INT8) return PKV_ERR_UNSUPPORTED;
@@ -605,9 +604,8 @@ extern "C" int paged_kv_append_int8(const void* k, const void* v, const int64_t*
     if (desc->block_size != kBlockTokens) return PKV_ERR_UNSUPPORTED;   // the tile layout is 16 rows
     if (num_tokens < 0) return PKV_ERR_INVALID;
     if (num_tokens == 0) return PKV_OK;
-    if (!k || !v || !slot_mapping || !k_pool || !v_pool) return PKV_ERR_INVALID;
-    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
-        !aligned(slot_mapping, 8))
+    if (!k || !v || !slot_mapping || !kv_pool) return PKV_ERR_INVALID;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(kv_pool, 16) || !aligned(slot_mapping, 8))
         return PKV_ERR_INVALID;
     int* err = device_error_ptr(&st);
     if (st != PKV_OK) return st;
@@ -615,8 +613,7 @@ extern "C" int paged_kv_append_int8(const void* k, const void* v, const int64_t*
     p.k = static_cast<const __nv_bfloat16*>(k);
     p.v = static_cast<const __nv_bfloat16*>(v);
     p.slots = slot_mapping;
-    p.k_pool = static_cast<unsigned char*>(k_pool);
-    p.v_pool = static_cast<unsigned char*>(v_pool);
+    p.kv_pool = static_cast<unsigned char*>(kv_pool);
     p.num_tokens = num_tokens;
     p.num_kv_heads = desc->num_kv_heads;
     p.block_size = desc->block_size;
@@ -632,8 +629,8 @@ extern "C" int paged_kv_append_int8(const void* k, const void* v, const int64_t*
     return cuda_status(cudaGetLastError());
 }
 
-extern "C" int paged_attention_decode_int8(void* out, const void* q, const void* k_pool,
-                                           const void* v_pool, const pkv_cache_desc* desc,
+extern "C" int paged_attention_decode_int8(void* out, const void* q, const void* kv_pool,
+                                           const pkv_cache_desc* desc,
                                            const int32_t* block_tables, int32_t max_blocks_per_seq,
                                            const int32_t* context_lens, int32_t num_seqs,
                                            int32_t max_context_len, float scale, void* workspace,
@@ -648,8 +645,8 @@ extern "C" int paged_attention_decode_int8(void* out, const void* q, const void*
     if (num_seqs < 0 || max_blocks_per_seq < 1 || max_context_len < 1) return PKV_ERR_INVALID;
     if (!std::isfinite(scale)) return PKV_ERR_INVALID;
     if (num_seqs == 0) return PKV_OK;
-    if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens) return PKV_ERR_INVALID;
-    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+    if (!out || !q || !kv_pool || !block_tables || !context_lens) return PKV_ERR_INVALID;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(kv_pool, 16) ||
         !aligned(block_tables, 4) || !aligned(context_lens, 4))
         return PKV_ERR_INVALID;
     const size_t need = pkv_decode_workspace_bytes(&qd, num_seqs, max_context_len);
@@ -672,9 +669,8 @@ extern "C" int paged_attention_decode_int8(void* out, const void* q, const void*
     a.stream = static_cast<cudaStream_t>(stream);
     if ((st = launch_plan(a)) != PKV_OK) return st;
     const int g = qd.num_q_heads / qd.num_kv_heads;
-    const auto* kp = static_cast<const unsigned char*>(k_pool);
-    const auto* vp = static_cast<const unsigned char*>(v_pool);
-    st = qd.head_dim == 128 ? launch_i8_d<128>(a, g, kp, vp) : launch_i8_d<64>(a, g, kp, vp);
+    const auto* kvp = static_cast<const unsigned char*>(kv_pool);
+    st = qd.head_dim == 128 ? launch_i8_d<128>(a, g, kvp) : launch_i8_d<64>(a, g, kvp);
     if (st != PKV_OK) return st;
     return launch_decode_merge(a);
 }

@@ -194,9 +194,9 @@ def test_int8_entry_points_validate_on_the_host(lib):
     # a tile is the 16 rows' codes and then their fp32 scales
     assert lib.int8_tile_bytes(128) == 16 * 128 + 64 and lib.int8_tile_bytes(64) == 1088
     # the 8-bit calls take only PKV_INT8, the others never take it
-    assert L.paged_kv_append_int8(fake, fake, fake, 4, fake, fake, ref(bf),
+    assert L.paged_kv_append_int8(fake, fake, fake, 4, fake, ref(bf),
                                   None) == lib.PKV_ERR_UNSUPPORTED
-    assert L.paged_attention_decode_int8(fake, fake, fake, fake, ref(bf), fake, 4,
+    assert L.paged_attention_decode_int8(fake, fake, fake, ref(bf), fake, 4,
                                          fake, 1, 16, 0.1, fake, 1 << 20,
                                          None) == lib.PKV_ERR_UNSUPPORTED
     assert L.paged_kv_append(fake, fake, fake, 4, fake, fake, ref(i8), None) == \
@@ -204,57 +204,65 @@ def test_int8_entry_points_validate_on_the_host(lib):
     assert L.paged_attention_decode(fake, fake, fake, fake, ref(i8), fake, 4, fake, 1, 16, 0.1,
                                     fake, 1 << 20, None) == lib.PKV_ERR_UNSUPPORTED
     # null pointers, a misaligned pool, head_dim, workspace, empty work
-    assert L.paged_kv_append_int8(None, fake, fake, 4, fake, fake, ref(i8),
+    assert L.paged_kv_append_int8(None, fake, fake, 4, fake, ref(i8),
                                   None) == lib.PKV_ERR_INVALID
-    assert L.paged_kv_append_int8(fake, fake, fake, 4, fake, None, ref(i8),
+    assert L.paged_kv_append_int8(fake, fake, fake, 4, None, ref(i8),
                                   None) == lib.PKV_ERR_INVALID
-    assert L.paged_kv_append_int8(fake, fake, fake, 4, ctypes.c_void_p((1 << 20) + 4), fake,
+    assert L.paged_kv_append_int8(fake, fake, fake, 4, ctypes.c_void_p((1 << 20) + 4),
                                   ref(i8), None) == lib.PKV_ERR_INVALID
-    assert L.paged_attention_decode_int8(fake, fake, fake, ctypes.c_void_p((1 << 20) + 8),
+    assert L.paged_attention_decode_int8(fake, fake, ctypes.c_void_p((1 << 20) + 8),
                                          ref(i8), fake, 4, fake, 1, 16, 0.1, fake, 1 << 20,
                                          None) == lib.PKV_ERR_INVALID
+    assert L.paged_attention_decode_int8(fake, fake, None, ref(i8), fake, 4, fake, 1, 16, 0.1,
+                                         fake, 1 << 20, None) == lib.PKV_ERR_INVALID
     d96 = lib.CacheDesc(lib.PKV_INT8, 100, 16, 8, 32, 96)
-    assert L.paged_kv_append_int8(fake, fake, fake, 4, fake, fake, ref(d96),
+    assert L.paged_kv_append_int8(fake, fake, fake, 4, fake, ref(d96),
                                   None) == lib.PKV_ERR_UNSUPPORTED
-    assert L.paged_attention_decode_int8(fake, fake, fake, fake, ref(i8), fake, 4,
+    assert L.paged_attention_decode_int8(fake, fake, fake, ref(i8), fake, 4,
                                          fake, 64, 4096, 0.1, fake, 256,
                                          None) == lib.PKV_ERR_WORKSPACE
-    assert L.paged_attention_decode_int8(fake, fake, fake, fake, ref(i8), fake, 4,
+    assert L.paged_attention_decode_int8(fake, fake, fake, ref(i8), fake, 4,
                                          fake, 1, 16, float("nan"), fake, 1 << 20,
                                          None) == lib.PKV_ERR_INVALID
-    assert L.paged_kv_append_int8(None, None, None, 0, None, None, ref(i8), None) == 0
+    assert L.paged_kv_append_int8(None, None, None, 0, None, ref(i8), None) == 0
     # copy-on-write for the 8-bit cache takes only PKV_INT8, with 16-row tiles
-    assert L.pkv_copy_blocks_int8(fake, 2, fake, fake, ref(bf), None) == \
+    assert L.pkv_copy_blocks_int8(fake, 2, fake, ref(bf), None) == \
         lib.PKV_ERR_UNSUPPORTED
     b8 = lib.CacheDesc(lib.PKV_INT8, 100, 8, 8, 32, 128)
-    assert L.pkv_copy_blocks_int8(fake, 2, fake, fake, ref(b8), None) == \
+    assert L.pkv_copy_blocks_int8(fake, 2, fake, ref(b8), None) == \
         lib.PKV_ERR_UNSUPPORTED
-    assert L.pkv_copy_blocks_int8(None, 2, fake, fake, ref(i8), None) == \
+    assert L.pkv_copy_blocks_int8(None, 2, fake, ref(i8), None) == \
         lib.PKV_ERR_INVALID
-    assert L.pkv_copy_blocks_int8(None, 0, None, None, ref(i8), None) == 0
+    assert L.pkv_copy_blocks_int8(fake, 2, ctypes.c_void_p((1 << 20) + 4), ref(i8), None) == \
+        lib.PKV_ERR_INVALID
+    assert L.pkv_copy_blocks_int8(None, 0, None, ref(i8), None) == 0
 
 
 def test_int8_cache_views_follow_the_tile_layout(lib):
-    """The binding's code and scale views alias the fused pools as the header
-    lays a tile out: 16 rows of codes, then the 16 rows' fp32 scales."""
+    """The binding's code and scale views alias the one pool as the header lays
+    it out: per (block, KV head) the K tile and then the V tile, each 16 rows of
+    codes and then the 16 rows' fp32 scales."""
     import numpy as np
     import torch
 
     for d in (128, 64):
         c = lib.Int8Cache(3, 2, 16, d, 4, device="cpu")
         tile = lib.int8_tile_bytes(d)
+        assert tuple(c.kv_pool.shape) == (3, 2, 2, tile) and c.kv_pool.dtype == torch.uint8
+        assert c.kv_pool.is_contiguous()
         assert tuple(c.k_pool.shape) == (3, 2, tile) and c.k_pool.dtype == torch.uint8
         assert tuple(c.k_codes.shape) == (3, 2, 16, d) and c.k_codes.dtype == torch.int8
         assert tuple(c.v_scales.shape) == (3, 2, 16) and c.v_scales.dtype == torch.float32
         c.k_codes[2, 1, 5, 7] = -3
         c.v_scales[1, 0, 9] = 0.25
-        kb = c.k_pool.numpy()
-        vb = c.v_pool.numpy()
-        assert kb[2, 1, 5 * d + 7].view(np.int8) == -3
-        assert vb[1, 0, 16 * d + 4 * 9:16 * d + 4 * 10].view(np.float32)[0] == 0.25
-        assert np.count_nonzero(kb) == 1 and np.count_nonzero(vb) == 2   # 0.25 = 0x3e800000
-        kp, vp = c.tensors()
-        assert kp is c.k_pool and vp is c.v_pool
+        flat = c.kv_pool.numpy().reshape(-1)
+        unit = 2 * tile                                   # one (block, head): K then V
+        assert flat[(2 * 2 + 1) * unit + 5 * d + 7].view(np.int8) == -3
+        at = (1 * 2 + 0) * unit + tile + 16 * d + 4 * 9
+        assert flat[at:at + 4].view(np.float32)[0] == 0.25
+        assert np.count_nonzero(flat) == 3                # -3, and 0.25 = 0x3e800000
+        (kv,) = c.tensors()
+        assert kv is c.kv_pool
 
 
 def test_binding_refuses_values_outside_int32(lib):
