@@ -73,6 +73,8 @@ int main(void) {
     CHECK(pkv_decode_workspace_bytes(&desc, 64, 4096) ==
           pkv_decode_workspace_bytes(&desc, 64, 4096));
     CHECK(PKV_INT8_TILE_BYTES(128) == 2112 && PKV_INT8_TILE_BYTES(64) == 1088);
+    /* the 8-bit pool: per (block, kv head) a K tile and a V tile */
+    CHECK(PKV_INT8_POOL_BYTES(3, 2, 128) == (size_t)3 * 2 * 2 * 2112);
 
     CHECK(pkv_status_string(PKV_OK) != NULL);
     CHECK(pkv_status_string(PKV_ERR_NO_BLOCKS) != NULL &&
