@@ -385,17 +385,23 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
     return r;
 }
 
-// Whether the phase with the given parity has completed, without waiting (a
-// test issued early, whose latency overlaps the work before its result is used).
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
+// A wait's first attempt and another barrier's test in one go, so the two
+// round trips overlap: whether the phase `wpar` of `wbar` has completed (the
+// try may suspend the thread a little while it has not), and in `tested`
+// whether the phase `tpar` of `tbar` has.
+__device__ __forceinline__ bool mbar_try_and_test(uint64_t* wbar, uint32_t wpar, uint64_t* tbar,
+                                                  uint32_t tpar, bool& tested) {
+    uint32_t a, b;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        "{\n .reg .pred pa, pb;\n"
+        " mbarrier.test_wait.parity.shared::cta.b64 pb, [%4], %5;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 pa, [%2], %3;\n"
+        " selp.u32 %0, 1, 0, pa;\n selp.u32 %1, 1, 0, pb;\n}\n"
+        : "=r"(a), "=r"(b)
+        : "r"(smem_u32(wbar)), "r"(wpar), "r"(smem_u32(tbar)), "r"(tpar)
         : "memory");
-    return ok != 0;
+    tested = b != 0;
+    return a != 0;
 }
 
 // Block ids of a unit's key tiles, fetched 4 tiles (32 blocks, one per lane) at
@@ -800,7 +806,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < x.n_tiles; ++j) {
                 const uint32_t g = kt + j;
-                ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_S_FULL + (g & 1)], (g >> 1) & 1, p.err));
+                // S(g), and whether the P V of tile g - 2 (the last reader of P
+                // buffer g & 1) has completed, tested without waiting (it nearly
+                // always has; the bounded wait runs before P is stored only if it
+                // has not)
+                bool p_done;
+                bool s_full = mbar_try_and_test(&bars[B_S_FULL + (g & 1)], (g >> 1) & 1,
+                                                &bars[B_O_DONE + (g & 1)], ((g - 2) >> 1) & 1, p_done);
+                if (!s_full) s_full = mbar_wait(&bars[B_S_FULL + (g & 1)], (g >> 1) & 1, p.err);
+                ok = __all_sync(0xffffffffu, s_full);
                 if (!ok) break;
                 tc_after();
                 float s[64];
@@ -815,10 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         s[32 + i] = __uint_as_float(v1[i]);
                     }
                 }
-                // whether the P V of tile g - 2 (the last reader of P buffer g & 1)
-                // has completed, tested without waiting (it nearly always has); the
-                // bounded wait runs before P is stored only if it has not
-                const bool p_free = g < 2 || mbar_test(&bars[B_O_DONE + (g & 1)], ((g - 2) >> 1) & 1);
+                const bool p_free = g < 2 || p_done;
 
                 // mask keys beyond this row's causal limit and below its window;
                 // max on the raw scores
