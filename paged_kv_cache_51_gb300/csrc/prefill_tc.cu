@@ -19,14 +19,16 @@
 // tensor cores:
 //   S = Q K^T   M = 128 query rows, N = 128 keys, K = 128 dims
 //   O += P V    M = 128 query rows, N = 128 dims, K = 128 keys
-// with bf16 operands in shared memory and fp32 accumulators in TMEM.
+// with bf16 operands (Q, K, V in shared memory, P in TMEM) and fp32
+// accumulators in TMEM.
 //
 // Tile shapes.  A tile's 128 rows are 128/G tokens x the G query heads of one
 // KV head (GQA packing, "大模型部署.md" §4.1 4. MQA 与 GQA), so every K/V byte
 // staged is used by all G heads.  A key tile is 8 paged blocks (128 keys).
-// Operands use the 128-byte-swizzled K-major layout (Q, K, P) and the 128-byte
-// swizzled MN-major layout (V); TMA tensor copies write K and V blocks straight
-// into that layout, one (block, 64-dim half) box of 16 x 128 B per copy.
+// Shared-memory operands use the 128-byte-swizzled K-major layout (Q, K) and
+// the 128-byte swizzled MN-major layout (V); TMA tensor copies write K and V
+// blocks straight into that layout, one (block, 64-dim half) box of 16 x 128 B
+// per copy.
 //
 // Warp roles (384 threads, one CTA per SM, persistent over work units):
 //   warps 0-7  softmax: two threads per query row, one per 64-key half of each
@@ -69,8 +71,8 @@
 //              products go out from two sub-partitions (2 and 3), each carrying
 //              half the issue work.  Tensor-core instructions of one thread run
 //              in issue order, but two threads' need not: a Q K^T into an S
-//              buffer waits until the scores it replaces (two tiles
-//              earlier) has been loaded by the softmax.  The pipe works on
+//              buffer waits until the softmax has loaded the scores it
+//              replaces (two tiles earlier).  The pipe works on
 //              Q K^T of tile q + 1 and P V of tile q - 1 while the softmax runs
 //              on tile q (across units as well).
 // Every wait is bounded; on a timeout the kernel records an error, stops
