@@ -37,7 +37,8 @@
  *     recorded in the device error word (read it with pkv_device_error).
  *   - Cache layout (fixed): K and V are separate pools, each
  *     [num_blocks][num_kv_heads][block_size][head_dim], row-major, in the
- *     cache dtype.  One (block, kv head) tile is contiguous.
+ *     cache dtype.  One (block, kv head) tile is contiguous.  The 8-bit cache
+ *     (PKV_INT8) is one pool instead, laid out with the *_int8 entry points.
  *   - Query head h uses KV head h / (num_q_heads / num_kv_heads).
  */
 #ifndef PAGEDKV_H
@@ -85,7 +86,8 @@ extern "C" {
 typedef struct pkv_cache_desc {
     int32_t dtype;        /* PKV_F32 or PKV_BF16: cache, q, k, v and out share it;
                              PKV_INT8: only the *_int8 entry points take it */
-    int32_t num_blocks;   /* physical blocks in each of the K and V pools */
+    int32_t num_blocks;   /* physical blocks in each of the K and V pools (in the
+                             one pool of an 8-bit cache) */
     int32_t block_size;   /* tokens per block (the kernels implement 16) */
     int32_t num_kv_heads;
     int32_t num_q_heads;  /* multiple of num_kv_heads; group size 1, 2, 4 or 8 */
